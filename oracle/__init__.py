@@ -1,0 +1,168 @@
+"""CPU oracle for the MoE expert-parallel layout / dispatch / combine path.
+
+TEST INFRASTRUCTURE ONLY.  Only the tests, the smoke check and the benchmark's
+CPU-baseline leg may import this package.  The product library never calls it
+and shares no code with it; the CUDA path fails loudly when its own extension
+is missing instead of falling back here.
+
+The arithmetic lives in plain C (ep_oracle.c, single-threaded, no fast-math,
+no contraction).  This module only marshals numpy arrays into it.  bf16 values
+travel as their uint16 bit patterns, e4m3 values as uint8 codes.
+
+Parity status: every routine here is pinned by the CPU tests in
+tests/test_oracle_*.py (brute force on tiny inputs, an independent stable-sort
+formulation, invariants, exhaustive e4m3 checks against torch's float8_e4m3fn
+cast, closed-form combine cases, error bounds).
+"""
+import ctypes
+import numpy as np
+
+from .build import build_oracle
+
+_lib = None
+
+_i32p = np.ctypeslib.ndpointer(dtype=np.int32, flags="C_CONTIGUOUS")
+_i64p = np.ctypeslib.ndpointer(dtype=np.int64, flags="C_CONTIGUOUS")
+_u16p = np.ctypeslib.ndpointer(dtype=np.uint16, flags="C_CONTIGUOUS")
+_u8p = np.ctypeslib.ndpointer(dtype=np.uint8, flags="C_CONTIGUOUS")
+_f32p = np.ctypeslib.ndpointer(dtype=np.float32, flags="C_CONTIGUOUS")
+_f64p = np.ctypeslib.ndpointer(dtype=np.float64, flags="C_CONTIGUOUS")
+
+
+def lib():
+    """Load (building first if needed) liboracle_ep.so."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    L = ctypes.CDLL(build_oracle())
+    c = ctypes
+    L.oracle_recv_capacity.restype = c.c_int64
+    L.oracle_recv_capacity.argtypes = [c.c_int, c.c_int, c.c_int, c.c_int]
+    L.oracle_layout.restype = c.c_int
+    L.oracle_layout.argtypes = [c.c_int, c.c_int, c.c_int, c.c_int, c.c_int,
+                                _i64p, c.c_int, _i32p, _i32p, _i32p, _i32p,
+                                _i32p, _i32p, c.c_int64, _i32p, _i32p]
+    L.oracle_dispatch_bf16.restype = None
+    L.oracle_dispatch_bf16.argtypes = [c.c_int, c.c_int, c.c_int, _u16p, _i32p, _u16p]
+    L.oracle_dispatch_fp8.restype = None
+    L.oracle_dispatch_fp8.argtypes = [c.c_int, c.c_int, c.c_int, _u16p, _i32p, _u8p, _f32p]
+    L.oracle_quant_fp8_row.restype = None
+    L.oracle_quant_fp8_row.argtypes = [c.c_int, _u16p, _u8p, _f32p]
+    L.oracle_combine.restype = None
+    L.oracle_combine.argtypes = [c.c_int, c.c_int, c.c_int, _u16p, _i32p, c.c_void_p, _u16p]
+    L.oracle_e4m3_encode_array.restype = None
+    L.oracle_e4m3_encode_array.argtypes = [c.c_int64, _f32p, _u8p]
+    L.oracle_e4m3_decode_array.restype = None
+    L.oracle_e4m3_decode_array.argtypes = [c.c_int64, _u8p, _f64p]
+    L.oracle_f32_to_bf16_array.restype = None
+    L.oracle_f32_to_bf16_array.argtypes = [c.c_int64, _f32p, _u16p]
+    _lib = L
+    return L
+
+
+def recv_capacity(max_tokens, topk, num_experts, alignment):
+    """Rows a receive buffer needs for any routing of max_tokens tokens."""
+    return int(lib().oracle_recv_capacity(max_tokens, topk, num_experts, alignment))
+
+
+def layout(topk_idx, world_size, max_tok_per_rank, num_expert_per_rank,
+           alignment, rcap=None):
+    """Layout of topk_idx (int64 [N, K]).  Returns a dict of numpy arrays:
+    cnt [E], tok_per_rank [W], psum_expert [E+1], psum_rank [W+1],
+    dst_slot [N, K], meta [rcap, K+2], num_recv (int), err (int), rcap (int)."""
+    topk_idx = np.ascontiguousarray(topk_idx, dtype=np.int64)
+    N, K = topk_idx.shape
+    W, T, Epr, A = world_size, max_tok_per_rank, num_expert_per_rank, alignment
+    E = W * Epr
+    if rcap is None:
+        rcap = recv_capacity(W * T, K, E, A)
+    out = dict(
+        cnt=np.zeros(E, np.int32), tok_per_rank=np.zeros(W, np.int32),
+        psum_expert=np.zeros(E + 1, np.int32), psum_rank=np.zeros(W + 1, np.int32),
+        dst_slot=np.zeros((N, K), np.int32), meta=np.zeros((rcap, K + 2), np.int32),
+    )
+    num_recv = np.zeros(1, np.int32)
+    err = np.zeros(1, np.int32)
+    rc = lib().oracle_layout(W, T, Epr, K, A, topk_idx.reshape(-1), N,
+                             out["cnt"], out["tok_per_rank"], out["psum_expert"],
+                             out["psum_rank"], out["dst_slot"].reshape(-1),
+                             out["meta"].reshape(-1), rcap, num_recv, err)
+    if rc != 0:
+        raise ValueError("oracle layout: receive capacity exceeded")
+    out["num_recv"] = int(num_recv[0])
+    out["err"] = int(err[0])
+    out["rcap"] = int(rcap)
+    return out
+
+
+def dispatch_bf16(x_bits, dst_slot, recv_x):
+    """recv_x[dst_slot[t, k]] = x[t] in place; x_bits / recv_x are uint16."""
+    N, H = x_bits.shape
+    K = dst_slot.shape[1]
+    assert recv_x.dtype == np.uint16 and recv_x.shape[1] == H and recv_x.flags.c_contiguous
+    lib().oracle_dispatch_bf16(N, H, K, np.ascontiguousarray(x_bits),
+                               np.ascontiguousarray(dst_slot, dtype=np.int32), recv_x)
+    return recv_x
+
+
+def dispatch_fp8(x_bits, dst_slot, recv_x, recv_scales):
+    """FP8 dispatch in place: recv_x uint8 [rows, H], recv_scales fp32 [rows, H/128]."""
+    N, H = x_bits.shape
+    K = dst_slot.shape[1]
+    assert H % 128 == 0
+    assert recv_x.dtype == np.uint8 and recv_x.flags.c_contiguous
+    assert recv_scales.dtype == np.float32 and recv_scales.flags.c_contiguous
+    lib().oracle_dispatch_fp8(N, H, K, np.ascontiguousarray(x_bits),
+                              np.ascontiguousarray(dst_slot, dtype=np.int32),
+                              recv_x, recv_scales)
+    return recv_x, recv_scales
+
+
+def quant_fp8_row(x_row_bits):
+    """Quantise one bf16 row: returns (e4m3 codes uint8 [H], scales fp32 [H/128])."""
+    x_row_bits = np.ascontiguousarray(x_row_bits, dtype=np.uint16)
+    H = x_row_bits.shape[0]
+    q = np.zeros(H, np.uint8)
+    s = np.zeros(H // 128, np.float32)
+    lib().oracle_quant_fp8_row(H, x_row_bits, q, s)
+    return q, s
+
+
+def combine(y_bits, dst_slot, weights=None):
+    """out[t] = bf16(sum_k w[t,k] * y[dst_slot[t,k]]) with the fixed fma order.
+    y_bits uint16 [rows, H]; weights fp32 [N, K] or None. Returns uint16 [N, H]."""
+    dst_slot = np.ascontiguousarray(dst_slot, dtype=np.int32)
+    N, K = dst_slot.shape
+    H = y_bits.shape[1]
+    out = np.zeros((N, H), np.uint16)
+    wp = None
+    if weights is not None:
+        weights = np.ascontiguousarray(weights, dtype=np.float32)
+        assert weights.shape == (N, K)
+        wp = weights.ctypes.data_as(ctypes.c_void_p)
+    lib().oracle_combine(N, H, K, np.ascontiguousarray(y_bits), dst_slot, wp, out)
+    return out
+
+
+def e4m3_encode(v):
+    """fp32 array -> e4m3 codes (round to nearest even, saturate to +-448)."""
+    v = np.ascontiguousarray(v, dtype=np.float32)
+    out = np.zeros(v.shape, np.uint8)
+    lib().oracle_e4m3_encode_array(v.size, v.reshape(-1), out.reshape(-1))
+    return out
+
+
+def e4m3_decode(c):
+    """e4m3 codes -> float64 values (NaN for 0x7F / 0xFF)."""
+    c = np.ascontiguousarray(c, dtype=np.uint8)
+    out = np.zeros(c.shape, np.float64)
+    lib().oracle_e4m3_decode_array(c.size, c.reshape(-1), out.reshape(-1))
+    return out
+
+
+def f32_to_bf16(v):
+    """fp32 array -> bf16 bit patterns (round to nearest even)."""
+    v = np.ascontiguousarray(v, dtype=np.float32)
+    out = np.zeros(v.shape, np.uint16)
+    lib().oracle_f32_to_bf16_array(v.size, v.reshape(-1), out.reshape(-1))
+    return out
