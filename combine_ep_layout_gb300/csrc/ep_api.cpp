@@ -1,0 +1,390 @@
+// ep_api.cpp -- the C ABI of libep_gb300.so (declared in include/ep_gb300.h).
+//
+// Conventions from "MORI JIT v2": every entry point is noexcept and reports
+// errors as a negative return code plus a thread-local message (§6: an
+// exception crossing extern "C" would take the interpreter down); a
+// configuration the kernels cannot serve is rejected when the handle is built
+// (§3.5, §5 "capability gate at construction, before allocation"); the
+// variant for a configuration is picked from a table of compiled
+// specialisations keyed by its shape (§5.1), never compiled on the hot path.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+#include <exception>
+#include <string>
+
+#include "ep_cfg.hpp"
+#include "ep_gb300.h"
+#include "ep_kernels.hpp"
+
+using namespace epg;
+
+namespace {
+
+thread_local std::string g_last_error;
+
+int fail(int code, const std::string& msg) {
+  g_last_error = msg;
+  return code;
+}
+
+int fail_cuda(cudaError_t e, const char* what) {
+  return fail(EP_ECUDA, std::string(what) + ": " + cudaGetErrorName(e) + " (" +
+                            cudaGetErrorString(e) + ")");
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Checks of "MORI JIT v2" §3.5 (token bytes 16-byte aligned; receive capacity
+// covers the worst case) plus this library's own limits.
+int validate(const ep_cfg_t* c) {
+  if (!c) return fail(EP_EINVAL, "cfg is NULL");
+  if (c->world_size < 1 || c->world_size > kMaxWorld)
+    return fail(EP_EINVAL, "world_size must be in [1, 64]");
+  if (c->max_tok_per_rank < 1) return fail(EP_EINVAL, "max_tok_per_rank must be >= 1");
+  const int64_t max_tokens = static_cast<int64_t>(c->world_size) * c->max_tok_per_rank;
+  if (max_tokens > kMaxTokens) return fail(EP_EINVAL, "world_size*max_tok_per_rank exceeds 2^24");
+  if (c->num_expert_per_rank < 1) return fail(EP_EINVAL, "num_expert_per_rank must be >= 1");
+  const int64_t E = static_cast<int64_t>(c->world_size) * c->num_expert_per_rank;
+  if (E > kMaxExperts) return fail(EP_EINVAL, "world_size*num_expert_per_rank exceeds 2048");
+  if (c->num_expert_per_token < 1 || c->num_expert_per_token > kMaxTopk)
+    return fail(EP_EINVAL, "num_expert_per_token must be in [1, 16]");
+  if (c->expert_alignment < 1 || c->expert_alignment > kMaxAlignment)
+    return fail(EP_EINVAL, "expert_alignment must be in [1, 4096]");
+  if (c->hidden_dim < 8 || c->hidden_dim > kMaxHidden || c->hidden_dim % 8 != 0)
+    return fail(EP_EINVAL, "hidden_dim must be a multiple of 8 in [8, 32768] (16-byte rows)");
+  if (c->use_weights != 0 && c->use_weights != 1) return fail(EP_EINVAL, "use_weights must be 0 or 1");
+  switch (c->dispatch_dtype) {
+    case EP_BF16: break;
+    case EP_FP8_E4M3:
+      if (c->hidden_dim % kScaleGroup != 0)
+        return fail(EP_EINVAL, "FP8 dispatch needs hidden_dim % 128 == 0 (one scale per 128 channels)");
+      break;
+    case EP_FP32:
+    case EP_FP4X2:
+      return fail(EP_EUNSUPPORTED, "dispatch dtype not served: only EP_BF16 and EP_FP8_E4M3");
+    default: return fail(EP_EINVAL, "unknown dispatch_dtype");
+  }
+  const int64_t rcap = RecvCapacity(max_tokens, c->num_expert_per_token, static_cast<int>(E),
+                                    c->expert_alignment);
+  if (rcap > INT32_MAX) return fail(EP_EINVAL, "receive capacity exceeds int32 rows");
+  return EP_OK;
+}
+
+}  // namespace
+
+struct ep_handle {
+  ep_cfg_t cfg;
+  int device = -1;
+  int W = 0, T = 0, Epr = 0, E = 0, K = 0, H = 0, A = 0;
+  int64_t max_tokens = 0, rcap = 0;
+  int max_chunks = 0;
+  int num_tokens = 0;
+  cudaStream_t last_stream = nullptr;
+  void* block = nullptr;
+  int32_t *cnt = nullptr, *tok_per_rank = nullptr, *psum_expert = nullptr, *psum_rank = nullptr,
+          *num_recv = nullptr, *err = nullptr, *dst_slot = nullptr, *meta = nullptr,
+          *chunk_hist = nullptr, *chunk_off = nullptr, *col_total = nullptr;
+  Variant<LayoutLaunch> layout{};
+  Variant<DispatchLaunch> dispatch{};
+  Variant<CombineLaunch> combine{};
+  LaunchGeom g_layout{}, g_dispatch{}, g_combine{};
+};
+
+namespace {
+
+int check_device(const ep_handle* h) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail_cuda(e, "cudaGetDevice");
+  if (dev != h->device)
+    return fail(EP_EINVAL, "the current device is not the device the handle was created on");
+  return EP_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int64_t ep_recv_capacity(const ep_cfg_t* cfg) noexcept {
+  try {
+    int rc = validate(cfg);
+    if (rc != EP_OK && rc != EP_EUNSUPPORTED) return rc;
+    return RecvCapacity(static_cast<int64_t>(cfg->world_size) * cfg->max_tok_per_rank,
+                        cfg->num_expert_per_token, cfg->world_size * cfg->num_expert_per_rank,
+                        cfg->expert_alignment);
+  } catch (const std::exception& ex) {
+    return fail(EP_EINVAL, ex.what());
+  } catch (...) {
+    return fail(EP_EINVAL, "unknown exception");
+  }
+}
+
+int ep_handle_create(const ep_cfg_t* cfg, ep_handle_t* out) noexcept {
+  try {
+    if (!out) return fail(EP_EINVAL, "out is NULL");
+    *out = nullptr;
+    int rc = validate(cfg);
+    if (rc != EP_OK) return rc;
+    ep_handle* h = new ep_handle();
+    h->cfg = *cfg;
+    h->W = cfg->world_size;
+    h->T = cfg->max_tok_per_rank;
+    h->Epr = cfg->num_expert_per_rank;
+    h->E = h->W * h->Epr;
+    h->K = cfg->num_expert_per_token;
+    h->H = cfg->hidden_dim;
+    h->A = cfg->expert_alignment;
+    h->max_tokens = static_cast<int64_t>(h->W) * h->T;
+    h->rcap = RecvCapacity(h->max_tokens, h->K, h->E, h->A);
+    h->max_chunks = NumLayoutChunks(static_cast<int>(h->max_tokens));
+
+    auto bail = [&](int code) {
+      if (h->block) cudaFree(h->block);
+      delete h;
+      return code;
+    };
+    cudaError_t e = cudaGetDevice(&h->device);
+    if (e != cudaSuccess) return bail(fail_cuda(e, "cudaGetDevice"));
+    int sms = 0;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, h->device);
+    if (e != cudaSuccess) return bail(fail_cuda(e, "cudaDeviceGetAttribute"));
+
+    h->layout = FindLayout(h->K);
+    h->dispatch = FindDispatch(h->H, h->K, static_cast<EpDType>(cfg->dispatch_dtype));
+    h->combine = FindCombine(h->H, h->K, cfg->use_weights != 0);
+    if (!h->dispatch.launch) return bail(fail(EP_EUNSUPPORTED, "no dispatch kernel for this dtype"));
+    h->g_layout.num_sms = h->g_dispatch.num_sms = h->g_combine.num_sms = sms;
+    const int cols = h->E + h->W;
+    if ((e = h->layout.prepare(h->H, h->K, cols, &h->g_layout)) != cudaSuccess)
+      return bail(fail_cuda(e, "layout kernel set-up"));
+    if ((e = h->dispatch.prepare(h->H, h->K, 0, &h->g_dispatch)) != cudaSuccess)
+      return bail(fail_cuda(e, "dispatch kernel set-up"));
+    if (h->g_dispatch.blocks_per_sm < 1)
+      return bail(fail(EP_EUNSUPPORTED, "dispatch kernel does not fit on an SM for this hidden_dim"));
+    if ((e = h->combine.prepare(h->H, h->K, 0, &h->g_combine)) != cudaSuccess)
+      return bail(fail_cuda(e, "combine kernel set-up"));
+
+    // one allocation, 256-byte aligned sub-buffers
+    auto al = [](size_t b) { return (b + 255) & ~static_cast<size_t>(255); };
+    const size_t n_small = al(4 * (h->E + h->W + (h->E + 1) + (h->W + 1) + 2));
+    const size_t n_slot = al(4 * static_cast<size_t>(h->max_tokens) * h->K);
+    const size_t n_meta = al(4 * static_cast<size_t>(h->rcap) * (h->K + 2));
+    const size_t n_scr = al(LayoutScratchBytes(h->max_chunks, cols));
+    e = cudaMalloc(&h->block, n_small + n_slot + n_meta + n_scr);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      return bail(fail(EP_ENOMEM, std::string("cudaMalloc of the handle's metadata failed: ") +
+                                      cudaGetErrorString(e)));
+    }
+    char* b = static_cast<char*>(h->block);
+    int32_t* s = reinterpret_cast<int32_t*>(b);
+    h->cnt = s;
+    h->tok_per_rank = h->cnt + h->E;
+    h->psum_expert = h->tok_per_rank + h->W;
+    h->psum_rank = h->psum_expert + h->E + 1;
+    h->num_recv = h->psum_rank + h->W + 1;
+    h->err = h->num_recv + 1;
+    h->dst_slot = reinterpret_cast<int32_t*>(b + n_small);
+    h->meta = reinterpret_cast<int32_t*>(b + n_small + n_slot);
+    int32_t* scr = reinterpret_cast<int32_t*>(b + n_small + n_slot + n_meta);
+    h->chunk_hist = scr;
+    h->chunk_off = scr + static_cast<size_t>(cols) * (h->max_chunks > 0 ? h->max_chunks : 1);
+    h->col_total = h->chunk_off + static_cast<size_t>(cols) * (h->max_chunks > 0 ? h->max_chunks : 1);
+    if ((e = cudaMemset(h->block, 0, n_small + n_slot + n_meta + n_scr)) != cudaSuccess)
+      return bail(fail_cuda(e, "cudaMemset"));
+    if ((e = cudaDeviceSynchronize()) != cudaSuccess) return bail(fail_cuda(e, "cudaDeviceSynchronize"));
+    *out = h;
+    return EP_OK;
+  } catch (const std::exception& ex) {
+    return fail(EP_EINVAL, ex.what());
+  } catch (...) {
+    return fail(EP_EINVAL, "unknown exception");
+  }
+}
+
+int ep_layout(ep_handle_t h, const int64_t* topk_idx, int32_t num_tokens, ep_stream_t stream) noexcept {
+  try {
+    if (!h) return fail(EP_EINVAL, "handle is NULL");
+    if (num_tokens < 0 || num_tokens > h->max_tokens)
+      return fail(EP_EINVAL, "num_tokens must be in [0, world_size*max_tok_per_rank]");
+    if (num_tokens > 0 && !topk_idx) return fail(EP_EINVAL, "topk_idx is NULL");
+    if (num_tokens > 0 && (reinterpret_cast<uintptr_t>(topk_idx) & 7u))
+      return fail(EP_EINVAL, "topk_idx must be 8-byte aligned");
+    int rc = check_device(h);
+    if (rc != EP_OK) return rc;
+    LayoutParams p{};
+    p.topk_idx = topk_idx;
+    p.num_tokens = num_tokens;
+    p.topk = h->K;
+    p.world_size = h->W;
+    p.max_tok_per_rank = h->T;
+    p.num_expert_per_rank = h->Epr;
+    p.num_experts = h->E;
+    p.alignment = h->A;
+    p.rcap = h->rcap;
+    p.num_chunks = NumLayoutChunks(num_tokens);
+    p.cnt = h->cnt;
+    p.tok_per_rank = h->tok_per_rank;
+    p.psum_expert = h->psum_expert;
+    p.psum_rank = h->psum_rank;
+    p.num_recv = h->num_recv;
+    p.dst_slot = h->dst_slot;
+    p.meta = h->meta;
+    p.err = h->err;
+    p.chunk_hist = h->chunk_hist;
+    p.chunk_off = h->chunk_off;
+    p.col_total = h->col_total;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = h->layout.launch(p, h->g_layout, s);
+    if (e != cudaSuccess) return fail_cuda(e, "layout launch");
+    h->num_tokens = num_tokens;
+    h->last_stream = s;
+    return EP_OK;
+  } catch (const std::exception& ex) {
+    return fail(EP_EINVAL, ex.what());
+  } catch (...) {
+    return fail(EP_EINVAL, "unknown exception");
+  }
+}
+
+int ep_dispatch(ep_handle_t h, const void* x, void* recv_x, float* recv_scales,
+                ep_stream_t stream) noexcept {
+  try {
+    if (!h) return fail(EP_EINVAL, "handle is NULL");
+    const bool fp8 = h->cfg.dispatch_dtype == EP_FP8_E4M3;
+    if (fp8 && !recv_scales) return fail(EP_EINVAL, "FP8 dispatch needs recv_scales");
+    if (!fp8 && recv_scales) return fail(EP_EINVAL, "recv_scales must be NULL for bf16 dispatch");
+    if (h->num_tokens > 0) {
+      if (!x || !recv_x) return fail(EP_EINVAL, "x / recv_x is NULL");
+      if (!aligned16(x) || !aligned16(recv_x) || (recv_scales && !aligned16(recv_scales)))
+        return fail(EP_EINVAL, "x, recv_x and recv_scales must be 16-byte aligned");
+    }
+    int rc = check_device(h);
+    if (rc != EP_OK) return rc;
+    DispatchParams p{};
+    p.x = x;
+    p.recv_x = recv_x;
+    p.recv_scales = recv_scales;
+    p.dst_slot = h->dst_slot;
+    p.num_tokens = h->num_tokens;
+    p.hidden = h->H;
+    p.topk = h->K;
+    p.err = h->err;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = h->dispatch.launch(p, h->g_dispatch, s);
+    if (e != cudaSuccess) return fail_cuda(e, "dispatch launch");
+    h->last_stream = s;
+    return EP_OK;
+  } catch (const std::exception& ex) {
+    return fail(EP_EINVAL, ex.what());
+  } catch (...) {
+    return fail(EP_EINVAL, "unknown exception");
+  }
+}
+
+int ep_combine(ep_handle_t h, const void* y, const float* topk_weights, void* out,
+               ep_stream_t stream) noexcept {
+  try {
+    if (!h) return fail(EP_EINVAL, "handle is NULL");
+    const bool weighted = h->cfg.use_weights != 0;
+    if (h->num_tokens > 0) {
+      if (!y || !out) return fail(EP_EINVAL, "y / out is NULL");
+      if (weighted && !topk_weights) return fail(EP_EINVAL, "use_weights is set but topk_weights is NULL");
+      if (!aligned16(y) || !aligned16(out)) return fail(EP_EINVAL, "y and out must be 16-byte aligned");
+      if (weighted && (reinterpret_cast<uintptr_t>(topk_weights) & 3u))
+        return fail(EP_EINVAL, "topk_weights must be 4-byte aligned");
+    }
+    int rc = check_device(h);
+    if (rc != EP_OK) return rc;
+    CombineParams p{};
+    p.y = y;
+    p.weights = weighted ? topk_weights : nullptr;
+    p.out = out;
+    p.dst_slot = h->dst_slot;
+    p.num_tokens = h->num_tokens;
+    p.hidden = h->H;
+    p.topk = h->K;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = h->combine.launch(p, h->g_combine, s);
+    if (e != cudaSuccess) return fail_cuda(e, "combine launch");
+    h->last_stream = s;
+    return EP_OK;
+  } catch (const std::exception& ex) {
+    return fail(EP_EINVAL, ex.what());
+  } catch (...) {
+    return fail(EP_EINVAL, "unknown exception");
+  }
+}
+
+void ep_handle_free(ep_handle_t h) noexcept {
+  try {
+    if (!h) return;
+    if (h->block) cudaFree(h->block);
+    delete h;
+  } catch (...) {
+  }
+}
+
+int ep_handle_get(ep_handle_t h, int32_t field, void** dev_ptr, int64_t* numel) noexcept {
+  try {
+    if (!h || !dev_ptr || !numel) return fail(EP_EINVAL, "NULL argument");
+    switch (field) {
+      case EP_FIELD_NUM_UNALIGNED_PER_EXPERT: *dev_ptr = h->cnt; *numel = h->E; break;
+      case EP_FIELD_NUM_TOKENS_PER_RANK: *dev_ptr = h->tok_per_rank; *numel = h->W; break;
+      case EP_FIELD_PSUM_PER_EXPERT: *dev_ptr = h->psum_expert; *numel = h->E + 1; break;
+      case EP_FIELD_PSUM_PER_RANK: *dev_ptr = h->psum_rank; *numel = h->W + 1; break;
+      case EP_FIELD_DST_SLOT:
+        *dev_ptr = h->dst_slot;
+        *numel = static_cast<int64_t>(h->num_tokens) * h->K;
+        break;
+      case EP_FIELD_RECV_SRC_METADATA: *dev_ptr = h->meta; *numel = h->rcap * (h->K + 2); break;
+      case EP_FIELD_NUM_RECV: *dev_ptr = h->num_recv; *numel = 1; break;
+      case EP_FIELD_DEVICE_ERROR: *dev_ptr = h->err; *numel = 1; break;
+      default: return fail(EP_EINVAL, "unknown field");
+    }
+    return EP_OK;
+  } catch (...) {
+    return fail(EP_EINVAL, "unknown exception");
+  }
+}
+
+int ep_handle_status(ep_handle_t h, int32_t* device_error) noexcept {
+  try {
+    if (!h || !device_error) return fail(EP_EINVAL, "NULL argument");
+    int rc = check_device(h);
+    if (rc != EP_OK) return rc;
+    cudaError_t e = cudaStreamSynchronize(h->last_stream);
+    if (e != cudaSuccess) return fail_cuda(e, "cudaStreamSynchronize");
+    int32_t v = 0;
+    if ((e = cudaMemcpy(&v, h->err, sizeof v, cudaMemcpyDeviceToHost)) != cudaSuccess)
+      return fail_cuda(e, "cudaMemcpy");
+    if ((e = cudaMemset(h->err, 0, sizeof v)) != cudaSuccess) return fail_cuda(e, "cudaMemset");
+    if ((e = cudaDeviceSynchronize()) != cudaSuccess) return fail_cuda(e, "cudaDeviceSynchronize");
+    *device_error = v;
+    return EP_OK;
+  } catch (...) {
+    return fail(EP_EINVAL, "unknown exception");
+  }
+}
+
+int ep_handle_variant(ep_handle_t h, int32_t step, char* buf, int32_t len) noexcept {
+  try {
+    if (!h || !buf || len < 1) return fail(EP_EINVAL, "NULL argument");
+    const char* name = step == 0 ? h->layout.name
+                     : step == 1 ? h->dispatch.name
+                     : step == 2 ? h->combine.name
+                                 : nullptr;
+    if (!name) return fail(EP_EINVAL, "step must be 0, 1 or 2");
+    std::snprintf(buf, static_cast<size_t>(len), "%s", name);
+    return EP_OK;
+  } catch (...) {
+    return fail(EP_EINVAL, "unknown exception");
+  }
+}
+
+const char* ep_last_error(void) noexcept { return g_last_error.c_str(); }
+
+}  // extern "C"

@@ -1,0 +1,96 @@
+// ep_kernels.hpp -- host-side interface between the C ABI (ep_api.cu) and the
+// kernel translation units.  Each kernel file exposes a registry lookup that
+// maps a runtime shape to the launcher of a compiled variant (a
+// specialisation from EPG_SHAPE_LIST, or the generic one), with the variant's
+// descriptive name ("MORI JIT v2" §3.3: the entry name carries the shape).
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+#include "ep_cfg.hpp"
+
+namespace epg {
+
+// Device error bits (sticky, read and cleared by ep_handle_status).
+constexpr int32_t kErrBadExpert = 1;   // a topk id outside [-1, E) was skipped
+constexpr int32_t kErrTimeout = 2;     // a bounded wait on a kernel's own copy ran out
+
+struct LayoutParams {
+  const int64_t* topk_idx;   // [N, K]
+  int num_tokens;            // N
+  int topk;                  // K
+  int world_size;            // W
+  int max_tok_per_rank;      // T
+  int num_expert_per_rank;   // Epr
+  int num_experts;           // E
+  int alignment;             // A
+  int64_t rcap;              // receive capacity (rows of meta)
+  int num_chunks;            // C = ceil(N / kLayoutTPC)
+  // outputs (handle)
+  int32_t* cnt;              // [E]
+  int32_t* tok_per_rank;     // [W]
+  int32_t* psum_expert;      // [E+1]
+  int32_t* psum_rank;        // [W+1]
+  int32_t* num_recv;         // [1]
+  int32_t* dst_slot;         // [N, K]
+  int32_t* meta;             // [rcap, K+2]
+  int32_t* err;              // [1]
+  // scratch (handle): per-chunk column histograms, column-major [E+W][C]
+  int32_t* chunk_hist;
+  int32_t* chunk_off;        // exclusive prefix over chunks, [E+W][C]
+  int32_t* col_total;        // [E+W]
+};
+
+struct DispatchParams {
+  const void* x;             // bf16 [N, H]
+  void* recv_x;              // bf16 or e4m3 [Rcap, H]
+  float* recv_scales;        // fp32 [Rcap, H/128] (FP8 only)
+  const int32_t* dst_slot;   // [N, K]
+  int num_tokens;
+  int hidden;
+  int topk;
+  int32_t* err;
+};
+
+struct CombineParams {
+  const void* y;             // bf16 [Rcap, H]
+  const float* weights;      // fp32 [N, K] or nullptr
+  void* out;                 // bf16 [N, H]
+  const int32_t* dst_slot;   // [N, K]
+  int num_tokens;
+  int hidden;
+  int topk;
+};
+
+// Launch geometry of a variant on the current device, filled by its prepare
+// function when a handle is built.
+struct LaunchGeom {
+  int num_sms;        // SMs of the device
+  int blocks_per_sm;  // resident CTAs per SM for the variant's block and shared memory
+};
+
+using LayoutLaunch = cudaError_t (*)(const LayoutParams&, const LaunchGeom&, cudaStream_t);
+using DispatchLaunch = cudaError_t (*)(const DispatchParams&, const LaunchGeom&, cudaStream_t);
+using CombineLaunch = cudaError_t (*)(const CombineParams&, const LaunchGeom&, cudaStream_t);
+// Per-device set-up of a variant (shared-memory opt-in, occupancy).  `aux` is
+// E+W for the layout and unused elsewhere.
+using PrepareFn = cudaError_t (*)(int hidden, int topk, int aux, LaunchGeom* geom);
+
+template <class F>
+struct Variant {
+  const char* name;
+  F launch;
+  PrepareFn prepare;
+};
+
+Variant<LayoutLaunch> FindLayout(int topk);
+Variant<DispatchLaunch> FindDispatch(int hidden, int topk, EpDType dtype);
+Variant<CombineLaunch> FindCombine(int hidden, int topk, bool use_weights);
+
+// Bytes of layout scratch for up to max_chunks chunks and `columns` = E+W columns.
+size_t LayoutScratchBytes(int max_chunks, int columns);
+
+}  // namespace epg

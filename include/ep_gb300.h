@@ -1,0 +1,186 @@
+/*
+ * ep_gb300.h -- C ABI of the single-GPU MoE expert-parallel layout /
+ * dispatch / combine library (libep_gb300.so, sm_103a).
+ *
+ * The operations are the ones of the EPHandle / dispatch / combine API of
+ * "DeepEP overall architecture analysis" (ElasticBuffer class diagram:
+ * dispatch(x, topk_idx, ...) -> (recv_x, handle), combine(x, handle, ...);
+ * EPHandle class listing; "Dispatch data flow" and "Combine data flow"
+ * figures), with the configuration fields of EpCfg from "MORI JIT v2" §3.2
+ * and that page's conventions for a C boundary (§6: every entry point catches
+ * everything, returns a negative code on error and leaves the message in a
+ * last-error string; §3.5: a configuration that cannot be served is rejected
+ * when the handle is built, never turned into wrong numbers).
+ *
+ * All "ranks" are logical: rank r owns experts [r*Epr, (r+1)*Epr) and one
+ * contiguous slice of the receive buffer, all in the memory of the current
+ * GPU.  No call transfers data between GPUs.
+ *
+ * Conventions for every entry point:
+ *   - Pointers documented "device" must point to memory of the current CUDA
+ *     device; the library never dereferences them on the host.
+ *   - The caller owns every buffer it passes (inputs and outputs).  The
+ *     handle owns its routing metadata (allocated by ep_handle_create, freed
+ *     by ep_handle_free).
+ *   - Work is enqueued on `stream` (NULL = the legacy default stream); no
+ *     entry point synchronises except ep_handle_status.  ep_layout,
+ *     ep_dispatch and ep_combine allocate nothing and can be enqueued while a
+ *     stream is being captured into a CUDA graph.
+ *   - Return value 0 on success, else one of the negative EP_E* codes, with
+ *     a message available from ep_last_error() on the calling thread.
+ */
+#ifndef EP_GB300_H
+#define EP_GB300_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+#define EP_NOEXCEPT noexcept
+extern "C" {
+#else
+#define EP_NOEXCEPT
+#endif
+
+/* Same object as cudaStream_t; declared here so that this header needs no CUDA header. */
+typedef struct CUstream_st *ep_stream_t;
+
+/* Transport dtype of the dispatched rows; numbering as EpDType in
+ * "MORI JIT v2" §3.7 (Bf16 = 0, Fp32 = 1, Fp8 = 2, Fp4x2 = 3).  This library
+ * dispatches EP_BF16 (a byte copy) and EP_FP8_E4M3 (a fused cast from bf16 to
+ * OCP e4m3 with one fp32 scale per 128 channels); the other two are rejected
+ * with EP_EUNSUPPORTED. */
+typedef enum {
+    EP_BF16 = 0,
+    EP_FP32 = 1,
+    EP_FP8_E4M3 = 2,
+    EP_FP4X2 = 3
+} ep_dtype_t;
+
+/* Configuration ("MORI JIT v2" §3.2 EpCfg; expert_alignment from the EPHandle
+ * listing).  Valid ranges (checked by ep_handle_create):
+ *   1 <= world_size <= 64, 1 <= max_tok_per_rank, world_size*max_tok_per_rank <= 2^24,
+ *   1 <= num_expert_per_rank, world_size*num_expert_per_rank <= 2048,
+ *   1 <= num_expert_per_token <= 16, 1 <= expert_alignment <= 4096,
+ *   hidden_dim >= 8, hidden_dim % 8 == 0 (rows are whole 16-byte units), hidden_dim <= 32768;
+ *   for EP_FP8_E4M3 also hidden_dim % 128 == 0;
+ *   the receive capacity (ep_recv_capacity) must fit in int32. */
+typedef struct {
+    int32_t world_size;           /* W: logical ranks */
+    int32_t hidden_dim;           /* H: channels per token row */
+    int32_t max_tok_per_rank;     /* T: tokens per logical rank; N <= W*T */
+    int32_t num_expert_per_rank;  /* Epr; E = W*Epr experts */
+    int32_t num_expert_per_token; /* K: top-k */
+    int32_t expert_alignment;     /* A: each expert's receive segment is padded to a multiple of A */
+    int32_t dispatch_dtype;       /* ep_dtype_t */
+    int32_t use_weights;          /* 1: combine weights rows by topk_weights; 0: plain sum */
+} ep_cfg_t;
+
+enum {
+    EP_OK = 0,
+    EP_EINVAL = -1,        /* invalid argument or configuration */
+    EP_EUNSUPPORTED = -2,  /* a valid request this library does not serve */
+    EP_ECUDA = -3,         /* a CUDA runtime call failed (message has the CUDA error) */
+    EP_ENOMEM = -4         /* device allocation failed */
+};
+
+/* Opaque handle: the configuration, the routing metadata of the last
+ * ep_layout call, and the kernels chosen for this configuration. */
+typedef struct ep_handle *ep_handle_t;
+
+/* Receive-buffer rows needed for any routing of up to W*T tokens:
+ * Rcap = W*T*K + E*(A-1) (every (token, k) gets a row; each expert segment
+ * adds at most A-1 padding rows).  Returns a negative EP_E* code for an
+ * invalid configuration. */
+int64_t ep_recv_capacity(const ep_cfg_t *cfg) EP_NOEXCEPT;
+
+/* Validate cfg, pick the compiled kernel variants for it and allocate the
+ * handle's device metadata on the current device (cudaMalloc; sized for W*T
+ * tokens).  *out receives the handle.  Errors: EP_EINVAL (bad cfg or NULL),
+ * EP_EUNSUPPORTED (dispatch dtype not served), EP_ENOMEM, EP_ECUDA. */
+int ep_handle_create(const ep_cfg_t *cfg, ep_handle_t *out) EP_NOEXCEPT;
+
+/* Layout.  topk_idx: device int64 [num_tokens, K] row-major, token t of
+ * logical rank t / T.  Entries equal to -1 are masked (no receive row); any
+ * other value outside [0, E) is skipped and sets bit 0 of the device error
+ * word (see ep_handle_status).  Computes on the device, into the handle:
+ *   num_unaligned_recv_tokens_per_expert [E]   entries routed to each expert
+ *   num_tokens_per_rank [W]                    tokens with >= 1 expert on rank r
+ *   psum_num_recv_tokens_per_expert [E+1]      exclusive prefix sum of the
+ *                                              counts padded to a multiple of A
+ *   psum_num_recv_tokens_per_rank [W+1]        the same sum at each rank's first expert
+ *   num_recv_tokens [1]                        R = psum_expert[E]
+ *   dst_slot [num_tokens, K]                   receive row of each (t, k), -1 if skipped;
+ *                                              rows of one expert follow the flat order t*K+k
+ *   recv_src_metadata [Rcap, K+2]              for each received row:
+ *                                              {t / T, t mod T, dst_slot[t][0..K-1]};
+ *                                              -1 in every row that receives nothing
+ * (EPHandle listing of "DeepEP overall architecture analysis").
+ * 0 <= num_tokens <= W*T, else EP_EINVAL.  The number of tokens is kept in the
+ * handle for the following ep_dispatch / ep_combine calls. */
+int ep_layout(ep_handle_t h, const int64_t *topk_idx, int32_t num_tokens, ep_stream_t stream) EP_NOEXCEPT;
+
+/* Dispatch ("Dispatch data flow": token data + scale factors to the receive
+ * buffer).  x: device bf16 [N, H] row-major (16-byte aligned).
+ * EP_BF16:     recv_x device bf16 [Rcap, H]; recv_x[dst_slot[t][k]] = x[t], bit-exact.
+ * EP_FP8_E4M3: recv_x device uint8 (e4m3) [Rcap, H], recv_scales device fp32
+ *              [Rcap, H/128]; per token and 128-channel group g:
+ *              s = amax|x[t, g]| / 448 (fp32), q = e4m3_rn_satfinite(x / s),
+ *              s = 0 and q = 0 when amax = 0; written to every row dst_slot[t][k].
+ * recv_scales must be NULL for EP_BF16 and non-NULL for EP_FP8_E4M3.  Rows
+ * that receive no token are not written.  Uses the routing of the last
+ * ep_layout call on this handle (same stream, or ordered after it).
+ * Buffers must be 16-byte aligned, else EP_EINVAL. */
+int ep_dispatch(ep_handle_t h, const void *x, void *recv_x, float *recv_scales,
+                ep_stream_t stream) EP_NOEXCEPT;
+
+/* Combine ("Combine data flow": reduce weighted by topk_weights back to token
+ * order).  y: device bf16 [Rcap, H] expert outputs, in the receive layout;
+ * topk_weights: device fp32 [N, K] (ignored, may be NULL, when use_weights is
+ * 0); out: device bf16 [N, H].  For every token t and channel c:
+ *   acc = +0.0f; for k = 0..K-1 with dst_slot[t][k] >= 0:
+ *       acc = fmaf(w[t][k], y[dst_slot[t][k]][c], acc)     (acc += y without weights)
+ *   out[t][c] = bf16 round-to-nearest-even(acc).
+ * Padding rows of y are never read.  Buffers must be 16-byte aligned. */
+int ep_combine(ep_handle_t h, const void *y, const float *topk_weights, void *out,
+               ep_stream_t stream) EP_NOEXCEPT;
+
+/* Release the handle and its device memory (cudaFree, which waits for work
+ * using it to finish).  NULL is ignored. */
+void ep_handle_free(ep_handle_t h) EP_NOEXCEPT;
+
+/* Fields of the handle, for ep_handle_get. */
+enum {
+    EP_FIELD_NUM_UNALIGNED_PER_EXPERT = 0, /* int32 [E] */
+    EP_FIELD_NUM_TOKENS_PER_RANK = 1,      /* int32 [W] */
+    EP_FIELD_PSUM_PER_EXPERT = 2,          /* int32 [E+1] */
+    EP_FIELD_PSUM_PER_RANK = 3,            /* int32 [W+1] */
+    EP_FIELD_DST_SLOT = 4,                 /* int32 [N, K] (N of the last layout) */
+    EP_FIELD_RECV_SRC_METADATA = 5,        /* int32 [Rcap, K+2] */
+    EP_FIELD_NUM_RECV = 6,                 /* int32 [1] */
+    EP_FIELD_DEVICE_ERROR = 7              /* int32 [1], sticky error bits */
+};
+
+/* Device pointer and element count of one handle field (the handle keeps
+ * ownership; valid until ep_handle_free).  EP_EINVAL for an unknown field. */
+int ep_handle_get(ep_handle_t h, int32_t field, void **dev_ptr, int64_t *numel) EP_NOEXCEPT;
+
+/* Synchronise the handle's last stream, read and clear the sticky device
+ * error word.  Bits: 1 = a topk id outside [-1, E) was skipped; 2 = a kernel
+ * gave up waiting on one of its own copies (the kernel returned early and its
+ * outputs are incomplete).  Returns EP_ECUDA if the synchronisation fails. */
+int ep_handle_status(ep_handle_t h, int32_t *device_error) EP_NOEXCEPT;
+
+/* Name of the kernel variant chosen for a step (0 = layout, 1 = dispatch,
+ * 2 = combine) written to buf (NUL-terminated, truncated to len).  A name
+ * carries the compile-time shape, e.g. "ep_dispatch_bf16_h7168_k8", or
+ * "..._generic" when no specialisation for the shape was compiled. */
+int ep_handle_variant(ep_handle_t h, int32_t step, char *buf, int32_t len) EP_NOEXCEPT;
+
+/* Message of the last failed call on this thread ("" if none). */
+const char *ep_last_error(void) EP_NOEXCEPT;
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* EP_GB300_H */

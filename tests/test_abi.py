@@ -1,0 +1,103 @@
+"""CPU checks of the C boundary: the library loads, exports every function the
+header declares, validates configurations on the host (no GPU needed), and the
+compile-time config header compiles with a host-only compiler ("MORI JIT v2"
+§3.5: the Cfg header needs no device compiler)."""
+import ctypes
+import os
+import subprocess
+
+import pytest
+
+import __graft_entry__
+import combine_ep_layout_gb300 as ep
+import oracle
+import synth
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    __graft_entry__.build()
+
+
+def test_exports_every_declared_symbol():
+    names = ep.declared_symbols()
+    assert len(names) == 10
+    L = ep.load_library()
+    for n in names:
+        assert hasattr(L, n), n
+    out = subprocess.run(["nm", "-D", "--defined-only", ep._native.LIB_PATH],
+                         capture_output=True, text=True, check=True).stdout
+    exported = {l.split()[-1] for l in out.splitlines() if " T " in l}
+    assert set(names) <= exported
+
+
+@pytest.mark.parametrize("name", list(synth.WORKLOADS))
+def test_recv_capacity_matches_the_oracle(name):
+    wl = synth.WORKLOADS[name]
+    cfg = ep.make_cfg(wl.world_size, wl.hidden, wl.max_tok_per_rank, wl.num_expert_per_rank,
+                      wl.topk, wl.alignment, wl.dispatch_dtype, wl.use_weights)
+    want = oracle.recv_capacity(wl.world_size * wl.max_tok_per_rank, wl.topk, wl.num_experts,
+                                wl.alignment)
+    assert ep.ep_recv_capacity(cfg) == want == wl.recv_capacity
+
+
+BAD = [
+    dict(world_size=0), dict(world_size=65), dict(max_tok_per_rank=0),
+    dict(num_expert_per_rank=0), dict(num_expert_per_rank=257),  # E = 8*257 > 2048
+    dict(num_expert_per_token=0), dict(num_expert_per_token=17),
+    dict(expert_alignment=0), dict(expert_alignment=4097),
+    dict(hidden_dim=7100), dict(hidden_dim=4), dict(hidden_dim=32776),
+    dict(dispatch_dtype=2, hidden_dim=7176),   # FP8 needs hidden % 128 == 0
+    dict(dispatch_dtype=9), dict(use_weights=2),
+    dict(max_tok_per_rank=1 << 22),            # W*T > 2^24
+]
+
+
+@pytest.mark.parametrize("bad", BAD)
+def test_invalid_configs_are_rejected_on_the_host(bad):
+    base = dict(world_size=8, hidden_dim=7168, max_tok_per_rank=128, num_expert_per_rank=8,
+                num_expert_per_token=8, expert_alignment=1, dispatch_dtype=0, use_weights=1)
+    base.update(bad)
+    cfg = ep.ep_cfg_t(**base)
+    L = ep.load_library()
+    h = ctypes.c_void_p()
+    rc = L.ep_handle_create(ctypes.byref(cfg), ctypes.byref(h))
+    assert rc == ep.EP_EINVAL
+    assert h.value is None
+    assert ep.ep_last_error()
+    assert L.ep_recv_capacity(ctypes.byref(cfg)) == ep.EP_EINVAL
+
+
+@pytest.mark.parametrize("dt", [ep.EP_FP32, ep.EP_FP4X2])
+def test_unserved_dtypes_are_unsupported(dt):
+    cfg = ep.make_cfg(8, 7168, 128, 8, 8, 1, dt, True)
+    h = ctypes.c_void_p()
+    assert ep.load_library().ep_handle_create(ctypes.byref(cfg), ctypes.byref(h)) == \
+        ep.EP_EUNSUPPORTED
+    assert "dtype" in ep.ep_last_error()
+
+
+def test_null_arguments_are_errors_not_crashes():
+    L = ep.load_library()
+    assert L.ep_handle_create(None, None) == ep.EP_EINVAL
+    assert L.ep_layout(None, None, 0, None) == ep.EP_EINVAL
+    assert L.ep_dispatch(None, None, None, None, None) == ep.EP_EINVAL
+    assert L.ep_combine(None, None, None, None, None) == ep.EP_EINVAL
+    L.ep_handle_free(None)
+    assert L.ep_handle_status(None, None) == ep.EP_EINVAL
+
+
+def test_cfg_header_compiles_without_a_device_compiler():
+    inc = os.path.join(ROOT, "combine_ep_layout_gb300", "csrc")
+    tu = '#include "ep_cfg.hpp"\nstatic_assert(epg::RecvCapacity(32768, 8, 256, 128) == 294656);\n' \
+         'int main() { return epg::EpShapeFieldCount() == 4 ? 0 : 1; }\n'
+    subprocess.run(["g++", "-std=c++20", "-fsyntax-only", "-Wall", "-Werror", "-I", inc, "-x", "c++",
+                    "-"], input=tu, text=True, check=True)
+
+
+def test_public_header_is_plain_c():
+    tu = '#include "ep_gb300.h"\nint main(void) { ep_cfg_t c = {0}; return (int)sizeof c; }\n'
+    subprocess.run(["gcc", "-std=c99", "-fsyntax-only", "-Wall", "-Werror", "-I",
+                    os.path.join(ROOT, "include"), "-x", "c", "-"], input=tu, text=True, check=True)
