@@ -1,0 +1,489 @@
+"""Benchmark of the MoE expert-parallel layout / dispatch / combine path on GB300.
+
+One step on the prefill workload (32768 tokens = 8 logical ranks x 4096,
+hidden 7168, 256 experts, top-8, expert_alignment 128, softmax weights):
+
+    layout (bf16 handle) -> dispatch bf16 -> identity experts -> combine
+    layout (fp8 handle)  -> dispatch FP8 e4m3 with per-128 scales
+
+i.e. every step of the hot path once, on the routing of that step.  Inputs
+are synthetic and seeded (synth module), resident in HBM before timing, and
+larger than L2 (x is 470 MB, the receive buffers 4.2 GB and 2.1 GB), so no L2
+flush is needed between steps.  Kernels are timed with CUDA events on the
+stream they are launched on.
+
+Prints one JSON line (rank 0).  --impl reference times the CPU oracle instead
+(test infrastructure used as the slow reference arm), on a bounded sample.
+Multi-GPU: replicas only (one independent replica per GPU, no collective on
+the data path); barrier + max-over-ranks timing.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "dispatch & combine GB/s and tokens/s on 1 GB300; % of HBM roofline"
+WORKLOAD = "prefill"
+WORKLOAD_DESC = ("prefill: 8 logical ranks x 4096 tokens = 32768 tokens, hidden 7168 bf16 ~N(0,1), "
+                 "256 experts (32/rank), top-8 uniform distinct, softmax weights, expert_alignment "
+                 "128; dispatch bf16 and FP8 e4m3 (per-128 fp32 scales); combine bf16 with fp32 fma")
+KERNEL_SOURCES = ["ep_layout.cu", "ep_dispatch.cu", "ep_combine.cu", "ep_ptx.cuh", "ep_cfg.hpp",
+                  "ep_kernels.hpp"]
+
+
+# ----------------------------------------------------------------- helpers
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")),
+            int(os.environ.get("WORLD_SIZE", "1")))
+
+
+def reduce_over_ranks(ms, units, world):
+    """Max of the per-rank elapsed time and the sum of the units processed."""
+    if world <= 1:
+        return ms, units
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([ms], dtype=torch.float64, device=dev)
+    u = torch.tensor([units], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
+def algorithmic_bytes(N, H, K, rcap, valid_entries=None):
+    """Bytes each kernel must move (padding rows excluded)."""
+    NK = N * K if valid_entries is None else valid_entries
+    G = H // 128
+    return {
+        "layout": N * K * 8 + N * K * 4 + rcap * (K + 2) * 4,
+        "dispatch_bf16": N * H * 2 + N * K * 4 + NK * H * 2,
+        "dispatch_fp8": N * H * 2 + N * K * 4 + NK * H + NK * G * 4,
+        "combine": NK * H * 2 + N * K * 4 + N * K * 4 + N * H * 2,
+    }
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def kernel_source_digest():
+    h = hashlib.sha256()
+    for n in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "combine_ep_layout_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, or None
+    when the summary is missing or was taken on other kernel sources."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except Exception:
+        return None
+    if d.get("source_digest") != kernel_source_digest():
+        return None
+    k = d.get("kernels", {}).get(kernel)
+    return None if k is None else k.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 50 ms; entering the
+    context waits (up to 5 s) for the first sample so that the sampler is
+    running when the timed region starts."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+            t0 = time.time()
+            while not self.lines and time.time() - t0 < 5.0 and self.proc.poll() is None:
+                time.sleep(0.01)
+            self.skip = len(self.lines)     # samples taken before the timed region
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines[getattr(self, "skip", 0):]:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------- GPU arm
+
+def prefill_workload(tokens=None):
+    """The prefill workload, or the same shape with fewer tokens (a smaller case
+    for profiler captures: 8 logical ranks x tokens/8)."""
+    import synth
+    wl = synth.WORKLOADS["prefill_bf16"]
+    if tokens is None or tokens == wl.num_tokens:
+        return wl
+    assert tokens % wl.world_size == 0
+    return wl.with_(num_tokens=tokens, max_tok_per_rank=tokens // wl.world_size)
+
+
+def run_ours(args, rank, local_rank, world):
+    import numpy as np
+    import torch
+
+    import combine_ep_layout_gb300 as ep
+    import synth
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    wl = prefill_workload(args.tokens)
+    N, H, K, R = wl.num_tokens, wl.hidden, wl.topk, wl.recv_capacity
+    cfg16 = ep.make_cfg(wl.world_size, H, wl.max_tok_per_rank, wl.num_expert_per_rank, K,
+                        wl.alignment, "bf16", True)
+    cfg8 = ep.make_cfg(wl.world_size, H, wl.max_tok_per_rank, wl.num_expert_per_rank, K,
+                       wl.alignment, "fp8", True)
+    h16, h8 = ep.EpHandle(cfg16), ep.EpHandle(cfg8)
+    topk_cpu = synth.gen_topk(wl)
+    w_cpu = synth.gen_weights(wl)
+    x = synth.gen_x(wl, device=dev)
+    topk, w = topk_cpu.to(dev), w_cpu.to(dev)
+    recv = torch.empty((R, H), dtype=torch.bfloat16, device=dev)
+    recv8 = torch.empty((R, H), dtype=torch.uint8, device=dev)
+    scales = torch.empty((R, H // 128), dtype=torch.float32, device=dev)
+    out = torch.empty((N, H), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    names = ["layout", "dispatch_bf16", "combine", "layout_fp8", "dispatch_fp8"]
+    launches_per_step = 3 + 1 + 1 + 3 + 1
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        h16.layout(topk, stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+        h16.dispatch(x, recv, stream=stream)
+        if ev is not None:
+            ev[2].record(stream)
+        h16.combine(recv, w, out, stream=stream)   # identity experts: y = recv
+        if ev is not None:
+            ev[3].record(stream)
+        h8.layout(topk, stream=stream)
+        if ev is not None:
+            ev[4].record(stream)
+        h8.dispatch(x, recv8, scales, stream=stream)
+        if ev is not None:
+            ev[5].record(stream)
+
+    import torch.distributed as dist
+    for _ in range(args.warmup):
+        step()
+    stream.synchronize()
+    assert h16.status() == 0 and h8.status() == 0
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local_rank) as clk:
+        start.record(stream)
+        for i in range(args.steps):
+            step(events[i])
+        stop.record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    total_ms = start.elapsed_time(stop)
+    per_kernel = {n: [] for n in names}
+    for ev in events:
+        for j, n in enumerate(names):
+            per_kernel[n].append(ev[j].elapsed_time(ev[j + 1]))
+    avg = {n: sum(v) / len(v) for n, v in per_kernel.items()}
+    assert h16.status() == 0 and h8.status() == 0
+
+    nbytes = algorithmic_bytes(N, H, K, R)
+    step_bytes = 2 * nbytes["layout"] + nbytes["dispatch_bf16"] + nbytes["combine"] + \
+        nbytes["dispatch_fp8"]
+    ms, units = reduce_over_ranks(total_ms / args.steps, step_bytes, world)
+    _, toks = reduce_over_ranks(total_ms / args.steps, N, world)
+    peak, peak_kind = measured_peaks()
+    kernels = {}
+    for n in names:
+        b = nbytes["layout" if n.startswith("layout") else n]
+        us = avg[n] * 1e3
+        gbs = b / (avg[n] * 1e-3) / 1e9
+        kernels[n] = {"us": round(us, 2), "algorithmic_bytes": b, "gbs": round(gbs, 1),
+                      "frac_of_peak": round(gbs / peak, 4),
+                      "frac_of_8tbs": round(gbs / 8000.0, 4)}
+    dom = max(["dispatch_bf16", "combine", "dispatch_fp8"], key=lambda n: avg[n])
+    kname = {"dispatch_bf16": "ep_dispatch_bf16_kernel", "combine": "ep_combine_kernel",
+             "dispatch_fp8": "ep_dispatch_fp8_kernel"}[dom]
+    roof = {"bound": "hbm", "kernel": dom, "achieved": kernels[dom]["gbs"], "peak": peak,
+            "peak_kind": peak_kind + " hbm_gbs (burst copy)", "unit": "GB/s",
+            "frac": kernels[dom]["frac_of_peak"], "traffic": ncu_traffic(kname),
+            "algorithmic_bytes": nbytes[dom]}
+
+    e2e = run_e2e(args, ep, torch, dev, wl, topk_cpu, w_cpu, x, (h16, h8), (recv, recv8, scales),
+                  step_bytes, world) if not args.no_e2e else None
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(wl, topk_cpu, w_cpu, x, budget_s=args.cpu_seconds)
+
+    if rank != 0:
+        return None
+    gbs = units / (ms * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": round(gbs, 1), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded; shapes and distributions of the prefill workload)",
+        "config": {"workload": WORKLOAD_DESC if N == 32768 else
+                   WORKLOAD_DESC.replace("4096 tokens = 32768", "%d tokens = %d" % (N // 8, N)),
+                   "tokens": N, "hidden": H, "experts": wl.num_experts,
+                   "world_size_logical": wl.world_size, "topk": K,
+                   "expert_alignment": wl.alignment, "recv_capacity": R,
+                   "step": "layout + dispatch bf16 + combine (identity experts) + layout + "
+                           "dispatch fp8",
+                   "l2": "no flush: every step's inputs/outputs exceed L2 (x 470 MB, recv_x "
+                         "4.2 GB, recv_x fp8 2.1 GB)",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "tokens_per_s": round(toks / (ms * 1e-3), 1),
+        "kernels": kernels,
+        "roofline": roof,
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk.summary(),
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+    }
+    return line
+
+
+def run_e2e(args, ep, torch, dev, wl, topk_cpu, w_cpu, x, handles, bufs, step_bytes, world):
+    """Same step through the public API, with this step's inputs copied from
+    pinned host memory and the combined output read back, inside the timed region."""
+    h16, h8 = handles
+    recv, recv8, scales = bufs
+    N, H = wl.num_tokens, wl.hidden
+    x_h = x.cpu().pin_memory()
+    topk_h = topk_cpu.pin_memory()
+    w_h = w_cpu.pin_memory()
+    out_h = torch.empty((N, H), dtype=torch.bfloat16).pin_memory()
+    x_d = torch.empty_like(x)
+    topk_d = torch.empty(topk_cpu.shape, dtype=torch.int64, device=dev)
+    w_d = torch.empty(w_cpu.shape, dtype=torch.float32, device=dev)
+    out_d = torch.empty((N, H), dtype=torch.bfloat16, device=dev)
+    s = torch.cuda.Stream(device=dev)
+
+    def step():
+        with torch.cuda.stream(s):
+            x_d.copy_(x_h, non_blocking=True)
+            topk_d.copy_(topk_h, non_blocking=True)
+            w_d.copy_(w_h, non_blocking=True)
+        h16.layout(topk_d, stream=s)
+        h16.dispatch(x_d, recv, stream=s)
+        h16.combine(recv, w_d, out_d, stream=s)
+        h8.layout(topk_d, stream=s)
+        h8.dispatch(x_d, recv8, scales, stream=s)
+        with torch.cuda.stream(s):
+            out_h.copy_(out_d, non_blocking=True)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    s.synchronize()
+    n = max(1, args.steps)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    import torch.distributed as dist
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    a.record(s)
+    for _ in range(n):
+        step()
+    b.record(s)
+    torch.cuda.synchronize()
+    ms, units = reduce_over_ranks(a.elapsed_time(b) / n, step_bytes, world)
+    h2d = x_h.numel() * 2 + topk_h.numel() * 8 + w_h.numel() * 4
+    return {"value": round(units / (ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+            "ms_per_step": round(ms, 4), "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": out_h.numel() * 2}
+
+
+# ------------------------------------------------------------- CPU oracle
+
+def oracle_step_sample(wl, topk_np, w_np, x_bits, tok0, ntok, bufs):
+    """One oracle pass of the step over tokens [tok0, tok0+ntok) of the prefill
+    workload (layout over the whole batch, the data movement over the sample).
+    Returns the algorithmic bytes it covered."""
+    import oracle
+    recv16, recv8, scales = bufs
+    lay = oracle.layout(topk_np, wl.world_size, wl.max_tok_per_rank, wl.num_expert_per_rank,
+                        wl.alignment)
+    sl = lay["dst_slot"][tok0:tok0 + ntok]
+    xs = x_bits[tok0:tok0 + ntok]
+    oracle.dispatch_bf16(xs, sl, recv16)
+    oracle.combine(recv16, sl, w_np[tok0:tok0 + ntok])
+    oracle.dispatch_fp8(xs, sl, recv8, scales)
+    N, H, K = wl.num_tokens, wl.hidden, wl.topk
+    nb_full = algorithmic_bytes(N, H, K, wl.recv_capacity)
+    nb = algorithmic_bytes(ntok, H, K, 0)
+    return nb_full["layout"] + nb["dispatch_bf16"] + nb["combine"] + nb["dispatch_fp8"], ntok
+
+
+def cpu_baseline(wl, topk_cpu, w_cpu, x, budget_s=15.0, block=512):
+    """The oracle as it stands (single-threaded C), on a bounded sample: blocks of
+    `block` tokens until ~budget_s seconds of CPU work."""
+    import numpy as np
+
+    import synth
+    x_bits = synth.bits16(x)
+    topk_np, w_np = topk_cpu.numpy(), w_cpu.numpy()
+    R, H = wl.recv_capacity, wl.hidden
+    bufs = (np.zeros((R, H), np.uint16), np.zeros((R, H), np.uint8),
+            np.zeros((R, H // 128), np.float32))
+    t0 = time.perf_counter()
+    nbytes, ntoks, tok = 0, 0, 0
+    while time.perf_counter() - t0 < budget_s and tok < wl.num_tokens:
+        b, n = oracle_step_sample(wl, topk_np, w_np, x_bits, tok, block, bufs)
+        nbytes += b
+        ntoks += n
+        tok += block
+    dt = time.perf_counter() - t0
+    return {"value": round(nbytes / dt / 1e9, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "tokens_per_s": round(ntoks / dt, 1),
+            "sample": "%d of %d tokens in blocks of %d (each block: layout of the whole batch + "
+                      "dispatch bf16 + combine + dispatch fp8 of the block), %.1f s" %
+                      (ntoks, wl.num_tokens, block, dt)}
+
+
+def run_reference(args, rank, world):
+    """Reference arm: the CPU oracle, timed on the host, same metric and unit."""
+    if rank != 0:
+        return None
+    import numpy as np
+
+    import synth
+    wl = synth.WORKLOADS["prefill_bf16"]
+    topk_cpu, w_cpu = synth.gen_topk(wl), synth.gen_weights(wl)
+    block = args.ref_block
+    x = synth.gen_bf16_normal(block * max(1, args.steps + args.warmup), wl.hidden,
+                              wl.seed * 16 + 3)
+    x_bits = synth.bits16(x)
+    R, H = wl.recv_capacity, wl.hidden
+    bufs = (np.zeros((R, H), np.uint16), np.zeros((R, H), np.uint8),
+            np.zeros((R, H // 128), np.float32))
+    topk_np, w_np = topk_cpu.numpy(), w_cpu.numpy()
+    xb_full = np.zeros((wl.num_tokens, H), np.uint16)
+    xb_full[:x_bits.shape[0]] = x_bits
+    for i in range(args.warmup):
+        oracle_step_sample(wl, topk_np, w_np, xb_full, i * block, block, bufs)
+    t0 = time.perf_counter()
+    nbytes = ntok = 0
+    for i in range(args.steps):
+        b, n = oracle_step_sample(wl, topk_np, w_np, xb_full, (args.warmup + i) * block, block,
+                                  bufs)
+        nbytes += b
+        ntok += n
+    dt = time.perf_counter() - t0
+    v = round(nbytes / dt / 1e9, 3)
+    return {"metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(dt / max(1, args.steps) * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic", "impl": "reference",
+            "config": {"workload": WORKLOAD_DESC,
+                       "sample": "each step: layout of the whole 32768-token batch + dispatch "
+                                 "bf16, combine and dispatch fp8 of %d tokens" % block},
+            "cpu_baseline": {"value": v, "unit": "GB/s", "kind": "oracle", "cores": 1,
+                             "sample": "%d tokens per step, %d steps, %.1f s" %
+                                       (block, args.steps, dt)},
+            "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--ref-block", type=int, default=256)
+    ap.add_argument("--tokens", type=int, default=None,
+                    help="tokens of a smaller case of the prefill shape (profiling only)")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    rank, local_rank, world = dist_env()
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return 0
+    import torch
+    import torch.distributed as dist
+    if world > 1:
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    import __graft_entry__
+    __graft_entry__.build()
+    line = run_ours(args, rank, local_rank, world)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())
