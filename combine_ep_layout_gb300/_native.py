@@ -74,6 +74,8 @@ def load_library():
     L.ep_handle_variant.argtypes = [vp, i32, c.c_char_p, i32]
     L.ep_last_error.restype = c.c_char_p
     L.ep_last_error.argtypes = []
+    L.ep_layout_noalloc.restype = c.c_int
+    L.ep_layout_noalloc.argtypes = [c.POINTER(ep_cfg_t), vp, i32] + [vp] * 8 + [vp]
     _lib = L
     return L
 
@@ -232,3 +234,19 @@ def ep_handle_status(h):
 
 def ep_handle_variant(h, step):
     return h.variant(step)
+
+
+NOALLOC_OUTPUTS = ("num_unaligned_per_expert", "num_tokens_per_rank", "psum_per_expert",
+                   "psum_per_rank", "num_recv", "dst_slot", "recv_src_metadata", "device_error")
+
+
+def ep_layout_noalloc(cfg, topk_idx, out, stream=None):
+    """Layout into caller-owned int32 CUDA tensors (dict keyed by NOALLOC_OUTPUTS);
+    the library allocates nothing for this call."""
+    n = topk_idx.shape[0]
+    assert topk_idx.dtype == torch.int64 and topk_idx.is_cuda and topk_idx.is_contiguous()
+    for k in NOALLOC_OUTPUTS:
+        assert out[k].dtype == torch.int32 and out[k].is_cuda and out[k].is_contiguous(), k
+    _check(load_library().ep_layout_noalloc(
+        ctypes.byref(cfg), _ptr(topk_idx) if n else None, n,
+        *[_ptr(out[k]) for k in NOALLOC_OUTPUTS], _stream_ptr(stream, topk_idx.device)))

@@ -75,6 +75,8 @@ int validate(const ep_cfg_t* c) {
 
 }  // namespace
 
+int epg::RecordError(int code, const char* msg) { return fail(code, msg ? msg : ""); }
+
 struct ep_handle {
   ep_cfg_t cfg;
   int device = -1;

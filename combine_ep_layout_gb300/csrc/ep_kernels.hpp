@@ -93,4 +93,8 @@ Variant<CombineLaunch> FindCombine(int hidden, int topk, bool use_weights);
 // Bytes of layout scratch for up to max_chunks chunks and `columns` = E+W columns.
 size_t LayoutScratchBytes(int max_chunks, int columns);
 
+// Record `msg` as the calling thread's ep_last_error() and return `code`
+// (for entry points defined outside ep_api.cpp).
+int RecordError(int code, const char* msg);
+
 }  // namespace epg

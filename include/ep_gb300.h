@@ -144,6 +144,43 @@ int ep_dispatch(ep_handle_t h, const void *x, void *recv_x, float *recv_scales,
 int ep_combine(ep_handle_t h, const void *y, const float *topk_weights, void *out,
                ep_stream_t stream) EP_NOEXCEPT;
 
+/* Layout without any device allocation.  The pages have no counterpart to
+ * this call; it exists for callers that cannot call cudaMalloc, for example
+ * code whose device memory is entirely owned by another framework's pool
+ * allocator, a serving loop that must not allocate after start-up, or a
+ * caller that is handed buffers but has no allocator of its own.
+ * ep_handle_create allocates the layout's outputs and scratch; this call
+ * writes the same outputs as ep_layout (same definitions, same bytes) into
+ * buffers the caller passes, and keeps its scratch in a fixed 1 MiB array
+ * compiled into the library (held by every GPU that loads the library until
+ * the process exits).
+ *   cfg                       as for ep_handle_create (dispatch_dtype,
+ *                             hidden_dim and use_weights are checked but unused)
+ *   topk_idx                  device int64 [num_tokens, K], 8-byte aligned
+ *   num_unaligned_per_expert  device int32 [E]
+ *   num_tokens_per_rank       device int32 [W]
+ *   psum_per_expert           device int32 [E+1]
+ *   psum_per_rank             device int32 [W+1]
+ *   num_recv                  device int32 [1]
+ *   dst_slot                  device int32 [num_tokens, K]
+ *   recv_src_metadata         device int32 [Rcap, K+2] (8-byte aligned when K is even)
+ *   device_error              device int32 [1]; cleared, then error bits as in
+ *                             ep_handle_status (bit 0: an id outside [-1, E) was skipped)
+ * Size limit: 2*(E+W)*ceil(num_tokens/128) + (E+W) int32 of scratch must fit
+ * in 262144 (for example 32768 tokens over 256 experts and 8 ranks need
+ * 135432); larger requests return EP_EINVAL with the sizes in the message.
+ * The first call on a device, with that device current, looks up the
+ * scratch array's address and sets the layout kernels' shared-memory limit
+ * on that device; make that first call before any stream capture.  Every
+ * call shares the scratch array: calls that may run at the same time on the
+ * GPU (unordered streams) overwrite each other's scratch and give wrong
+ * results, so order them (one stream, or events).  Allocates nothing. */
+int ep_layout_noalloc(const ep_cfg_t *cfg, const int64_t *topk_idx, int32_t num_tokens,
+                      int32_t *num_unaligned_per_expert, int32_t *num_tokens_per_rank,
+                      int32_t *psum_per_expert, int32_t *psum_per_rank, int32_t *num_recv,
+                      int32_t *dst_slot, int32_t *recv_src_metadata, int32_t *device_error,
+                      ep_stream_t stream) EP_NOEXCEPT;
+
 /* Release the handle and its device memory (cudaFree, which waits for work
  * using it to finish).  NULL is ignored. */
 void ep_handle_free(ep_handle_t h) EP_NOEXCEPT;

@@ -1,0 +1,93 @@
+"""ep_layout_noalloc: the layout entry point for callers that cannot allocate
+device memory (their memory belongs to another framework's pool, or they must
+not allocate after start-up).  It takes every output from the caller and keeps
+its scratch in a fixed array inside the library.
+
+Checked against the handle-based ep_layout, which allocates its scratch with
+cudaMalloc: the outputs must be the same bytes, on two calls in a row with
+different routings (the shared scratch keeps the previous call's contents).
+This file is collected last, and passes alone in a fresh process too.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import combine_ep_layout_gb300 as ep
+import synth
+
+
+@pytest.fixture(scope="module")
+def gpu():
+    import __graft_entry__
+    __graft_entry__.build()
+    torch.cuda.set_device(0)
+
+
+def cfg_of(wl):
+    return ep.make_cfg(wl.world_size, wl.hidden, wl.max_tok_per_rank, wl.num_expert_per_rank,
+                       wl.topk, wl.alignment, wl.dispatch_dtype, wl.use_weights)
+
+
+def noalloc_outputs(wl, n):
+    dev = "cuda"
+    E, W, K = wl.num_experts, wl.world_size, wl.topk
+    shapes = {"num_unaligned_per_expert": (E,), "num_tokens_per_rank": (W,),
+              "psum_per_expert": (E + 1,), "psum_per_rank": (W + 1,), "num_recv": (1,),
+              "dst_slot": (n, K), "recv_src_metadata": (wl.recv_capacity, K + 2),
+              "device_error": (1,)}
+    # filled with a pattern so that an output the call fails to write shows up
+    return {k: torch.full(s, -12345, dtype=torch.int32, device=dev) for k, s in shapes.items()}
+
+
+PAIRS = [
+    ("num_unaligned_per_expert", ep.FIELD_NUM_UNALIGNED_PER_EXPERT),
+    ("num_tokens_per_rank", ep.FIELD_NUM_TOKENS_PER_RANK),
+    ("psum_per_expert", ep.FIELD_PSUM_PER_EXPERT),
+    ("psum_per_rank", ep.FIELD_PSUM_PER_RANK),
+    ("num_recv", ep.FIELD_NUM_RECV),
+    ("dst_slot", ep.FIELD_DST_SLOT),
+    ("recv_src_metadata", ep.FIELD_RECV_SRC_METADATA),
+]
+
+
+@pytest.mark.gpu
+def test_noalloc_layout_matches_the_allocating_layout_on_two_calls_in_a_row(gpu):
+    calls = [synth.WORKLOADS["prefill_bf16"], synth.WORKLOADS["skewed"]]
+    for wl in calls:                       # call 1, then call 2 on the same static scratch
+        topk = synth.gen_topk(wl, mask_frac=0.01).cuda()
+        out = noalloc_outputs(wl, wl.num_tokens)
+        ep.ep_layout_noalloc(cfg_of(wl), topk, out)
+        h = ep.EpHandle(cfg_of(wl))
+        h.layout(topk)
+        torch.cuda.synchronize()
+        for name, field in PAIRS:
+            want = h.field(field).cpu().numpy()
+            got = out[name].cpu().numpy()
+            assert np.array_equal(got, want), (wl.name, name)   # integer outputs: bit-exact
+        assert int(out["device_error"].cpu()[0]) == 0
+        assert h.status() == 0
+        h.free()
+
+
+@pytest.mark.gpu
+def test_noalloc_reports_bad_expert_ids(gpu):
+    wl = synth.WORKLOADS["tiny"]
+    topk = synth.gen_topk(wl)
+    topk[0, 0] = wl.num_experts + 3
+    out = noalloc_outputs(wl, wl.num_tokens)
+    ep.ep_layout_noalloc(cfg_of(wl), topk.cuda(), out)
+    torch.cuda.synchronize()
+    assert int(out["device_error"].cpu()[0]) == ep.ERR_BAD_EXPERT
+    assert int(out["dst_slot"].cpu()[0, 0]) == -1
+
+
+def test_noalloc_rejects_requests_beyond_the_static_scratch():
+    # 64 ranks x 32 experts and 16384 tokens: 2*(2048+64)*128 + 2112 int32 > 262144
+    cfg = ep.make_cfg(64, 1024, 256, 32, 8, 1, "bf16", True)
+    L = ep.load_library()
+    dummy = ctypes.c_void_p(256)          # never dereferenced: the size check comes first
+    rc = L.ep_layout_noalloc(ctypes.byref(cfg), dummy, 16384, *([dummy] * 8), None)
+    assert rc == ep.EP_EINVAL
+    assert "static scratch" in ep.ep_last_error()
