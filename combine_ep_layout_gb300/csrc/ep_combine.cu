@@ -8,10 +8,11 @@
 // acc = +0.0f, masked k skipped.  The order is fixed, so the result is
 // bit-for-bit reproducible.
 //
-// One CTA per token; each thread owns 16-byte column chunks (8 channels) and
-// issues the loads of all K rows for a chunk before reducing them, so K row
-// fetches are in flight per thread.  Expert rows are read exactly once, so the
-// loads bypass L1 and carry an evict-first L2 hint.
+// One CTA per token; each thread owns 32-byte (16 channels) column chunks --
+// 16-byte chunks when a buffer is only 16-byte aligned -- and issues the loads
+// of all K rows for a chunk before folding them, so K row fetches are in
+// flight per thread.  Expert rows are read exactly once, so the loads bypass
+// L1 and carry an evict-first L2 hint.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -27,20 +28,46 @@ namespace {
 
 constexpr int kCombineThreads = 128;
 
-__device__ __forceinline__ uint4 ld_stream(const uint4* p, uint64_t pol) {
-  uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p), "l"(pol));
-  return v;
+template <int V>
+struct Vec {
+  uint32_t w[V];
+};
+
+template <int V>
+__device__ __forceinline__ void ld_stream(const void* p, uint64_t pol, Vec<V>& r) {
+  if constexpr (V == 8) {
+    asm volatile(
+        "ld.global.nc.L1::no_allocate.L2::cache_hint.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8], %9;"
+        : "=r"(r.w[0]), "=r"(r.w[1]), "=r"(r.w[2]), "=r"(r.w[3]), "=r"(r.w[4]), "=r"(r.w[5]),
+          "=r"(r.w[6]), "=r"(r.w[7])
+        : "l"(p), "l"(pol));
+  } else {
+    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.b32 {%0,%1,%2,%3}, [%4], %5;"
+                 : "=r"(r.w[0]), "=r"(r.w[1]), "=r"(r.w[2]), "=r"(r.w[3])
+                 : "l"(p), "l"(pol));
+  }
 }
 
-__device__ __forceinline__ void fold8(float (&acc)[8], const uint4& v, float w, bool weighted) {
-  const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+template <int V>
+__device__ __forceinline__ void st_stream(void* p, const Vec<V>& r) {
+  if constexpr (V == 8) {
+    asm volatile("st.global.cs.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(r.w[0]),
+                 "r"(r.w[1]), "r"(r.w[2]), "r"(r.w[3]), "r"(r.w[4]), "r"(r.w[5]), "r"(r.w[6]),
+                 "r"(r.w[7])
+                 : "memory");
+  } else {
+    asm volatile("st.global.cs.v4.b32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(r.w[0]), "r"(r.w[1]),
+                 "r"(r.w[2]), "r"(r.w[3])
+                 : "memory");
+  }
+}
+
+template <int V>
+__device__ __forceinline__ void fold(float (&acc)[2 * V], const Vec<V>& v, float w, bool weighted) {
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float lo = __uint_as_float(u[i] << 16);
-    const float hi = __uint_as_float(u[i] & 0xffff0000u);
+  for (int i = 0; i < V; ++i) {
+    const float lo = __uint_as_float(v.w[i] << 16);
+    const float hi = __uint_as_float(v.w[i] & 0xffff0000u);
     if (weighted) {
       acc[2 * i] = __fmaf_rn(w, lo, acc[2 * i]);
       acc[2 * i + 1] = __fmaf_rn(w, hi, acc[2 * i + 1]);
@@ -56,12 +83,14 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&b);
 }
 
-template <int HC, int KC, bool WEIGHTED>
+template <int HC, int KC, bool WEIGHTED, int V>
 __global__ void __launch_bounds__(kCombineThreads) ep_combine_kernel(CombineParams p) {
   constexpr int KM = KC ? KC : kMaxTopk;
+  constexpr int UNIT = 4 * V;  // bytes per chunk
   const int H = HC ? HC : p.hidden;
   const int K = KC ? KC : p.topk;
-  const int chunks = H / 8;  // 16-byte chunks per row
+  const int row = 2 * H;
+  const int chunks = row / UNIT;
   const int t = blockIdx.x;
 
   int32_t slot[KM];
@@ -75,41 +104,46 @@ __global__ void __launch_bounds__(kCombineThreads) ep_combine_kernel(CombinePara
       if (WEIGHTED) w[k] = __ldg(p.weights + static_cast<int64_t>(t) * K + k);
     }
   }
-  const uint4* y = static_cast<const uint4*>(p.y);
-  uint4* out = static_cast<uint4*>(p.out) + static_cast<int64_t>(t) * chunks;
+  const uint8_t* y = static_cast<const uint8_t*>(p.y);
+  uint8_t* out = static_cast<uint8_t*>(p.out) + static_cast<int64_t>(t) * row;
   const uint64_t pol = policy_evict_first();
 
   for (int c = threadIdx.x; c < chunks; c += kCombineThreads) {
-    uint4 v[KM];
+    Vec<V> v[KM];
 #pragma unroll
     for (int k = 0; k < KM; ++k)
-      if (slot[k] >= 0) v[k] = ld_stream(y + static_cast<int64_t>(slot[k]) * chunks + c, pol);
-    float acc[8];
+      if (slot[k] >= 0)
+        ld_stream<V>(y + static_cast<int64_t>(slot[k]) * row + static_cast<int64_t>(c) * UNIT, pol, v[k]);
+    float acc[2 * V];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+    for (int i = 0; i < 2 * V; ++i) acc[i] = 0.0f;
 #pragma unroll
     for (int k = 0; k < KM; ++k)
-      if (slot[k] >= 0) fold8(acc, v[k], w[k], WEIGHTED);
-    uint4 o;
-    o.x = pack_bf16x2(acc[0], acc[1]);
-    o.y = pack_bf16x2(acc[2], acc[3]);
-    o.z = pack_bf16x2(acc[4], acc[5]);
-    o.w = pack_bf16x2(acc[6], acc[7]);
-    __stcs(out + c, o);
+      if (slot[k] >= 0) fold<V>(acc, v[k], w[k], WEIGHTED);
+    Vec<V> o;
+#pragma unroll
+    for (int i = 0; i < V; ++i) o.w[i] = pack_bf16x2(acc[2 * i], acc[2 * i + 1]);
+    st_stream<V>(out + static_cast<int64_t>(c) * UNIT, o);
   }
 }
+
+inline bool aligned32(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 31u) == 0; }
 
 template <int HC, int KC, bool WEIGHTED>
 cudaError_t launch_combine(const CombineParams& p, const LaunchGeom&, cudaStream_t s) {
   if (p.num_tokens == 0) return cudaSuccess;
-  ep_combine_kernel<HC, KC, WEIGHTED><<<p.num_tokens, kCombineThreads, 0, s>>>(p);
+  // 32-byte chunks when every row start is 32-byte aligned
+  if (p.hidden % 16 == 0 && aligned32(p.y) && aligned32(p.out))
+    ep_combine_kernel<HC, KC, WEIGHTED, 8><<<p.num_tokens, kCombineThreads, 0, s>>>(p);
+  else
+    ep_combine_kernel<HC, KC, WEIGHTED, 4><<<p.num_tokens, kCombineThreads, 0, s>>>(p);
   return cudaGetLastError();
 }
 
 template <int HC, int KC, bool WEIGHTED>
 cudaError_t prepare_combine(int, int, int, LaunchGeom* g) {
   return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-      &g->blocks_per_sm, ep_combine_kernel<HC, KC, WEIGHTED>, kCombineThreads, 0);
+      &g->blocks_per_sm, ep_combine_kernel<HC, KC, WEIGHTED, 8>, kCombineThreads, 0);
 }
 
 }  // namespace

@@ -4,24 +4,24 @@
 // transport dtype is a property of the copy, not arithmetic).
 //
 // On one GPU the pages' two hops (symmetric buffer, then copy epilogue) fold
-// into one pass: read x[t] once, write it K times.  The copy never touches
-// registers: the TMA unit moves whole rows with cp.async.bulk, global ->
-// shared (one load per token) and shared -> global (K stores per token).
+// into one pass: read x[t] once, write it K times.  One CTA per token: every
+// thread loads its whole share of the row first (all loads of the row in
+// flight at once), then writes it to the K destination rows.  Accesses are
+// 32 bytes per thread (the 256-bit ld/st of the sm_100 family) when the row
+// and the buffers are 32-byte aligned, 16 bytes otherwise.
 //
-//   bf16: one warp per CTA; lane 0 drives an S-stage ring of row buffers.
-//         Loads run up to S-1 tokens ahead; a stage is refilled once the bulk
-//         stores of its previous token have finished reading it
-//         (cp.async.bulk.wait_group.read).
-//   FP8:  one producer warp (loads and stores) and kFp8ConsumerWarps
-//         consumer warps that turn the staged bf16 row into e4m3 bytes and
-//         per-128-channel fp32 scales in shared memory, once per token; the
-//         producer then stores the same bytes to all K rows.  full / ready /
-//         empty mbarriers per stage order the three roles.
+// Design note: a cp.async.bulk (TMA) ring that staged each row in shared
+// memory and issued K bulk stores moved the same bytes with one thread per CTA,
+// but saturated at ~6.0 TB/s on the prefill shape at every ring depth and CTA
+// count tried; the register copy with many CTAs per SM reaches ~6.8 TB/s,
+// above the device's pure-write rate, because the loads overlap the stores.
 //
-// Persistent grid: (#SMs x resident CTAs) CTAs, each with a contiguous run of
-// tokens whose K slots it stages in shared memory first.  Every wait is
-// bounded; on a timeout a kernel sets kErrTimeout, drains its own copies and
-// returns.
+//   bf16: a byte copy.
+//   FP8:  each 128-channel group is held by 8 (32-byte) or 16 (16-byte)
+//         consecutive lanes; amax is reduced across them with shuffles, the
+//         scale is amax/448 (IEEE division), values are x/s (IEEE division)
+//         converted with cvt.rn.satfinite.e4m3x2.f32, once per token, and the
+//         bytes plus the scale are written to every destination row.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -34,111 +34,109 @@ namespace epg {
 
 namespace {
 
-constexpr int kBf16Stages = 4;
-constexpr int kFp8Stages = 3;
-constexpr int kFp8ConsumerWarps = 4;
-constexpr int kSlotCap = 2048;  // int32 slots staged per CTA (8 KB)
+// ---- vector access ---------------------------------------------------------
 
-__host__ __device__ constexpr uint32_t align128(uint32_t v) { return (v + 127u) & ~127u; }
-
-struct Bf16Smem {
-  uint32_t row;        // row bytes
-  uint32_t row_pad;    // row stride in shared memory
-  uint32_t bars;       // offset of S mbarriers
-  uint32_t slots;      // offset of the slot table
-  uint32_t total;
+template <int V>
+struct Vec {
+  uint32_t w[V];
 };
 
-__host__ __device__ constexpr Bf16Smem bf16_smem(int hidden) {
-  const uint32_t row = 2u * hidden;
-  const uint32_t rp = align128(row);
-  const uint32_t bars = rp * kBf16Stages;
-  const uint32_t slots = bars + 8u * kBf16Stages;
-  return {row, rp, bars, slots, slots + 4u * kSlotCap};
+template <int V>
+__device__ __forceinline__ void load_stream(const void* p, Vec<V>& r) {
+  if constexpr (V == 8) {
+    asm volatile("ld.global.nc.L1::no_allocate.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(r.w[0]), "=r"(r.w[1]), "=r"(r.w[2]), "=r"(r.w[3]), "=r"(r.w[4]),
+                   "=r"(r.w[5]), "=r"(r.w[6]), "=r"(r.w[7])
+                 : "l"(p));
+  } else {
+    asm volatile("ld.global.nc.L1::no_allocate.v4.b32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.w[0]), "=r"(r.w[1]), "=r"(r.w[2]), "=r"(r.w[3])
+                 : "l"(p));
+  }
 }
 
-template <int HC, int KC>
-__global__ void __launch_bounds__(32) ep_dispatch_bf16_kernel(DispatchParams p, int tokens_per_cta) {
-  constexpr int S = kBf16Stages;
-  const int H = HC ? HC : p.hidden;
+template <int V>
+__device__ __forceinline__ void store(void* p, const Vec<V>& r) {
+  if constexpr (V == 8) {
+    asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(r.w[0]),
+                 "r"(r.w[1]), "r"(r.w[2]), "r"(r.w[3]), "r"(r.w[4]), "r"(r.w[5]), "r"(r.w[6]),
+                 "r"(r.w[7])
+                 : "memory");
+  } else {
+    asm volatile("st.global.v4.b32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(r.w[0]), "r"(r.w[1]),
+                 "r"(r.w[2]), "r"(r.w[3])
+                 : "memory");
+  }
+}
+
+// ---- geometry ----------------------------------------------------------------
+
+// Threads per CTA for a row of `chunks` vectors: the largest multiple of 32 that
+// divides it and is at most 256 (so every thread owns the same number of
+// vectors); 0 when there is none (the row is then walked in a loop).
+constexpr int threads_for(int chunks) {
+  for (int t = 256; t >= 32; t -= 32)
+    if (chunks % t == 0 && chunks / t <= 8) return t;
+  return 0;
+}
+
+constexpr int kLoopThreads = 256;
+
+// ---- bf16 -------------------------------------------------------------------
+
+template <int HC, int KC, int V>
+__global__ void __launch_bounds__(HC ? (threads_for(2 * HC / (4 * V)) ? threads_for(2 * HC / (4 * V))
+                                                                      : kLoopThreads)
+                                     : kLoopThreads)
+    ep_dispatch_bf16_kernel(DispatchParams p) {
+  constexpr int UNIT = 4 * V;  // bytes per vector
+  constexpr int KM = KC ? KC : kMaxTopk;
   const int K = KC ? KC : p.topk;
-  const Bf16Smem L = bf16_smem(H);
-  extern __shared__ __align__(128) uint8_t smem[];
-  int32_t* slots = reinterpret_cast<int32_t*>(smem + L.slots);
-
-  const int lane = threadIdx.x;
-  const int t0 = blockIdx.x * tokens_per_cta;
-  const int t1 = min(p.num_tokens, t0 + tokens_per_cta);
-  if (t0 >= t1) return;
-  const int n = t1 - t0;
-  for (int i = lane; i < n * K; i += 32) slots[i] = p.dst_slot[static_cast<int64_t>(t0) * K + i];
-  const uint32_t rows0 = smem_addr(smem);
-  const uint32_t bar0 = smem_addr(smem + L.bars);
-  if (lane == 0) {
-#pragma unroll
-    for (int s = 0; s < S; ++s) mbar_init(bar0 + 8 * s, 1);
-    fence_mbar_init();
-  }
-  __syncwarp();
-  if (lane != 0) return;
-
-  const uint8_t* xb = static_cast<const uint8_t*>(p.x) + static_cast<int64_t>(t0) * L.row;
+  const int row = 2 * (HC ? HC : p.hidden);
+  const int t = blockIdx.x;
+  const uint8_t* xr = static_cast<const uint8_t*>(p.x) + static_cast<int64_t>(t) * row;
   uint8_t* rx = static_cast<uint8_t*>(p.recv_x);
-  const uint64_t pol_x = policy_evict_first();
-  int issued = 0;
-  auto issue_load = [&](int j) {
-    const int s = j % S;
-    mbar_arrive_expect_tx(bar0 + 8 * s, L.row);
-    bulk_g2s_hint(rows0 + s * L.row_pad, xb + static_cast<int64_t>(j) * L.row, L.row, bar0 + 8 * s,
-                  pol_x);
-    ++issued;
-  };
-  const int pro = n < S ? n : S;
-  for (int j = 0; j < pro; ++j) issue_load(j);
+  const int32_t* sl = p.dst_slot + static_cast<int64_t>(t) * K;
 
-  int j = 0;
-  for (; j < n; ++j) {
-    const int s = j % S;
-    if (!mbar_wait(bar0 + 8 * s, (j / S) & 1)) break;
-    const int32_t* sl = slots + j * K;
+  constexpr int CH = HC ? 2 * HC / UNIT : 0;
+  constexpr int T = HC ? threads_for(CH) : 0;
+  if constexpr (T != 0) {
+    constexpr int PER = CH / T;
+    Vec<V> v[PER];
 #pragma unroll
-    for (int k = 0; k < (KC ? KC : kMaxTopk); ++k) {
+    for (int u = 0; u < PER; ++u)
+      load_stream<V>(xr + static_cast<int64_t>(threadIdx.x + u * T) * UNIT, v[u]);
+#pragma unroll
+    for (int k = 0; k < KM; ++k) {
       if (k >= K) break;
-      const int32_t d = sl[k];
-      if (d >= 0) bulk_s2g(rx + static_cast<int64_t>(d) * L.row, rows0 + s * L.row_pad, L.row);
+      const int32_t d = __ldg(sl + k);
+      if (d < 0) continue;
+      uint8_t* dr = rx + static_cast<int64_t>(d) * row;
+#pragma unroll
+      for (int u = 0; u < PER; ++u) store<V>(dr + static_cast<int64_t>(threadIdx.x + u * T) * UNIT, v[u]);
     }
-    bulk_commit();
-    if (j >= 1 && j - 1 + S < n) {
-      bulk_wait_read<1>();  // the stores of token j-1 have read their stage
-      issue_load(j - 1 + S);
+  } else {
+    const int chunks = row / UNIT;
+    int32_t d[KM];
+#pragma unroll
+    for (int k = 0; k < KM; ++k) d[k] = k < K ? __ldg(sl + k) : -1;
+    for (int c0 = threadIdx.x; c0 < chunks; c0 += 2 * kLoopThreads) {
+      const int c1 = c0 + kLoopThreads;
+      Vec<V> a, b;
+      load_stream<V>(xr + static_cast<int64_t>(c0) * UNIT, a);
+      if (c1 < chunks) load_stream<V>(xr + static_cast<int64_t>(c1) * UNIT, b);
+#pragma unroll
+      for (int k = 0; k < KM; ++k) {
+        if (d[k] < 0) continue;
+        uint8_t* dr = rx + static_cast<int64_t>(d[k]) * row;
+        store<V>(dr + static_cast<int64_t>(c0) * UNIT, a);
+        if (c1 < chunks) store<V>(dr + static_cast<int64_t>(c1) * UNIT, b);
+      }
     }
   }
-  if (j < n) {  // timed out: report, then let our own loads land before leaving
-    atomicOr(p.err, kErrTimeout);
-    for (int jj = j; jj < issued; ++jj) mbar_wait(bar0 + 8 * (jj % S), (jj / S) & 1);
-  }
-  bulk_wait_all<0>();
 }
 
-struct Fp8Smem {
-  uint32_t in_row, in_pad;   // bf16 input row
-  uint32_t q_row, q_pad;     // e4m3 row
-  uint32_t sc_row, sc_pad;   // scales row
-  uint32_t in, q, sc;        // region offsets
-  uint32_t bars;             // full[S], ready[S], empty[S]
-  uint32_t slots;
-  uint32_t total;
-};
-
-__host__ __device__ constexpr Fp8Smem fp8_smem(int hidden) {
-  const uint32_t in_row = 2u * hidden, q_row = hidden, sc_row = 4u * (hidden / kScaleGroup);
-  const uint32_t in_pad = align128(in_row), q_pad = align128(q_row), sc_pad = align128(sc_row);
-  const uint32_t in = 0, q = in + kFp8Stages * in_pad, sc = q + kFp8Stages * q_pad;
-  const uint32_t bars = sc + kFp8Stages * sc_pad;
-  const uint32_t slots = bars + 8u * 3 * kFp8Stages;
-  return {in_row, in_pad, q_row, q_pad, sc_row, sc_pad, in, q, sc, bars, slots,
-          slots + 4u * kSlotCap};
-}
+// ---- FP8 --------------------------------------------------------------------
 
 // Two fp32 values to packed e4m3 (round to nearest even, saturate to +-448);
 // `lo` lands in the low byte.
@@ -148,190 +146,165 @@ __device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {
   return r;
 }
 
-template <int HC, int KC>
-__global__ void __launch_bounds__(32 * (1 + kFp8ConsumerWarps))
-    ep_dispatch_fp8_kernel(DispatchParams p, int tokens_per_cta) {
-  constexpr int S = kFp8Stages;
-  constexpr int NC = kFp8ConsumerWarps;
+// Quantise the 2V bf16 values of one vector with the scale of its 128-channel
+// group; `lanes` consecutive lanes (a power of two) hold the group.  Every lane
+// of the warp must call this (the reduction is a full-warp shuffle).
+template <int V>
+__device__ __forceinline__ void quantise(const Vec<V>& in, int lanes, uint32_t (&q)[V / 2],
+                                         float& scale) {
+  float f[2 * V];
+#pragma unroll
+  for (int i = 0; i < V; ++i) {
+    f[2 * i] = __uint_as_float(in.w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(in.w[i] & 0xffff0000u);
+  }
+  uint32_t a = 0;
+#pragma unroll
+  for (int i = 0; i < 2 * V; ++i) {
+    uint32_t b = __float_as_uint(f[i]) & 0x7fffffffu;
+    b = b > 0x7f800000u ? 0u : b;  // NaN does not take part in the maximum
+    a = b > a ? b : a;
+  }
+  for (int o = 1; o < lanes; o <<= 1) {
+    const uint32_t other = __shfl_xor_sync(0xffffffffu, a, o);
+    a = other > a ? other : a;
+  }
+  scale = 0.0f;
+#pragma unroll
+  for (int i = 0; i < V / 2; ++i) q[i] = 0u;
+  if (a != 0u) {
+    scale = __fdiv_rn(__uint_as_float(a), 448.0f);
+#pragma unroll
+    for (int i = 0; i < V / 2; ++i) {
+      const float r0 = __fdiv_rn(f[4 * i], scale), r1 = __fdiv_rn(f[4 * i + 1], scale);
+      const float r2 = __fdiv_rn(f[4 * i + 2], scale), r3 = __fdiv_rn(f[4 * i + 3], scale);
+      q[i] = cvt_e4m3x2(r0, r1) | (cvt_e4m3x2(r2, r3) << 16);
+    }
+  }
+}
+
+template <int V>
+__device__ __forceinline__ void store_q(void* p, const uint32_t (&q)[V / 2]) {
+  if constexpr (V == 8) {
+    asm volatile("st.global.v4.b32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(q[0]), "r"(q[1]), "r"(q[2]),
+                 "r"(q[3])
+                 : "memory");
+  } else {
+    asm volatile("st.global.v2.b32 [%0], {%1,%2};" ::"l"(p), "r"(q[0]), "r"(q[1]) : "memory");
+  }
+}
+
+template <int HC, int KC, int V>
+__global__ void __launch_bounds__(HC ? (threads_for(2 * HC / (4 * V)) ? threads_for(2 * HC / (4 * V))
+                                                                      : kLoopThreads)
+                                     : kLoopThreads)
+    ep_dispatch_fp8_kernel(DispatchParams p) {
+  constexpr int UNIT = 4 * V;            // input bytes per vector (2V channels)
+  constexpr int LANES = 128 / (2 * V);   // lanes per 128-channel group
+  constexpr int KM = KC ? KC : kMaxTopk;
   const int H = HC ? HC : p.hidden;
   const int K = KC ? KC : p.topk;
   const int G = H / kScaleGroup;
-  const Fp8Smem L = fp8_smem(H);
-  const bool sc_bulk = (L.sc_row % 16u) == 0;
-  extern __shared__ __align__(128) uint8_t smem[];
-  int32_t* slots = reinterpret_cast<int32_t*>(smem + L.slots);
-
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int t0 = blockIdx.x * tokens_per_cta;
-  const int t1 = min(p.num_tokens, t0 + tokens_per_cta);
-  if (t0 >= t1) return;
-  const int n = t1 - t0;
-  for (int i = tid; i < n * K; i += blockDim.x) slots[i] = p.dst_slot[static_cast<int64_t>(t0) * K + i];
-  const uint32_t full0 = smem_addr(smem + L.bars);
-  const uint32_t ready0 = full0 + 8 * S;
-  const uint32_t empty0 = ready0 + 8 * S;
-  if (tid == 0) {
-#pragma unroll
-    for (int s = 0; s < S; ++s) {
-      mbar_init(full0 + 8 * s, 1);
-      mbar_init(ready0 + 8 * s, NC);
-      mbar_init(empty0 + 8 * s, 1);
-    }
-    fence_mbar_init();
-  }
-  __syncthreads();
-
+  const int t = blockIdx.x;
+  const uint8_t* xr = static_cast<const uint8_t*>(p.x) + static_cast<int64_t>(t) * 2 * H;
   uint8_t* rq = static_cast<uint8_t*>(p.recv_x);
   float* rs = p.recv_scales;
+  const int32_t* sl = p.dst_slot + static_cast<int64_t>(t) * K;
+  const bool leader = (threadIdx.x % LANES) == 0;
 
-  if (warp == 0) {
-    // ---------------- producer ----------------
-    if (lane != 0) return;
-    const uint8_t* xb = static_cast<const uint8_t*>(p.x) + static_cast<int64_t>(t0) * L.in_row;
-    const uint32_t in0 = smem_addr(smem + L.in), q0 = smem_addr(smem + L.q),
-                   sc0 = smem_addr(smem + L.sc);
-    const uint64_t pol_x = policy_evict_first();
-    int issued = 0;
-    auto issue_load = [&](int j) {
-      const int s = j % S;
-      mbar_arrive_expect_tx(full0 + 8 * s, L.in_row);
-      bulk_g2s_hint(in0 + s * L.in_pad, xb + static_cast<int64_t>(j) * L.in_row, L.in_row,
-                    full0 + 8 * s, pol_x);
-      ++issued;
-    };
-    const int pro = n < S ? n : S;
-    for (int j = 0; j < pro; ++j) issue_load(j);
-    int j = 0;
-    for (; j < n; ++j) {
-      const int s = j % S;
-      if (!mbar_wait(ready0 + 8 * s, (j / S) & 1)) break;
-      const int32_t* sl = slots + j * K;
+  constexpr int CH = HC ? 2 * HC / UNIT : 0;
+  constexpr int T = HC ? threads_for(CH) : 0;
+  if constexpr (T != 0) {
+    constexpr int PER = CH / T;
+    Vec<V> v[PER];
 #pragma unroll
-      for (int k = 0; k < (KC ? KC : kMaxTopk); ++k) {
-        if (k >= K) break;
-        const int32_t d = sl[k];
-        if (d < 0) continue;
-        bulk_s2g(rq + static_cast<int64_t>(d) * L.q_row, q0 + s * L.q_pad, L.q_row);
-        if (sc_bulk)
-          bulk_s2g(reinterpret_cast<uint8_t*>(rs) + static_cast<int64_t>(d) * L.sc_row,
-                   sc0 + s * L.sc_pad, L.sc_row);
-      }
-      bulk_commit();
-      if (j + S < n) issue_load(j + S);  // consumers are done with the input stage
-      if (j >= 1) {
-        bulk_wait_read<1>();               // stores of token j-1 have read their stage
-        mbar_arrive(empty0 + 8 * ((j - 1) % S));
-      }
-    }
-    if (j < n) {
-      atomicOr(p.err, kErrTimeout);
-      for (int jj = j; jj < issued; ++jj) mbar_wait(full0 + 8 * (jj % S), (jj / S) & 1);
-    }
-    bulk_wait_all<0>();
-    return;
-  }
-
-  // ---------------- consumers: bf16 -> e4m3 + scales ----------------
-  const int cw = warp - 1;
-  for (int j = 0; j < n; ++j) {
-    const int s = j % S;
-    if (!mbar_wait(full0 + 8 * s, (j / S) & 1)) { atomicOr(p.err, kErrTimeout); return; }
-    if (j >= S && !mbar_wait(empty0 + 8 * s, ((j / S) - 1) & 1)) {
-      atomicOr(p.err, kErrTimeout);
-      return;
-    }
-    const uint8_t* in_s = smem + L.in + s * L.in_pad;
-    uint8_t* q_s = smem + L.q + s * L.q_pad;
-    float* sc_s = reinterpret_cast<float*>(smem + L.sc + s * L.sc_pad);
-    for (int g = cw; g < G; g += NC) {
-      const uint2 raw = *reinterpret_cast<const uint2*>(in_s + g * 256 + lane * 8);
-      float f[4];
-      f[0] = __uint_as_float(raw.x << 16);
-      f[1] = __uint_as_float(raw.x & 0xffff0000u);
-      f[2] = __uint_as_float(raw.y << 16);
-      f[3] = __uint_as_float(raw.y & 0xffff0000u);
-      uint32_t a = 0;
+    for (int u = 0; u < PER; ++u)
+      load_stream<V>(xr + static_cast<int64_t>(threadIdx.x + u * T) * UNIT, v[u]);
+    uint32_t q[PER][V / 2];
+    float s[PER];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        uint32_t b = __float_as_uint(f[i]) & 0x7fffffffu;
-        b = b > 0x7f800000u ? 0u : b;  // NaN does not take part in the maximum
-        a = b > a ? b : a;
-      }
-      a = __reduce_max_sync(0xffffffffu, a);
-      float sc = 0.0f;
-      uint32_t q4 = 0;
-      if (a != 0u) {
-        sc = __fdiv_rn(__uint_as_float(a), 448.0f);
-        const float r0 = __fdiv_rn(f[0], sc), r1 = __fdiv_rn(f[1], sc);
-        const float r2 = __fdiv_rn(f[2], sc), r3 = __fdiv_rn(f[3], sc);
-        q4 = cvt_e4m3x2(r0, r1) | (cvt_e4m3x2(r2, r3) << 16);
-      }
-      *reinterpret_cast<uint32_t*>(q_s + g * 128 + lane * 4) = q4;
-      if (lane == 0) {
-        sc_s[g] = sc;
-        if (!sc_bulk) {
-          const int32_t* sl = slots + j * K;
-          for (int k = 0; k < K; ++k)
-            if (sl[k] >= 0) rs[static_cast<int64_t>(sl[k]) * G + g] = sc;
-        }
+    for (int u = 0; u < PER; ++u) quantise<V>(v[u], LANES, q[u], s[u]);
+#pragma unroll
+    for (int k = 0; k < KM; ++k) {
+      if (k >= K) break;
+      const int32_t d = __ldg(sl + k);
+      if (d < 0) continue;
+#pragma unroll
+      for (int u = 0; u < PER; ++u) {
+        const int c = threadIdx.x + u * T;
+        store_q<V>(rq + static_cast<int64_t>(d) * H + static_cast<int64_t>(c) * (2 * V), q[u]);
+        if (leader) rs[static_cast<int64_t>(d) * G + c / LANES] = s[u];
       }
     }
-    fence_proxy_async_smem();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(ready0 + 8 * s);
+  } else {
+    const int chunks = 2 * H / UNIT;
+    int32_t d[KM];
+#pragma unroll
+    for (int k = 0; k < KM; ++k) d[k] = k < K ? __ldg(sl + k) : -1;
+    for (int c0 = 0; c0 < chunks; c0 += kLoopThreads) {  // uniform trip count: shuffles see every lane
+      const int c = c0 + threadIdx.x;
+      const bool in = c < chunks;
+      Vec<V> v;
+#pragma unroll
+      for (int i = 0; i < V; ++i) v.w[i] = 0u;
+      if (in) load_stream<V>(xr + static_cast<int64_t>(c) * UNIT, v);
+      uint32_t q[V / 2];
+      float s;
+      quantise<V>(v, LANES, q, s);
+      if (!in) continue;
+#pragma unroll
+      for (int k = 0; k < KM; ++k) {
+        if (d[k] < 0) continue;
+        store_q<V>(rq + static_cast<int64_t>(d[k]) * H + static_cast<int64_t>(c) * (2 * V), q);
+        if (leader) rs[static_cast<int64_t>(d[k]) * G + c / LANES] = s;
+      }
+    }
   }
 }
 
-// Persistent grid: CTAs resident at once, each with a contiguous run of tokens,
-// no more than kSlotCap / K tokens per CTA.
-inline void persistent_split(int num_tokens, int topk, const LaunchGeom& g, int* grid, int* per) {
-  const int resident = g.num_sms * (g.blocks_per_sm > 0 ? g.blocks_per_sm : 1);
-  int tpc = (num_tokens + resident - 1) / resident;
-  const int cap = kSlotCap / topk;
-  if (tpc > cap) tpc = cap;
-  if (tpc < 1) tpc = 1;
-  *per = tpc;
-  *grid = (num_tokens + tpc - 1) / tpc;
+// ---- launchers -------------------------------------------------------------
+
+constexpr int block_for(int hidden_c, int v) {
+  return hidden_c ? (threads_for(2 * hidden_c / (4 * v)) ? threads_for(2 * hidden_c / (4 * v))
+                                                         : kLoopThreads)
+                  : kLoopThreads;
 }
+
+inline bool aligned32(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 31u) == 0; }
 
 template <int HC, int KC>
-cudaError_t launch_bf16(const DispatchParams& p, const LaunchGeom& g, cudaStream_t s) {
+cudaError_t launch_bf16(const DispatchParams& p, const LaunchGeom&, cudaStream_t s) {
   if (p.num_tokens == 0) return cudaSuccess;
-  int grid, per;
-  persistent_split(p.num_tokens, p.topk, g, &grid, &per);
-  const Bf16Smem L = bf16_smem(p.hidden);
-  ep_dispatch_bf16_kernel<HC, KC><<<grid, 32, L.total, s>>>(p, per);
+  // 32-byte vectors when every row start is 32-byte aligned
+  const bool v8 = (p.hidden % 16 == 0) && aligned32(p.x) && aligned32(p.recv_x);
+  if (v8)
+    ep_dispatch_bf16_kernel<HC, KC, 8><<<p.num_tokens, block_for(HC, 8), 0, s>>>(p);
+  else
+    ep_dispatch_bf16_kernel<HC, KC, 4><<<p.num_tokens, block_for(HC, 4), 0, s>>>(p);
   return cudaGetLastError();
 }
 
 template <int HC, int KC>
-cudaError_t prepare_bf16(int hidden, int, int, LaunchGeom* g) {
-  const Bf16Smem L = bf16_smem(hidden);
-  cudaError_t e = cudaFuncSetAttribute(ep_dispatch_bf16_kernel<HC, KC>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, L.total);
-  if (e != cudaSuccess) return e;
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(&g->blocks_per_sm,
-                                                       ep_dispatch_bf16_kernel<HC, KC>, 32, L.total);
-}
-
-template <int HC, int KC>
-cudaError_t launch_fp8(const DispatchParams& p, const LaunchGeom& g, cudaStream_t s) {
-  if (p.num_tokens == 0) return cudaSuccess;
-  int grid, per;
-  persistent_split(p.num_tokens, p.topk, g, &grid, &per);
-  const Fp8Smem L = fp8_smem(p.hidden);
-  ep_dispatch_fp8_kernel<HC, KC><<<grid, 32 * (1 + kFp8ConsumerWarps), L.total, s>>>(p, per);
-  return cudaGetLastError();
-}
-
-template <int HC, int KC>
-cudaError_t prepare_fp8(int hidden, int, int, LaunchGeom* g) {
-  const Fp8Smem L = fp8_smem(hidden);
-  cudaError_t e = cudaFuncSetAttribute(ep_dispatch_fp8_kernel<HC, KC>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, L.total);
-  if (e != cudaSuccess) return e;
+cudaError_t prepare_bf16(int, int, int, LaunchGeom* g) {
   return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-      &g->blocks_per_sm, ep_dispatch_fp8_kernel<HC, KC>, 32 * (1 + kFp8ConsumerWarps), L.total);
+      &g->blocks_per_sm, ep_dispatch_bf16_kernel<HC, KC, 8>, block_for(HC, 8), 0);
+}
+
+template <int HC, int KC>
+cudaError_t launch_fp8(const DispatchParams& p, const LaunchGeom&, cudaStream_t s) {
+  if (p.num_tokens == 0) return cudaSuccess;
+  // hidden % 128 == 0 here, so 32-byte input vectors only need an aligned x
+  if (aligned32(p.x))
+    ep_dispatch_fp8_kernel<HC, KC, 8><<<p.num_tokens, block_for(HC, 8), 0, s>>>(p);
+  else
+    ep_dispatch_fp8_kernel<HC, KC, 4><<<p.num_tokens, block_for(HC, 4), 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+template <int HC, int KC>
+cudaError_t prepare_fp8(int, int, int, LaunchGeom* g) {
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+      &g->blocks_per_sm, ep_dispatch_fp8_kernel<HC, KC, 8>, block_for(HC, 8), 0);
 }
 
 }  // namespace

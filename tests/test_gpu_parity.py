@@ -435,3 +435,49 @@ def test_misaligned_buffers_are_rejected():
     with pytest.raises(ep.EpError) as e:
         h.dispatch(x[1:1 + wl.num_tokens * wl.hidden], recv)
     assert e.value.code == ep.EP_EINVAL
+
+
+@pytest.mark.parametrize("name", ["tiny", "decode"])
+def test_sixteen_byte_aligned_buffers_take_the_16_byte_path(name):
+    """Buffers that are 16- but not 32-byte aligned are served with 16-byte
+    accesses; results are the same bytes."""
+    wl = synth.WORKLOADS[name]
+    case = synth.make_case(wl, device="cuda")
+    H, R, N = wl.hidden, wl.recv_capacity, wl.num_tokens
+    ref = oracle_layout(wl, case["topk_idx"].numpy())
+
+    def off16(shape, dtype, fill=0):
+        n = int(np.prod(shape))
+        per = 16 // torch.tensor([], dtype=dtype).element_size()
+        base = torch.full((n + 2 * per,), fill, dtype=dtype, device="cuda")
+        t = base[per:per + n].view(shape)
+        assert t.data_ptr() % 32 == 16
+        return t
+
+    x = off16((N, H), torch.bfloat16)
+    x.copy_(case["x"])
+    # bf16 dispatch + combine
+    h = ep.EpHandle(cfg_of(wl, "bf16"))
+    h.layout(case["topk_idx"].cuda())
+    recv = off16((R, H), torch.bfloat16)
+    h.dispatch(x, recv)
+    out = off16((N, H), torch.bfloat16)
+    h.combine(recv, case["topk_weights"].cuda(), out)
+    torch.cuda.synchronize()
+    rx = np.zeros((R, H), np.uint16)
+    oracle.dispatch_bf16(synth.bits16(case["x"]), ref["dst_slot"], rx)
+    assert np.array_equal(synth.bits16(recv), rx)
+    assert np.array_equal(synth.bits16(out),
+                          oracle.combine(rx, ref["dst_slot"], case["topk_weights"].numpy()))
+    # FP8 dispatch from a 16-byte-aligned x
+    h8 = ep.EpHandle(cfg_of(wl, "fp8"))
+    h8.layout(case["topk_idx"].cuda())
+    rq = torch.zeros((R, H), dtype=torch.uint8, device="cuda")
+    rs = torch.zeros((R, H // 128), dtype=torch.float32, device="cuda")
+    h8.dispatch(x, rq, rs)
+    torch.cuda.synchronize()
+    q = np.zeros((R, H), np.uint8)
+    s = np.zeros((R, H // 128), np.float32)
+    oracle.dispatch_fp8(synth.bits16(case["x"]), ref["dst_slot"], q, s)
+    assert np.array_equal(rq.cpu().numpy(), q)
+    assert np.array_equal(rs.cpu().numpy().view(np.uint32), s.view(np.uint32))
