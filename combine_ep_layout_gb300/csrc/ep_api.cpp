@@ -88,7 +88,7 @@ struct ep_handle {
   void* block = nullptr;
   int32_t *cnt = nullptr, *tok_per_rank = nullptr, *psum_expert = nullptr, *psum_rank = nullptr,
           *num_recv = nullptr, *err = nullptr, *dst_slot = nullptr, *meta = nullptr,
-          *chunk_hist = nullptr, *chunk_off = nullptr, *col_total = nullptr;
+          *scratch = nullptr;
   Variant<LayoutLaunch> layout{};
   Variant<DispatchLaunch> dispatch{};
   Variant<CombineLaunch> combine{};
@@ -174,7 +174,7 @@ int ep_handle_create(const ep_cfg_t* cfg, ep_handle_t* out) noexcept {
     const size_t n_small = al(4 * (h->E + h->W + (h->E + 1) + (h->W + 1) + 2));
     const size_t n_slot = al(4 * static_cast<size_t>(h->max_tokens) * h->K);
     const size_t n_meta = al(4 * static_cast<size_t>(h->rcap) * (h->K + 2));
-    const size_t n_scr = al(LayoutScratchBytes(h->max_chunks, cols));
+    const size_t n_scr = al(sizeof(int32_t) * static_cast<size_t>(LayoutScratchInts(h->max_chunks, cols)));
     e = cudaMalloc(&h->block, n_small + n_slot + n_meta + n_scr);
     if (e != cudaSuccess) {
       cudaGetLastError();
@@ -191,10 +191,7 @@ int ep_handle_create(const ep_cfg_t* cfg, ep_handle_t* out) noexcept {
     h->err = h->num_recv + 1;
     h->dst_slot = reinterpret_cast<int32_t*>(b + n_small);
     h->meta = reinterpret_cast<int32_t*>(b + n_small + n_slot);
-    int32_t* scr = reinterpret_cast<int32_t*>(b + n_small + n_slot + n_meta);
-    h->chunk_hist = scr;
-    h->chunk_off = scr + static_cast<size_t>(cols) * (h->max_chunks > 0 ? h->max_chunks : 1);
-    h->col_total = h->chunk_off + static_cast<size_t>(cols) * (h->max_chunks > 0 ? h->max_chunks : 1);
+    h->scratch = reinterpret_cast<int32_t*>(b + n_small + n_slot + n_meta);
     if ((e = cudaMemset(h->block, 0, n_small + n_slot + n_meta + n_scr)) != cudaSuccess)
       return bail(fail_cuda(e, "cudaMemset"));
     if ((e = cudaDeviceSynchronize()) != cudaSuccess) return bail(fail_cuda(e, "cudaDeviceSynchronize"));
@@ -236,9 +233,8 @@ int ep_layout(ep_handle_t h, const int64_t* topk_idx, int32_t num_tokens, ep_str
     p.dst_slot = h->dst_slot;
     p.meta = h->meta;
     p.err = h->err;
-    p.chunk_hist = h->chunk_hist;
-    p.chunk_off = h->chunk_off;
-    p.col_total = h->col_total;
+    p.epr_magic = RankMagic(h->Epr);
+    BindLayoutScratch(&p, h->scratch, h->max_chunks, h->E + h->W);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e = h->layout.launch(p, h->g_layout, s);
     if (e != cudaSuccess) return fail_cuda(e, "layout launch");

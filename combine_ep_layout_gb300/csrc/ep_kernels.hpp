@@ -38,7 +38,8 @@ struct LayoutParams {
   int32_t* dst_slot;         // [N, K]
   int32_t* meta;             // [rcap, K+2]
   int32_t* err;              // [1]
-  // scratch (handle): per-chunk column histograms, column-major [E+W][C]
+  uint32_t epr_magic;        // RankMagic(num_expert_per_rank)
+  // scratch (BindLayoutScratch): per-chunk column histograms, column-major [E+W][C]
   int32_t* chunk_hist;
   int32_t* chunk_off;        // exclusive prefix over chunks, [E+W][C]
   int32_t* col_total;        // [E+W]
@@ -90,8 +91,13 @@ Variant<LayoutLaunch> FindLayout(int topk);
 Variant<DispatchLaunch> FindDispatch(int hidden, int topk, EpDType dtype);
 Variant<CombineLaunch> FindCombine(int hidden, int topk, bool use_weights);
 
-// Bytes of layout scratch for up to max_chunks chunks and `columns` = E+W columns.
-size_t LayoutScratchBytes(int max_chunks, int columns);
+// int32 words of layout scratch for up to max_chunks chunks and `columns` = E+W
+// columns: [chunk_hist] [chunk_off], each [columns][max_chunks], then [columns] totals.
+int64_t LayoutScratchInts(int max_chunks, int columns);
+// Point p's scratch fields into `base` (LayoutScratchInts(max_chunks, columns) words).
+void BindLayoutScratch(LayoutParams* p, int32_t* base, int max_chunks, int columns);
+// Magic multiplier for dividing an expert id by num_expert_per_rank on the device.
+uint32_t RankMagic(int num_expert_per_rank);
 
 // Record `msg` as the calling thread's ep_last_error() and return `code`
 // (for entry points defined outside ep_api.cpp).

@@ -6,23 +6,31 @@
 //
 // Rows of one expert are ordered by the flat index t*K+k, so the slot of an
 // entry is psum_expert[e] + (number of earlier entries routed to e): a stable
-// counting sort.  Three launches, no device-side waiting:
+// counting sort.  Three launches, the last two with programmatic dependent
+// launch so that each is scheduled while its predecessor drains:
 //
-//   count  one CTA per chunk of kLayoutTPC tokens.  Each warp histograms a
-//          contiguous run of the chunk's entries in shared memory, combining
-//          lanes that carry the same expert with __match_any_sync (one update
-//          per distinct expert per 32 entries, which keeps hot experts of a
-//          skewed routing from serialising).  An exclusive scan across the
-//          warps gives each warp its start per expert; a second pass over the
-//          same entries gives each entry its stable rank within the chunk.
-//          The chunk's column totals (E experts + W ranks) go to a
-//          column-major [E+W][C] table.
-//   spine  one warp per column: exclusive scan over the C chunks.
-//   slots  each CTA rebuilds the aligned exclusive prefix over experts from
-//          the column totals (E values, cheaper than another launch), then
-//          turns every entry's in-chunk rank into its slot and writes the
-//          metadata rows; extra CTAs write -1 into every row that receives
-//          nothing.
+//   count  one CTA per chunk of kLayoutTPC tokens.  The chunk's ids are staged
+//          in shared memory with one coalesced load and every pass runs from
+//          there.  Per-warp histograms over contiguous runs of entries use
+//          shared-memory atomics; an exclusive scan across the warps gives each
+//          warp its start per expert, and a pass over 32-entry batches that
+//          combines lanes carrying the same expert with __match_any_sync gives
+//          each entry its stable rank in the chunk.  Tokens per rank: each
+//          entry ORs its rank bit into its token's mask, then warp ballots
+//          count the set bits.  The chunk's column totals (E experts + W ranks)
+//          go to a column-major [E+W][C] table.
+//   spine  a warp per column scans the C chunk totals (chunk offsets and
+//          column totals).
+//   slots  every CTA rebuilds the aligned exclusive prefix over the experts
+//          from the column totals (E values, cheaper than another launch) and
+//          CTA 0 writes the counts, the prefix sums and the number of receive
+//          rows.  One CTA per chunk turns ranks into slots (dst_slot), sorts the
+//          chunk's entries by (expert, rank) in shared memory and writes their
+//          metadata rows through a flat index: the rows of one expert from one
+//          chunk are contiguous, so consecutive threads write consecutive words.
+//          Every CTA also writes -1 into its share of the rows that receive
+//          nothing (expert padding and [R, capacity)).
+// No kernel waits on another CTA.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -37,64 +45,125 @@ namespace {
 
 constexpr int kCountThreads = kLayoutCountWarps * 32;
 constexpr int kSpineWarps = 8;
-constexpr int kSlotThreads = kLayoutTPC;  // one token per thread
+constexpr int kSlotThreads = 256;
 
 __device__ __forceinline__ int expert_of(int64_t v, int E) {
   return (v >= 0 && v < E) ? static_cast<int>(v) : -1;
 }
 
+// Rank of expert e, e / Epr, as a multiply-high with the magic number of
+// RankMagic (0 when Epr == 1).
+__device__ __forceinline__ int rank_of(int e, uint32_t magic) {
+  return magic ? static_cast<int>(__umulhi(static_cast<uint32_t>(e), magic)) : e;
+}
+
+// Let the next kernel of the stream (launched with programmatic stream
+// serialisation) be scheduled; it waits for this grid's completion itself.
+__device__ __forceinline__ void allow_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Wait until the preceding grid of the stream has completed and its writes are visible.
+__device__ __forceinline__ void wait_for_preceding_grid() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Block-wide exclusive scan of align(v[e], A) for e in [0, n) into out[0..n]
+// (out[n] = total).  warp_tot needs 33 words.  All threads must call it.
+__device__ void block_exclusive_scan(const int32_t* v, int n, int A, int32_t* out,
+                                     int32_t* warp_tot) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int nthr = blockDim.x, nwarp = nthr >> 5;
+  const int V = (n + nthr - 1) / nthr;
+  const int beg = min(n, tid * V), end = min(n, beg + V);
+  int sum = 0;
+  for (int e = beg; e < end; ++e) sum += (v[e] + A - 1) / A * A;
+  int incl = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) warp_tot[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const int w = lane < nwarp ? warp_tot[lane] : 0;
+    int s = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, s, o);
+      if (lane >= o) s += y;
+    }
+    if (lane < nwarp) warp_tot[lane] = s - w;  // exclusive warp offsets
+    if (lane == nwarp - 1) warp_tot[32] = s;  // grand total
+  }
+  __syncthreads();
+  int run = warp_tot[warp] + incl - sum;
+  for (int e = beg; e < end; ++e) {
+    out[e] = run;
+    run += (v[e] + A - 1) / A * A;
+  }
+  if (tid == 0) out[n] = warp_tot[32];
+  __syncthreads();
+}
+
+// ---------------------------------------------------------------- count
+
 template <int KC>
 __global__ void __launch_bounds__(kCountThreads) ep_layout_count_kernel(LayoutParams p) {
   constexpr int NW = kLayoutCountWarps;
   const int K = KC ? KC : p.topk;
-  const int E = p.num_experts;
-  const int EW = E + p.world_size;
+  const int E = p.num_experts, W = p.world_size;
+  const int EW = E + W;
   const int C = p.num_chunks;
-  extern __shared__ int32_t whist[];  // [NW][EW] per-warp counts, then per-warp starts
+  extern __shared__ int32_t sm[];
+  int32_t* whist = sm;                                     // [NW][EW]
+  int32_t* ids = whist + NW * EW;                          // [TPC*K] expert ids, -1 = skip
+  unsigned long long* tokmask =                            // [TPC] ranks touched by a token
+      reinterpret_cast<unsigned long long*>(ids + ((kLayoutTPC * K + 1) & ~1));
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int c = blockIdx.x;
   const int t0 = c * kLayoutTPC;
-  const int t1 = min(p.num_tokens, t0 + kLayoutTPC);
-  const int nent = (t1 - t0) * K;
+  const int ntok = min(p.num_tokens, t0 + kLayoutTPC) - t0;
+  const int nent = ntok * K;
   const int64_t* topk = p.topk_idx + static_cast<int64_t>(t0) * K;
 
+  allow_dependents();
+  bool bad = false;
+  for (int i = tid; i < nent; i += kCountThreads) {
+    const int64_t v = topk[i];
+    const int e = expert_of(v, E);
+    bad |= (e < 0 && v != -1);
+    ids[i] = e;
+  }
   for (int i = tid; i < NW * EW; i += kCountThreads) whist[i] = 0;
+  for (int i = tid; i < kLayoutTPC; i += kCountThreads) tokmask[i] = 0ull;
   __syncthreads();
 
-  // contiguous run of entries per warp, whole 32-entry batches
+  // per-warp histogram over a contiguous run of entries (whole 32-entry batches)
   const int per_warp = (((nent + NW - 1) / NW) + 31) & ~31;
   const int wbeg = warp * per_warp;
   const int wend = min(nent, wbeg + per_warp);
   int32_t* wh = whist + warp * EW;
-
-  bool bad = false;
-  for (int i = wbeg; i < wend; i += 32) {
-    const int idx = i + lane;
-    int e = -1;
-    if (idx < wend) {
-      const int64_t v = topk[idx];
-      e = expert_of(v, E);
-      bad |= (e < 0 && v != -1);
-    }
-    const unsigned peers = __match_any_sync(0xffffffffu, e);
-    if (e >= 0 && lane == __ffs(peers) - 1) wh[e] += __popc(peers);
-    __syncwarp();
+  for (int i = wbeg + lane; i < wend; i += 32) {
+    const int e = ids[i];
+    if (e >= 0) atomicAdd(&wh[e], 1);
   }
+  // ranks touched by each token
+  for (int i = tid; i < nent; i += kCountThreads) {
+    const int e = ids[i];
+    if (e >= 0) atomicOr(&tokmask[i / K], 1ull << rank_of(e, p.epr_magic));
+  }
+  __syncthreads();
 
-  // tokens that touch each rank (a token counts once per rank)
-  const int Epr = p.num_expert_per_rank;
-  for (int t = t0 + tid; t < t1; t += kCountThreads) {
-    uint64_t mask = 0;
-    const int64_t* row = p.topk_idx + static_cast<int64_t>(t) * K;
-    for (int k = 0; k < K; ++k) {
-      const int e = expert_of(row[k], E);
-      if (e >= 0) mask |= 1ull << (e / Epr);
-    }
-    while (mask) {
-      const int r = __ffsll(static_cast<long long>(mask)) - 1;
-      mask &= mask - 1;
-      atomicAdd(&whist[E + r], 1);
+  // tokens per rank: warp ballots over the token masks
+  for (int tl0 = warp * 32; tl0 < ntok; tl0 += kCountThreads) {
+    const int tl = tl0 + lane;
+    const unsigned long long mask = tl < ntok ? tokmask[tl] : 0ull;
+    for (int r = 0; r < W; ++r) {
+      const int n = __popc(__ballot_sync(0xffffffffu, (mask >> r) & 1ull));
+      if (lane == 0 && n) atomicAdd(&whist[E + r], n);
     }
   }
   __syncthreads();
@@ -116,7 +185,7 @@ __global__ void __launch_bounds__(kCountThreads) ep_layout_count_kernel(LayoutPa
   int32_t* local = p.dst_slot + static_cast<int64_t>(t0) * K;
   for (int i = wbeg; i < wend; i += 32) {
     const int idx = i + lane;
-    const int e = idx < wend ? expert_of(topk[idx], E) : -1;
+    const int e = idx < wend ? ids[idx] : -1;
     const unsigned peers = __match_any_sync(0xffffffffu, e);
     const int base = e >= 0 ? wh[e] : 0;
     const int rank = base + __popc(peers & lanemask_lt());
@@ -128,19 +197,34 @@ __global__ void __launch_bounds__(kCountThreads) ep_layout_count_kernel(LayoutPa
   if (bad) atomicOr(p.err, kErrBadExpert);
 }
 
-// One warp per column j of the [E+W][C] table: exclusive scan over chunks.
+// ---------------------------------------------------------------- spine
+
+// A warp per column j of the [E+W][C] table: exclusive scan over the C chunks
+// (each lane a contiguous run of chunks, kept in registers when short).
 __global__ void __launch_bounds__(kSpineWarps * 32) ep_layout_spine_kernel(LayoutParams p) {
   const int EW = p.num_experts + p.world_size;
   const int C = p.num_chunks;
   const int j = blockIdx.x * kSpineWarps + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
+  allow_dependents();
+  wait_for_preceding_grid();
   if (j >= EW) return;
   const int32_t* in = p.chunk_hist + static_cast<int64_t>(j) * C;
   int32_t* out = p.chunk_off + static_cast<int64_t>(j) * C;
-  const int V = (C + 31) / 32;  // a contiguous run of chunks per lane
+  constexpr int kRegRun = 8;
+  const int V = (C + 31) / 32;
   const int cbeg = min(C, lane * V), cend = min(C, cbeg + V);
   int sum = 0;
-  for (int c = cbeg; c < cend; ++c) sum += in[c];
+  int reg[kRegRun];
+  if (V <= kRegRun) {
+#pragma unroll
+    for (int u = 0; u < kRegRun; ++u) {
+      reg[u] = cbeg + u < cend ? in[cbeg + u] : 0;
+      sum += reg[u];
+    }
+  } else {
+    for (int c = cbeg; c < cend; ++c) sum += in[c];
+  }
   int incl = sum;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -148,158 +232,184 @@ __global__ void __launch_bounds__(kSpineWarps * 32) ep_layout_spine_kernel(Layou
     if (lane >= o) incl += y;
   }
   int run = incl - sum;
-  for (int c = cbeg; c < cend; ++c) {
-    const int v = in[c];
-    out[c] = run;
-    run += v;
+  if (V <= kRegRun) {
+#pragma unroll
+    for (int u = 0; u < kRegRun; ++u)
+      if (cbeg + u < cend) {
+        out[cbeg + u] = run;
+        run += reg[u];
+      }
+  } else {
+    for (int c = cbeg; c < cend; ++c) {
+      const int v = in[c];
+      out[c] = run;
+      run += v;
+    }
   }
   const int total = __shfl_sync(0xffffffffu, incl, 31);
   if (lane == 0) p.col_total[j] = total;
 }
 
-// Block-wide exclusive scan of align(cnt[e]) for e in [0, E) into psum[0..E].
-__device__ void aligned_exclusive_scan(const int32_t* __restrict__ cnt, int E, int A,
-                                       int32_t* psum, int32_t* warp_tot) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int nthr = blockDim.x, nwarp = nthr >> 5;
-  const int V = (E + nthr - 1) / nthr;
-  const int beg = min(E, tid * V), end = min(E, beg + V);
-  int sum = 0;
-  for (int e = beg; e < end; ++e) sum += (cnt[e] + A - 1) / A * A;
-  int incl = sum;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += y;
-  }
-  if (lane == 31) warp_tot[warp] = incl;
-  __syncthreads();
-  if (warp == 0) {
-    int v = lane < nwarp ? warp_tot[lane] : 0;
-    int s = v;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, s, o);
-      if (lane >= o) s += y;
-    }
-    if (lane < nwarp) warp_tot[lane] = s - v;  // exclusive warp offsets
-    if (lane == nwarp - 1) warp_tot[32] = s;  // grand total
-  }
-  __syncthreads();
-  int run = warp_tot[warp] + incl - sum;
-  for (int e = beg; e < end; ++e) {
-    psum[e] = run;
-    run += (cnt[e] + A - 1) / A * A;
-  }
-  if (tid == 0) psum[E] = warp_tot[32];
-  __syncthreads();
-}
+// ---------------------------------------------------------------- slots
 
 template <int KC>
 __global__ void __launch_bounds__(kSlotThreads) ep_layout_slots_kernel(LayoutParams p) {
+  constexpr int KM = KC ? KC : kMaxTopk;
   const int K = KC ? KC : p.topk;
-  const int E = p.num_experts, W = p.world_size, C = p.num_chunks;
-  const int Epr = p.num_expert_per_rank, T = p.max_tok_per_rank;
+  const int KW = K + 2;  // metadata row width
+  const int E = p.num_experts, C = p.num_chunks;
+  const int T = p.max_tok_per_rank;
   extern __shared__ int32_t sm[];
-  int32_t* cnt_s = sm;               // [E]
-  int32_t* psum_s = sm + E;          // [E+1]
-  int32_t* warp_tot = psum_s + E + 1;  // [33]
+  int32_t* psum_s = sm;                   // [E+1]
+  int32_t* cnt_s = psum_s + E + 1;        // [E]
+  int32_t* cl = cnt_s + E;                // [E]   this chunk's count per expert
+  int32_t* co = cl + E;                   // [E]   chunk_off of this chunk per expert
+  int32_t* cx = co + E;                   // [E+1] exclusive scan of cl over experts
+  int32_t* warp_tot = cx + E + 1;         // [33]
+  int32_t* slots_s = warp_tot + 33;       // [TPC*K]
+  int32_t* sorted = slots_s + kLayoutTPC * K;  // [TPC*K] entries ordered by (expert, rank)
+  int32_t* src = sorted + kLayoutTPC * K;      // [2*TPC] {t / T, t mod T} per token
 
-  for (int e = threadIdx.x; e < E; e += blockDim.x) cnt_s[e] = p.col_total[e];
+  const int c = blockIdx.x;
+  const bool has_tokens = c < C;
+  wait_for_preceding_grid();
+  for (int e = threadIdx.x; e < E; e += kSlotThreads) {
+    cnt_s[e] = p.col_total[e];
+    if (has_tokens) {
+      cl[e] = p.chunk_hist[static_cast<int64_t>(e) * C + c];
+      co[e] = p.chunk_off[static_cast<int64_t>(e) * C + c];
+    }
+  }
   __syncthreads();
-  aligned_exclusive_scan(cnt_s, E, p.alignment, psum_s, warp_tot);
-
-  if (blockIdx.x == 0) {
-    for (int e = threadIdx.x; e <= E; e += blockDim.x) {
+  // the aligned exclusive prefix over experts (every CTA; E values)
+  block_exclusive_scan(cnt_s, E, p.alignment, psum_s, warp_tot);
+  if (c == 0) {
+    const int W = p.world_size;
+    for (int e = threadIdx.x; e <= E; e += kSlotThreads) {
       p.psum_expert[e] = psum_s[e];
       if (e < E) p.cnt[e] = cnt_s[e];
     }
-    for (int r = threadIdx.x; r <= W; r += blockDim.x) {
-      p.psum_rank[r] = psum_s[r * Epr];
+    for (int r = threadIdx.x; r <= W; r += kSlotThreads) {
+      p.psum_rank[r] = psum_s[r * p.num_expert_per_rank];
       if (r < W) p.tok_per_rank[r] = p.col_total[E + r];
     }
     if (threadIdx.x == 0) *p.num_recv = psum_s[E];
   }
+  if (has_tokens) block_exclusive_scan(cl, E, 1, cx, warp_tot);  // uniform per CTA
 
-  const int KW = K + 2;  // metadata row width
-  if (static_cast<int>(blockIdx.x) < C) {
-    const int c = blockIdx.x;
-    const int t = c * kLayoutTPC + threadIdx.x;
-    if (t >= p.num_tokens) return;
-    int32_t slot[KC ? KC : kMaxTopk];
+  const int t0 = c * kLayoutTPC;
+  const int ntok = has_tokens ? min(p.num_tokens, t0 + kLayoutTPC) - t0 : 0;
+  if (threadIdx.x < ntok) {
+    const int tl = threadIdx.x, t = t0 + tl;
     const int64_t* row = p.topk_idx + static_cast<int64_t>(t) * K;
     int32_t* ds = p.dst_slot + static_cast<int64_t>(t) * K;
+    int32_t slot[KM];
 #pragma unroll
-    for (int k = 0; k < (KC ? KC : kMaxTopk); ++k) {
+    for (int k = 0; k < KM; ++k) {
       if (k < K) {
         const int e = expert_of(row[k], E);
         const int loc = ds[k];
-        slot[k] = e >= 0 ? psum_s[e] + p.chunk_off[static_cast<int64_t>(e) * C + c] + loc : -1;
+        slot[k] = e >= 0 ? psum_s[e] + co[e] + loc : -1;
+        if (e >= 0) sorted[cx[e] + loc] = tl * K + k;
       }
     }
 #pragma unroll
-    for (int k = 0; k < (KC ? KC : kMaxTopk); ++k)
-      if (k < K) ds[k] = slot[k];
-    const int src_rank = t / T, src_local = t - src_rank * T;
-#pragma unroll
-    for (int k = 0; k < (KC ? KC : kMaxTopk); ++k) {
-      if (k >= K || slot[k] < 0) continue;
-      int32_t* m = p.meta + static_cast<int64_t>(slot[k]) * KW;
-      if ((KW & 1) == 0) {  // 8-byte aligned rows: paired stores
-        int2* m2 = reinterpret_cast<int2*>(m);
-        m2[0] = make_int2(src_rank, src_local);
-#pragma unroll
-        for (int j = 0; j < (KC ? KC : kMaxTopk); j += 2)
-          if (j < K) m2[1 + j / 2] = make_int2(slot[j], slot[j + 1]);
-      } else {
-        m[0] = src_rank;
-        m[1] = src_local;
-#pragma unroll
-        for (int j = 0; j < (KC ? KC : kMaxTopk); ++j)
-          if (j < K) m[2 + j] = slot[j];
+    for (int k = 0; k < KM; ++k)
+      if (k < K) {
+        ds[k] = slot[k];
+        slots_s[tl * K + k] = slot[k];
       }
-    }
-  } else {
-    // rows that receive nothing: padding inside an expert segment, and [R, rcap)
-    const int64_t nfill = static_cast<int64_t>(gridDim.x - C) * blockDim.x;
-    for (int64_t r = static_cast<int64_t>(blockIdx.x - C) * blockDim.x + threadIdx.x; r < p.rcap;
-         r += nfill) {
-      // largest e in [0, E] with psum_s[e] <= r
-      int lo = 0, hi = E;
-      while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (psum_s[mid] <= r) lo = mid; else hi = mid - 1;
-      }
-      const bool pad = (lo == E) || (r >= psum_s[lo] + cnt_s[lo]);
-      if (!pad) continue;
-      int32_t* m = p.meta + r * KW;
-      for (int j = 0; j < KW; ++j) m[j] = -1;
+    const int r = t / T;
+    src[2 * tl] = r;
+    src[2 * tl + 1] = t - r * T;
+  }
+  __syncthreads();
+
+  // metadata rows of this chunk, in (expert, rank) order: flat words f of the
+  // concatenated rows; rows of one expert are contiguous in memory.
+  if (has_tokens) {
+    const int nvalid = cx[E];
+    const int nwords = nvalid * KW;
+    for (int f = threadIdx.x; f < nwords; f += kSlotThreads) {
+      const int q = f / KW, col = f - q * KW;
+      const int entry = sorted[q];
+      const int tl = entry / K;
+      const int v = col < 2 ? src[2 * tl + col] : slots_s[tl * K + col - 2];
+      p.meta[static_cast<int64_t>(slots_s[entry]) * KW + col] = v;
     }
   }
+
+  // rows that receive nothing: the padding of experts e = c, c + grid, ... and
+  // this CTA's slice of [R, capacity)
+  for (int e = c; e < E; e += gridDim.x) {
+    const int64_t beg = static_cast<int64_t>(psum_s[e] + cnt_s[e]) * KW;
+    const int64_t end = static_cast<int64_t>(psum_s[e + 1]) * KW;
+    for (int64_t f = beg + threadIdx.x; f < end; f += kSlotThreads) p.meta[f] = -1;
+  }
+  const int64_t tail_beg = static_cast<int64_t>(psum_s[E]) * KW;
+  const int64_t tail_words = p.rcap * KW - tail_beg;
+  const int64_t per = (tail_words + gridDim.x - 1) / gridDim.x;
+  const int64_t sbeg = tail_beg + per * c;
+  const int64_t send = sbeg + per < p.rcap * KW ? sbeg + per : p.rcap * KW;
+  for (int64_t f = sbeg + threadIdx.x; f < send; f += kSlotThreads) p.meta[f] = -1;
+}
+
+// ---------------------------------------------------------------- launch
+
+template <class Kern>
+cudaError_t launch_dependent(Kern kernel, int grid, int block, size_t smem, cudaStream_t s,
+                             const LayoutParams& p) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, p);
+}
+
+size_t count_smem(int topk, int cols) {
+  const size_t ids = (static_cast<size_t>(kLayoutTPC) * topk + 1) & ~static_cast<size_t>(1);
+  return sizeof(int32_t) * (static_cast<size_t>(kLayoutCountWarps) * cols + ids) +
+         sizeof(unsigned long long) * kLayoutTPC;
+}
+
+size_t slots_smem(int E, int topk) {
+  return sizeof(int32_t) * (5 * static_cast<size_t>(E) + 2 + 33 + 2 * kLayoutTPC * topk +
+                            2 * kLayoutTPC);
 }
 
 template <int KC>
 cudaError_t launch_layout(const LayoutParams& p, const LaunchGeom& g, cudaStream_t s) {
   const int EW = p.num_experts + p.world_size;
-  if (p.num_chunks > 0) {
-    const size_t smem = sizeof(int32_t) * kLayoutCountWarps * EW;
-    ep_layout_count_kernel<KC><<<p.num_chunks, kCountThreads, smem, s>>>(p);
-  }
-  ep_layout_spine_kernel<<<(EW + kSpineWarps - 1) / kSpineWarps, kSpineWarps * 32, 0, s>>>(p);
-  const int64_t fill_ctas = (p.rcap + kSlotThreads * 8 - 1) / (kSlotThreads * 8);
-  const int nfill = static_cast<int>(fill_ctas < 1 ? 1 : (fill_ctas > 2 * g.num_sms ? 2 * g.num_sms
-                                                                                     : fill_ctas));
-  const size_t smem2 = sizeof(int32_t) * (2 * p.num_experts + 1 + 33);
-  ep_layout_slots_kernel<KC><<<p.num_chunks + nfill, kSlotThreads, smem2, s>>>(p);
-  return cudaGetLastError();
+  if (p.num_chunks > 0)
+    ep_layout_count_kernel<KC><<<p.num_chunks, kCountThreads, count_smem(p.topk, EW), s>>>(p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  e = launch_dependent(ep_layout_spine_kernel, (EW + kSpineWarps - 1) / kSpineWarps,
+                       kSpineWarps * 32, 0, s, p);
+  if (e != cudaSuccess) return e;
+  const int grid = p.num_chunks > g.num_sms ? p.num_chunks : g.num_sms;
+  return launch_dependent(ep_layout_slots_kernel<KC>, grid, kSlotThreads,
+                          slots_smem(p.num_experts, p.topk), s, p);
 }
 
+// Shared-memory limits are set to what the largest launch can need (every E+W
+// and, for the generic variant, every top-k the library accepts), so that
+// handles with different shapes never lower them for each other.
 template <int KC>
-cudaError_t prepare_layout(int /*hidden*/, int /*topk*/, int num_experts_plus_ranks,
-                           LaunchGeom* g) {
-  const int smem = static_cast<int>(sizeof(int32_t)) * kLayoutCountWarps * num_experts_plus_ranks;
+cudaError_t prepare_layout(int, int, int, LaunchGeom* g) {
+  const int kmax = KC ? KC : kMaxTopk;
   cudaError_t e = cudaFuncSetAttribute(ep_layout_count_kernel<KC>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(count_smem(kmax, kMaxExperts + kMaxWorld)));
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(ep_layout_slots_kernel<KC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(slots_smem(kMaxExperts, kmax)));
   if (e != cudaSuccess) return e;
   g->blocks_per_sm = 1;
   return cudaSuccess;
@@ -307,10 +417,23 @@ cudaError_t prepare_layout(int /*hidden*/, int /*topk*/, int num_experts_plus_ra
 
 }  // namespace
 
-size_t LayoutScratchBytes(int max_chunks, int columns) {
-  // chunk_hist [columns][C] + chunk_off [columns][C] + col_total [columns]
-  return sizeof(int32_t) * (2 * static_cast<size_t>(columns) * (max_chunks > 0 ? max_chunks : 1) +
-                            static_cast<size_t>(columns));
+int64_t LayoutScratchInts(int max_chunks, int columns) {
+  return 2LL * columns * (max_chunks > 0 ? max_chunks : 1) + columns;
+}
+
+void BindLayoutScratch(LayoutParams* p, int32_t* base, int max_chunks, int columns) {
+  const int64_t cap = max_chunks > 0 ? max_chunks : 1;
+  p->chunk_hist = base;
+  p->chunk_off = base + static_cast<int64_t>(columns) * cap;
+  p->col_total = p->chunk_off + static_cast<int64_t>(columns) * cap;
+}
+
+uint32_t RankMagic(int num_expert_per_rank) {
+  // m = floor(2^32 / d) + 1 gives umulhi(e, m) = floor(e/d + e*(d - 2^32 mod d)/(d*2^32)):
+  // the added term is below 2^-21 while e/d is at least 1/d >= 2^-11 short of the
+  // next integer, so the result is e / d for every e < 2^11 and 2 <= d <= 2^11.
+  if (num_expert_per_rank <= 1) return 0u;
+  return static_cast<uint32_t>((1ull << 32) / static_cast<uint64_t>(num_expert_per_rank) + 1ull);
 }
 
 Variant<LayoutLaunch> FindLayout(int topk) {

@@ -99,12 +99,12 @@ extern "C" int ep_layout_noalloc(const ep_cfg_t* cfg, const int64_t* topk_idx, i
       return RecordError(EP_EINVAL, "num_tokens must be in [0, world_size*max_tok_per_rank]");
     const int cols = E + W;
     const int C = NumLayoutChunks(num_tokens);
-    const int64_t need = 2LL * cols * (C > 0 ? C : 1) + cols;
+    const int64_t need = LayoutScratchInts(C, cols);
     if (need > kNoAllocScratchInts) {
       char buf[320];
       std::snprintf(buf, sizeof buf,
                     "ep_layout_noalloc: %d tokens over %d experts + %d ranks need %lld int32 of "
-                    "scratch (2*(E+W)*ceil(N/%d) + E+W); the static scratch holds %lld",
+                    "scratch (2*(E+W)*ceil(N/%d) + (E+W)); the static scratch holds %lld",
                     num_tokens, E, W, static_cast<long long>(need), kLayoutTPC,
                     static_cast<long long>(kNoAllocScratchInts));
       return RecordError(EP_EINVAL, buf);
@@ -149,9 +149,8 @@ extern "C" int ep_layout_noalloc(const ep_cfg_t* cfg, const int64_t* topk_idx, i
     p.dst_slot = dst_slot;
     p.meta = recv_src_metadata;
     p.err = device_error;
-    p.chunk_hist = s->scratch;
-    p.chunk_off = s->scratch + static_cast<int64_t>(cols) * Cs;
-    p.col_total = s->scratch + 2LL * cols * Cs;
+    p.epr_magic = RankMagic(cfg->num_expert_per_rank);
+    BindLayoutScratch(&p, s->scratch, Cs, cols);
     const LaunchGeom g{s->num_sms, 1};
     if ((e = FindLayout(K).launch(p, g, st)) != cudaSuccess) return err_cuda(e, "layout launch");
     return EP_OK;

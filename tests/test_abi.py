@@ -101,3 +101,13 @@ def test_public_header_is_plain_c():
     tu = '#include "ep_gb300.h"\nint main(void) { ep_cfg_t c = {0}; return (int)sizeof c; }\n'
     subprocess.run(["gcc", "-std=c99", "-fsyntax-only", "-Wall", "-Werror", "-I",
                     os.path.join(ROOT, "include"), "-x", "c", "-"], input=tu, text=True, check=True)
+
+
+def test_rank_magic_divides_exactly_over_the_whole_domain():
+    """The layout divides expert ids by experts-per-rank with a multiply-high by
+    floor(2^32/d) + 1; check the identity for every id < 2048 and d in [2, 2048]."""
+    import numpy as np
+    e = np.arange(2048, dtype=np.uint64)
+    for d in range(2, 2049):
+        m = np.uint64((1 << 32) // d + 1)
+        assert np.array_equal((e * m) >> np.uint64(32), e // np.uint64(d)), d

@@ -102,6 +102,10 @@ EDGE = {
     "max_experts": dict(base="tiny", world_size=64, num_expert_per_rank=32, max_tok_per_rank=64,
                         num_tokens=4096, topk=8, alignment=2),
     "big_alignment": dict(base="decode", alignment=4096),
+    # one expert per rank, and a non-power-of-two experts-per-rank
+    "epr1": dict(base="tiny", num_expert_per_rank=1, topk=4, alignment=2),
+    "epr7": dict(base="tiny", world_size=3, num_expert_per_rank=7, max_tok_per_rank=64,
+                 num_tokens=150, alignment=5),
     "zipf_hot": dict(base="skewed", num_tokens=4096),
 }
 
