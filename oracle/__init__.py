@@ -56,6 +56,14 @@ def lib():
     L.oracle_e4m3_decode_array.argtypes = [c.c_int64, _u8p, _f64p]
     L.oracle_f32_to_bf16_array.restype = None
     L.oracle_f32_to_bf16_array.argtypes = [c.c_int64, _f32p, _u16p]
+    L.oracle_dispatch_bytes.restype = None
+    L.oracle_dispatch_bytes.argtypes = [c.c_int, c.c_int64, c.c_int, _u8p, _i32p, _u8p]
+    L.oracle_forward_routing.restype = None
+    L.oracle_forward_routing.argtypes = [c.c_int, c.c_int, _i64p, c.c_void_p, _i32p, c.c_void_p,
+                                         c.c_void_p]
+    L.oracle_combine_ex.restype = None
+    L.oracle_combine_ex.argtypes = [c.c_int, c.c_int, c.c_int, _u16p, _i32p, c.c_void_p,
+                                    c.c_void_p, c.c_void_p, c.c_void_p]
     _lib = L
     return L
 
@@ -165,4 +173,50 @@ def f32_to_bf16(v):
     v = np.ascontiguousarray(v, dtype=np.float32)
     out = np.zeros(v.shape, np.uint16)
     lib().oracle_f32_to_bf16_array(v.size, v.reshape(-1), out.reshape(-1))
+    return out
+
+
+def _vp(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def dispatch_bytes(x_bytes, dst_slot, recv):
+    """recv[dst_slot[t, k]] = x[t] as raw bytes; x_bytes uint8 [N, row_bytes],
+    recv uint8 [rows, row_bytes], in place."""
+    x_bytes = np.ascontiguousarray(x_bytes, dtype=np.uint8)
+    N, rb = x_bytes.shape
+    K = dst_slot.shape[1]
+    assert recv.dtype == np.uint8 and recv.shape[1] == rb and recv.flags.c_contiguous
+    lib().oracle_dispatch_bytes(N, rb, K, x_bytes, np.ascontiguousarray(dst_slot, np.int32), recv)
+    return recv
+
+
+def forward_routing(topk_idx, weights, dst_slot, recv_w=None, recv_idx=None):
+    """recv_w[dst_slot[t, k]] = weights[t, k]; recv_idx[dst_slot[t, k]] = topk_idx[t, k]
+    (in place; either output may be None)."""
+    topk_idx = np.ascontiguousarray(topk_idx, np.int64)
+    N, K = topk_idx.shape
+    w = None if weights is None else np.ascontiguousarray(weights, np.float32)
+    for a, dt in ((recv_w, np.float32), (recv_idx, np.int32)):
+        assert a is None or (a.dtype == dt and a.flags.c_contiguous)
+    lib().oracle_forward_routing(N, K, topk_idx, _vp(w), np.ascontiguousarray(dst_slot, np.int32),
+                                 _vp(recv_w), _vp(recv_idx))
+
+
+def combine_ex(y_bits, dst_slot, weights=None, bias_bits=None, out_dtype="bf16"):
+    """Combine + optional bf16 bias [N, H]; returns uint16 bf16 bits or float32 [N, H]."""
+    dst_slot = np.ascontiguousarray(dst_slot, dtype=np.int32)
+    N, K = dst_slot.shape
+    H = y_bits.shape[1]
+    w = None if weights is None else np.ascontiguousarray(weights, np.float32)
+    b = None if bias_bits is None else np.ascontiguousarray(bias_bits, np.uint16)
+    assert b is None or b.shape == (N, H)
+    if out_dtype == "fp32":
+        out = np.zeros((N, H), np.float32)
+        lib().oracle_combine_ex(N, H, K, np.ascontiguousarray(y_bits), dst_slot, _vp(w), _vp(b),
+                                None, _vp(out))
+    else:
+        out = np.zeros((N, H), np.uint16)
+        lib().oracle_combine_ex(N, H, K, np.ascontiguousarray(y_bits), dst_slot, _vp(w), _vp(b),
+                                _vp(out), None)
     return out

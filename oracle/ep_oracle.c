@@ -364,3 +364,72 @@ void oracle_f32_to_bf16_array(int64_t n, const float *v, uint16_t *out)
     for (int64_t i = 0; i < n; ++i)
         out[i] = oracle_f32_to_bf16(v[i]);
 }
+
+/* ------------------------------------------------- transport and routing */
+
+/* Dispatch of an opaque payload: recv[dst_slot[t][k]] = x[t] as row_bytes raw
+ * bytes.  This is how the pages treat the narrow and wide transports ("MORI
+ * JIT v2" §3.7: Fp32, Fp8 and Fp4x2 payloads are moved, never computed on;
+ * an Fp4x2 row of H channels is H/2 bytes). */
+void oracle_dispatch_bytes(int N, int64_t row_bytes, int K, const uint8_t *x,
+                           const int32_t *dst_slot, uint8_t *recv)
+{
+    for (int t = 0; t < N; ++t)
+        for (int k = 0; k < K; ++k) {
+            int32_t s = dst_slot[(int64_t)t * K + k];
+            if (s < 0)
+                continue;
+            memcpy(recv + (int64_t)s * row_bytes, x + (int64_t)t * row_bytes, (size_t)row_bytes);
+        }
+}
+
+/* Routing that travels with each received row (the dispatch copy epilogue of
+ * "DeepEP overall architecture analysis" fills recv_topk_idx and
+ * recv_topk_weights): the row of (t, k) carries the expert it was sent to and
+ * the token's weight for that expert.  Rows nothing maps to are untouched. */
+void oracle_forward_routing(int N, int K, const int64_t *topk_idx, const float *w,
+                            const int32_t *dst_slot, float *recv_w, int32_t *recv_idx)
+{
+    for (int t = 0; t < N; ++t)
+        for (int k = 0; k < K; ++k) {
+            int64_t i = (int64_t)t * K + k;
+            int32_t s = dst_slot[i];
+            if (s < 0)
+                continue;
+            if (recv_w)
+                recv_w[s] = w[i];
+            if (recv_idx)
+                recv_idx[s] = (int32_t)topk_idx[i];
+        }
+}
+
+/* Combine with an optional bias and an fp32 or bf16 output ("Combine data
+ * flow": reduce weighted by topk_weights, "+ bias", write back).  The fold is
+ * oracle_combine's; the bias (bf16 [N][H], may be NULL) is then added with one
+ * fp32 addition; the sum is stored as fp32 (out_f32) or rounded once to bf16
+ * (out_bf16).  Exactly one of out_bf16 / out_f32 is non-NULL. */
+void oracle_combine_ex(int N, int H, int K, const uint16_t *y, const int32_t *dst_slot,
+                       const float *w, const uint16_t *bias, uint16_t *out_bf16, float *out_f32)
+{
+    for (int t = 0; t < N; ++t) {
+        for (int c = 0; c < H; ++c) {
+            float acc = 0.0f;
+            for (int k = 0; k < K; ++k) {
+                int32_t s = dst_slot[(int64_t)t * K + k];
+                if (s < 0)
+                    continue;
+                float v = oracle_bf16_to_f32(y[(int64_t)s * H + c]);
+                if (w)
+                    acc = fmaf(w[(int64_t)t * K + k], v, acc);
+                else
+                    acc = acc + v;
+            }
+            if (bias)
+                acc = acc + oracle_bf16_to_f32(bias[(int64_t)t * H + c]);
+            if (out_f32)
+                out_f32[(int64_t)t * H + c] = acc;
+            else
+                out_bf16[(int64_t)t * H + c] = oracle_f32_to_bf16(acc);
+        }
+    }
+}
