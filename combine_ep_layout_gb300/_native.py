@@ -20,7 +20,7 @@ EP_BF16, EP_FP32, EP_FP8_E4M3, EP_FP4X2 = 0, 1, 2, 3
 EP_OK, EP_EINVAL, EP_EUNSUPPORTED, EP_ECUDA, EP_ENOMEM = 0, -1, -2, -3, -4
 (FIELD_NUM_UNALIGNED_PER_EXPERT, FIELD_NUM_TOKENS_PER_RANK, FIELD_PSUM_PER_EXPERT,
  FIELD_PSUM_PER_RANK, FIELD_DST_SLOT, FIELD_RECV_SRC_METADATA, FIELD_NUM_RECV,
- FIELD_DEVICE_ERROR) = range(8)
+ FIELD_DEVICE_ERROR, FIELD_TOPK_IDX) = range(9)
 ERR_BAD_EXPERT, ERR_TIMEOUT = 1, 2
 
 _DTYPES = {"bf16": EP_BF16, "fp32": EP_FP32, "fp8": EP_FP8_E4M3, "fp8_e4m3": EP_FP8_E4M3,
@@ -64,6 +64,10 @@ def load_library():
     L.ep_dispatch.argtypes = [vp, vp, vp, vp, vp]
     L.ep_combine.restype = c.c_int
     L.ep_combine.argtypes = [vp, vp, vp, vp, vp]
+    L.ep_dispatch_fwd.restype = c.c_int
+    L.ep_dispatch_fwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp]
+    L.ep_combine_ex.restype = c.c_int
+    L.ep_combine_ex.argtypes = [vp, vp, vp, vp, vp, i32, vp]
     L.ep_handle_free.restype = None
     L.ep_handle_free.argtypes = [vp]
     L.ep_handle_get.restype = c.c_int
@@ -155,17 +159,35 @@ class EpHandle:
                                         _stream_ptr(stream, self.device)))
         self.num_tokens = n
 
-    def dispatch(self, x, recv_x, recv_scales=None, stream=None):
+    def dispatch(self, x, recv_x, recv_scales=None, topk_weights=None, recv_topk_weights=None,
+                 recv_topk_idx=None, stream=None):
+        """ep_dispatch, or ep_dispatch_fwd when recv_topk_weights / recv_topk_idx are given."""
         assert x.is_cuda and x.is_contiguous() and recv_x.is_contiguous()
-        assert recv_scales is None or recv_scales.is_contiguous()
-        _check(load_library().ep_dispatch(self.ptr, _ptr(x), _ptr(recv_x), _ptr(recv_scales),
-                                          _stream_ptr(stream, self.device)))
+        for t in (recv_scales, topk_weights, recv_topk_weights, recv_topk_idx):
+            assert t is None or t.is_contiguous()
+        L = load_library()
+        st = _stream_ptr(stream, self.device)
+        if recv_topk_weights is None and recv_topk_idx is None:
+            _check(L.ep_dispatch(self.ptr, _ptr(x), _ptr(recv_x), _ptr(recv_scales), st))
+        else:
+            _check(L.ep_dispatch_fwd(self.ptr, _ptr(x), _ptr(recv_x), _ptr(recv_scales),
+                                     _ptr(topk_weights), _ptr(recv_topk_weights),
+                                     _ptr(recv_topk_idx), st))
 
-    def combine(self, y, topk_weights, out, stream=None):
+    def combine(self, y, topk_weights, out, bias=None, stream=None):
+        """ep_combine, or ep_combine_ex when a bias is given or out is fp32."""
         assert y.is_cuda and y.is_contiguous() and out.is_contiguous()
         assert topk_weights is None or topk_weights.is_contiguous()
-        _check(load_library().ep_combine(self.ptr, _ptr(y), _ptr(topk_weights), _ptr(out),
-                                         _stream_ptr(stream, self.device)))
+        assert bias is None or (bias.dtype == torch.bfloat16 and bias.is_contiguous())
+        assert out.dtype in (torch.bfloat16, torch.float32)
+        L = load_library()
+        st = _stream_ptr(stream, self.device)
+        if bias is None and out.dtype == torch.bfloat16:
+            _check(L.ep_combine(self.ptr, _ptr(y), _ptr(topk_weights), _ptr(out), st))
+        else:
+            odt = EP_FP32 if out.dtype == torch.float32 else EP_BF16
+            _check(L.ep_combine_ex(self.ptr, _ptr(y), _ptr(topk_weights), _ptr(bias), _ptr(out),
+                                   odt, st))
 
     def field(self, field):
         """A torch int32 view (no copy) of one handle field on the device."""
@@ -174,6 +196,8 @@ class EpHandle:
         K = self.cfg.num_expert_per_token
         shape = (n.value,)
         if field == FIELD_DST_SLOT:
+            shape = (n.value // K, K)
+        elif field == FIELD_TOPK_IDX:
             shape = (n.value // K, K)
         elif field == FIELD_RECV_SRC_METADATA:
             shape = (n.value // (K + 2), K + 2)
@@ -213,11 +237,20 @@ def ep_layout(h, topk_idx, num_tokens=None, stream=None):
 
 
 def ep_dispatch(h, x, recv_x, recv_scales=None, stream=None):
-    h.dispatch(x, recv_x, recv_scales, stream)
+    h.dispatch(x, recv_x, recv_scales, stream=stream)
+
+
+def ep_dispatch_fwd(h, x, recv_x, recv_scales, topk_weights, recv_topk_weights, recv_topk_idx,
+                    stream=None):
+    h.dispatch(x, recv_x, recv_scales, topk_weights, recv_topk_weights, recv_topk_idx, stream)
 
 
 def ep_combine(h, y, topk_weights, out, stream=None):
-    h.combine(y, topk_weights, out, stream)
+    h.combine(y, topk_weights, out, stream=stream)
+
+
+def ep_combine_ex(h, y, topk_weights, bias, out, stream=None):
+    h.combine(y, topk_weights, out, bias, stream)
 
 
 def ep_handle_free(h):

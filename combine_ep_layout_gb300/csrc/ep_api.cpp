@@ -62,9 +62,11 @@ int validate(const ep_cfg_t* c) {
       if (c->hidden_dim % kScaleGroup != 0)
         return fail(EP_EINVAL, "FP8 dispatch needs hidden_dim % 128 == 0 (one scale per 128 channels)");
       break;
-    case EP_FP32:
+    case EP_FP32: break;
     case EP_FP4X2:
-      return fail(EP_EUNSUPPORTED, "dispatch dtype not served: only EP_BF16 and EP_FP8_E4M3");
+      if (c->hidden_dim % 32 != 0)
+        return fail(EP_EINVAL, "FP4x2 transport needs hidden_dim % 32 == 0 (16-byte rows of H/2 bytes)");
+      break;
     default: return fail(EP_EINVAL, "unknown dispatch_dtype");
   }
   const int64_t rcap = RecvCapacity(max_tokens, c->num_expert_per_token, static_cast<int>(E),
@@ -88,7 +90,7 @@ struct ep_handle {
   void* block = nullptr;
   int32_t *cnt = nullptr, *tok_per_rank = nullptr, *psum_expert = nullptr, *psum_rank = nullptr,
           *num_recv = nullptr, *err = nullptr, *dst_slot = nullptr, *meta = nullptr,
-          *scratch = nullptr;
+          *topk_i32 = nullptr, *scratch = nullptr;
   Variant<LayoutLaunch> layout{};
   Variant<DispatchLaunch> dispatch{};
   Variant<CombineLaunch> combine{};
@@ -172,10 +174,11 @@ int ep_handle_create(const ep_cfg_t* cfg, ep_handle_t* out) noexcept {
     // one allocation, 256-byte aligned sub-buffers
     auto al = [](size_t b) { return (b + 255) & ~static_cast<size_t>(255); };
     const size_t n_small = al(4 * (h->E + h->W + (h->E + 1) + (h->W + 1) + 2));
-    const size_t n_slot = al(4 * static_cast<size_t>(h->max_tokens) * h->K);
+    const size_t n_slot = al(4 * static_cast<size_t>(h->max_tokens) * h->K);  // dst_slot, and the id clone
     const size_t n_meta = al(4 * static_cast<size_t>(h->rcap) * (h->K + 2));
     const size_t n_scr = al(sizeof(int32_t) * static_cast<size_t>(LayoutScratchInts(h->max_chunks, cols)));
-    e = cudaMalloc(&h->block, n_small + n_slot + n_meta + n_scr);
+    const size_t total = n_small + 2 * n_slot + n_meta + n_scr;
+    e = cudaMalloc(&h->block, total);
     if (e != cudaSuccess) {
       cudaGetLastError();
       return bail(fail(EP_ENOMEM, std::string("cudaMalloc of the handle's metadata failed: ") +
@@ -190,9 +193,10 @@ int ep_handle_create(const ep_cfg_t* cfg, ep_handle_t* out) noexcept {
     h->num_recv = h->psum_rank + h->W + 1;
     h->err = h->num_recv + 1;
     h->dst_slot = reinterpret_cast<int32_t*>(b + n_small);
-    h->meta = reinterpret_cast<int32_t*>(b + n_small + n_slot);
-    h->scratch = reinterpret_cast<int32_t*>(b + n_small + n_slot + n_meta);
-    if ((e = cudaMemset(h->block, 0, n_small + n_slot + n_meta + n_scr)) != cudaSuccess)
+    h->topk_i32 = reinterpret_cast<int32_t*>(b + n_small + n_slot);
+    h->meta = reinterpret_cast<int32_t*>(b + n_small + 2 * n_slot);
+    h->scratch = reinterpret_cast<int32_t*>(b + n_small + 2 * n_slot + n_meta);
+    if ((e = cudaMemset(h->block, 0, total)) != cudaSuccess)
       return bail(fail_cuda(e, "cudaMemset"));
     if ((e = cudaDeviceSynchronize()) != cudaSuccess) return bail(fail_cuda(e, "cudaDeviceSynchronize"));
     *out = h;
@@ -233,6 +237,7 @@ int ep_layout(ep_handle_t h, const int64_t* topk_idx, int32_t num_tokens, ep_str
     p.dst_slot = h->dst_slot;
     p.meta = h->meta;
     p.err = h->err;
+    p.topk_i32 = h->topk_i32;
     p.epr_magic = RankMagic(h->Epr);
     BindLayoutScratch(&p, h->scratch, h->max_chunks, h->E + h->W);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -250,15 +255,27 @@ int ep_layout(ep_handle_t h, const int64_t* topk_idx, int32_t num_tokens, ep_str
 
 int ep_dispatch(ep_handle_t h, const void* x, void* recv_x, float* recv_scales,
                 ep_stream_t stream) noexcept {
+  return ep_dispatch_fwd(h, x, recv_x, recv_scales, nullptr, nullptr, nullptr, stream);
+}
+
+int ep_dispatch_fwd(ep_handle_t h, const void* x, void* recv_x, float* recv_scales,
+                    const float* topk_weights, float* recv_topk_weights, int32_t* recv_topk_idx,
+                    ep_stream_t stream) noexcept {
   try {
     if (!h) return fail(EP_EINVAL, "handle is NULL");
     const bool fp8 = h->cfg.dispatch_dtype == EP_FP8_E4M3;
     if (fp8 && !recv_scales) return fail(EP_EINVAL, "FP8 dispatch needs recv_scales");
-    if (!fp8 && recv_scales) return fail(EP_EINVAL, "recv_scales must be NULL for bf16 dispatch");
+    if (!fp8 && recv_scales) return fail(EP_EINVAL, "recv_scales is only written by FP8 dispatch");
+    if (recv_topk_weights && !topk_weights)
+      return fail(EP_EINVAL, "recv_topk_weights needs topk_weights");
     if (h->num_tokens > 0) {
       if (!x || !recv_x) return fail(EP_EINVAL, "x / recv_x is NULL");
       if (!aligned16(x) || !aligned16(recv_x) || (recv_scales && !aligned16(recv_scales)))
         return fail(EP_EINVAL, "x, recv_x and recv_scales must be 16-byte aligned");
+      if ((topk_weights && (reinterpret_cast<uintptr_t>(topk_weights) & 3u)) ||
+          (recv_topk_weights && (reinterpret_cast<uintptr_t>(recv_topk_weights) & 3u)) ||
+          (recv_topk_idx && (reinterpret_cast<uintptr_t>(recv_topk_idx) & 3u)))
+        return fail(EP_EINVAL, "weights and ids must be 4-byte aligned");
     }
     int rc = check_device(h);
     if (rc != EP_OK) return rc;
@@ -270,7 +287,12 @@ int ep_dispatch(ep_handle_t h, const void* x, void* recv_x, float* recv_scales,
     p.num_tokens = h->num_tokens;
     p.hidden = h->H;
     p.topk = h->K;
+    p.row_bytes = static_cast<int>(RowBytes(h->H, static_cast<EpDType>(h->cfg.dispatch_dtype)));
     p.err = h->err;
+    p.topk_weights = topk_weights;
+    p.topk_i32 = h->topk_i32;
+    p.recv_topk_weights = recv_topk_weights;
+    p.recv_topk_idx = recv_topk_idx;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e = h->dispatch.launch(p, h->g_dispatch, s);
     if (e != cudaSuccess) return fail_cuda(e, "dispatch launch");
@@ -285,13 +307,21 @@ int ep_dispatch(ep_handle_t h, const void* x, void* recv_x, float* recv_scales,
 
 int ep_combine(ep_handle_t h, const void* y, const float* topk_weights, void* out,
                ep_stream_t stream) noexcept {
+  return ep_combine_ex(h, y, topk_weights, nullptr, out, EP_BF16, stream);
+}
+
+int ep_combine_ex(ep_handle_t h, const void* y, const float* topk_weights, const void* bias,
+                  void* out, int32_t out_dtype, ep_stream_t stream) noexcept {
   try {
     if (!h) return fail(EP_EINVAL, "handle is NULL");
+    if (out_dtype != EP_BF16 && out_dtype != EP_FP32)
+      return fail(EP_EINVAL, "combine output dtype must be EP_BF16 or EP_FP32");
     const bool weighted = h->cfg.use_weights != 0;
     if (h->num_tokens > 0) {
       if (!y || !out) return fail(EP_EINVAL, "y / out is NULL");
       if (weighted && !topk_weights) return fail(EP_EINVAL, "use_weights is set but topk_weights is NULL");
-      if (!aligned16(y) || !aligned16(out)) return fail(EP_EINVAL, "y and out must be 16-byte aligned");
+      if (!aligned16(y) || !aligned16(out) || (bias && !aligned16(bias)))
+        return fail(EP_EINVAL, "y, bias and out must be 16-byte aligned");
       if (weighted && (reinterpret_cast<uintptr_t>(topk_weights) & 3u))
         return fail(EP_EINVAL, "topk_weights must be 4-byte aligned");
     }
@@ -300,11 +330,13 @@ int ep_combine(ep_handle_t h, const void* y, const float* topk_weights, void* ou
     CombineParams p{};
     p.y = y;
     p.weights = weighted ? topk_weights : nullptr;
+    p.bias = bias;
     p.out = out;
     p.dst_slot = h->dst_slot;
     p.num_tokens = h->num_tokens;
     p.hidden = h->H;
     p.topk = h->K;
+    p.out_f32 = out_dtype == EP_FP32 ? 1 : 0;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e = h->combine.launch(p, h->g_combine, s);
     if (e != cudaSuccess) return fail_cuda(e, "combine launch");
@@ -341,6 +373,10 @@ int ep_handle_get(ep_handle_t h, int32_t field, void** dev_ptr, int64_t* numel) 
       case EP_FIELD_RECV_SRC_METADATA: *dev_ptr = h->meta; *numel = h->rcap * (h->K + 2); break;
       case EP_FIELD_NUM_RECV: *dev_ptr = h->num_recv; *numel = 1; break;
       case EP_FIELD_DEVICE_ERROR: *dev_ptr = h->err; *numel = 1; break;
+      case EP_FIELD_TOPK_IDX:
+        *dev_ptr = h->topk_i32;
+        *numel = static_cast<int64_t>(h->num_tokens) * h->K;
+        break;
       default: return fail(EP_EINVAL, "unknown field");
     }
     return EP_OK;

@@ -8,6 +8,10 @@
 // acc = +0.0f, masked k skipped.  The order is fixed, so the result is
 // bit-for-bit reproducible.
 //
+// Optionally a bf16 bias [N, H] is added after the fold (one fp32 addition,
+// the "+ bias" of the pages' combine epilogue) and the output is fp32 instead
+// of bf16.
+//
 // One CTA per token; each thread owns 32-byte (16 channels) column chunks --
 // 16-byte chunks when a buffer is only 16-byte aligned -- and issues the loads
 // of all K rows for a chunk before folding them, so K row fetches are in
@@ -83,10 +87,23 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&b);
 }
 
-template <int HC, int KC, bool WEIGHTED, int V>
+template <int V>
+__device__ __forceinline__ void st_f32(void* p, const float (&acc)[2 * V]) {
+  // 2V fp32 values: two vectors of V words
+  Vec<V> a, b;
+#pragma unroll
+  for (int i = 0; i < V; ++i) {
+    a.w[i] = __float_as_uint(acc[i]);
+    b.w[i] = __float_as_uint(acc[V + i]);
+  }
+  st_stream<V>(p, a);
+  st_stream<V>(static_cast<uint8_t*>(p) + 4 * V, b);
+}
+
+template <int HC, int KC, bool WEIGHTED, int V, bool BIAS, bool F32>
 __global__ void __launch_bounds__(kCombineThreads) ep_combine_kernel(CombineParams p) {
   constexpr int KM = KC ? KC : kMaxTopk;
-  constexpr int UNIT = 4 * V;  // bytes per chunk
+  constexpr int UNIT = 4 * V;  // bytes of bf16 per chunk (2V channels)
   const int H = HC ? HC : p.hidden;
   const int K = KC ? KC : p.topk;
   const int row = 2 * H;
@@ -105,43 +122,66 @@ __global__ void __launch_bounds__(kCombineThreads) ep_combine_kernel(CombinePara
     }
   }
   const uint8_t* y = static_cast<const uint8_t*>(p.y);
-  uint8_t* out = static_cast<uint8_t*>(p.out) + static_cast<int64_t>(t) * row;
+  const uint8_t* bias = BIAS ? static_cast<const uint8_t*>(p.bias) + static_cast<int64_t>(t) * row
+                             : nullptr;
+  uint8_t* out = static_cast<uint8_t*>(p.out) + static_cast<int64_t>(t) * (F32 ? 2 * row : row);
   for (int c = threadIdx.x; c < chunks; c += kCombineThreads) {
     Vec<V> v[KM];
 #pragma unroll
     for (int k = 0; k < KM; ++k)
       if (slot[k] >= 0)
         ld_stream<V>(y + static_cast<int64_t>(slot[k]) * row + static_cast<int64_t>(c) * UNIT, v[k]);
+    Vec<V> bv;
+    if (BIAS) ld_stream<V>(bias + static_cast<int64_t>(c) * UNIT, bv);
     float acc[2 * V];
 #pragma unroll
     for (int i = 0; i < 2 * V; ++i) acc[i] = 0.0f;
 #pragma unroll
     for (int k = 0; k < KM; ++k)
       if (slot[k] >= 0) fold<V>(acc, v[k], w[k], WEIGHTED);
-    Vec<V> o;
+    if (BIAS) fold<V>(acc, bv, 1.0f, false);  // one fp32 addition after the fold
+    if (F32) {
+      st_f32<V>(out + static_cast<int64_t>(c) * 2 * UNIT, acc);
+    } else {
+      Vec<V> o;
 #pragma unroll
-    for (int i = 0; i < V; ++i) o.w[i] = pack_bf16x2(acc[2 * i], acc[2 * i + 1]);
-    st_stream<V>(out + static_cast<int64_t>(c) * UNIT, o);
+      for (int i = 0; i < V; ++i) o.w[i] = pack_bf16x2(acc[2 * i], acc[2 * i + 1]);
+      st_stream<V>(out + static_cast<int64_t>(c) * UNIT, o);
+    }
   }
 }
 
 inline bool aligned32(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 31u) == 0; }
 
+template <int HC, int KC, bool WEIGHTED, int V>
+cudaError_t launch_flags(const CombineParams& p, cudaStream_t s) {
+  const bool bias = p.bias != nullptr, f32 = p.out_f32 != 0;
+  if (bias && f32)
+    ep_combine_kernel<HC, KC, WEIGHTED, V, true, true><<<p.num_tokens, kCombineThreads, 0, s>>>(p);
+  else if (bias)
+    ep_combine_kernel<HC, KC, WEIGHTED, V, true, false><<<p.num_tokens, kCombineThreads, 0, s>>>(p);
+  else if (f32)
+    ep_combine_kernel<HC, KC, WEIGHTED, V, false, true><<<p.num_tokens, kCombineThreads, 0, s>>>(p);
+  else
+    ep_combine_kernel<HC, KC, WEIGHTED, V, false, false><<<p.num_tokens, kCombineThreads, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
 template <int HC, int KC, bool WEIGHTED>
 cudaError_t launch_combine(const CombineParams& p, const LaunchGeom&, cudaStream_t s) {
   if (p.num_tokens == 0) return cudaSuccess;
-  // 32-byte chunks when every row start is 32-byte aligned
-  if (p.hidden % 16 == 0 && aligned32(p.y) && aligned32(p.out))
-    ep_combine_kernel<HC, KC, WEIGHTED, 8><<<p.num_tokens, kCombineThreads, 0, s>>>(p);
-  else
-    ep_combine_kernel<HC, KC, WEIGHTED, 4><<<p.num_tokens, kCombineThreads, 0, s>>>(p);
-  return cudaGetLastError();
+  // 32-byte chunks when every row start is 32-byte aligned; otherwise the
+  // generic variant with 16-byte chunks
+  const bool v8 = p.hidden % 16 == 0 && aligned32(p.y) && aligned32(p.out) &&
+                  (p.bias == nullptr || aligned32(p.bias));
+  if (v8) return launch_flags<HC, KC, WEIGHTED, 8>(p, s);
+  return launch_flags<0, 0, WEIGHTED, 4>(p, s);
 }
 
 template <int HC, int KC, bool WEIGHTED>
 cudaError_t prepare_combine(int, int, int, LaunchGeom* g) {
   return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-      &g->blocks_per_sm, ep_combine_kernel<HC, KC, WEIGHTED, 8>, kCombineThreads, 0);
+      &g->blocks_per_sm, ep_combine_kernel<HC, KC, WEIGHTED, 8, false, false>, kCombineThreads, 0);
 }
 
 }  // namespace

@@ -16,12 +16,16 @@
 // count tried; the register copy with many CTAs per SM reaches ~6.8 TB/s,
 // above the device's pure-write rate, because the loads overlap the stores.
 //
-//   bf16: a byte copy.
+//   copy: bf16, fp32 and packed-fp4 (Fp4x2: H channels in H/2 bytes) rows
+//         are moved as bytes, unchanged.
 //   FP8:  each 128-channel group is held by 8 (32-byte) or 16 (16-byte)
 //         consecutive lanes; amax is reduced across them with shuffles, the
 //         scale is amax/448 (IEEE division), values are x/s (IEEE division)
 //         converted with cvt.rn.satfinite.e4m3x2.f32, once per token, and the
 //         bytes plus the scale are written to every destination row.
+// Optionally each destination row also receives the routing it came with
+// (its expert id and the token's weight for it), as the pages' dispatch copy
+// epilogue fills recv_topk_idx / recv_topk_weights.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -73,33 +77,56 @@ __device__ __forceinline__ void store(void* p, const Vec<V>& r) {
 
 // Threads per CTA for a row of `chunks` vectors: the largest multiple of 32 that
 // divides it and is at most 256 (so every thread owns the same number of
-// vectors); 0 when there is none (the row is then walked in a loop).
+// vectors, at most 8); 0 when there is none (the row is then walked in a loop).
 constexpr int threads_for(int chunks) {
   for (int t = 256; t >= 32; t -= 32)
     if (chunks % t == 0 && chunks / t <= 8) return t;
   return 0;
 }
 
-constexpr int kLoopThreads = 256;
+constexpr int kMaxThreads = 256;
 
-// ---- bf16 -------------------------------------------------------------------
+// CTA size of the loop path: enough threads for `per_iter` vectors per thread
+// per iteration, a multiple of 32, at most kMaxThreads.
+inline int loop_block(int chunks, int per_iter) {
+  int t = (chunks + per_iter - 1) / per_iter;
+  t = (t + 31) / 32 * 32;
+  return t < 32 ? 32 : (t > kMaxThreads ? kMaxThreads : t);
+}
 
-template <int HC, int KC, int V>
-__global__ void __launch_bounds__(HC ? (threads_for(2 * HC / (4 * V)) ? threads_for(2 * HC / (4 * V))
-                                                                      : kLoopThreads)
-                                     : kLoopThreads)
-    ep_dispatch_bf16_kernel(DispatchParams p) {
+// Forward the routing with the rows (the dispatch copy epilogue's
+// recv_topk_weights / recv_topk_idx): row dst_slot[t][k] gets topk_weights[t][k]
+// and the expert id of (t, k).
+__device__ __forceinline__ void forward_routing(const DispatchParams& p, int t, int K,
+                                                const int32_t* sl) {
+  if (p.recv_topk_weights == nullptr && p.recv_topk_idx == nullptr) return;
+  for (int k = threadIdx.x; k < K; k += blockDim.x) {
+    const int32_t d = sl[k];
+    if (d < 0) continue;
+    const int64_t i = static_cast<int64_t>(t) * K + k;
+    if (p.recv_topk_weights) p.recv_topk_weights[d] = p.topk_weights[i];
+    if (p.recv_topk_idx) p.recv_topk_idx[d] = p.topk_i32[i];
+  }
+}
+
+// ---- copy (bf16, fp32 and packed-fp4 transports) ------------------------------
+
+template <int RB, int KC, int V>
+__global__ void __launch_bounds__(RB ? (threads_for(RB / (4 * V)) ? threads_for(RB / (4 * V))
+                                                                  : kMaxThreads)
+                                     : kMaxThreads)
+    ep_dispatch_copy_kernel(DispatchParams p) {
   constexpr int UNIT = 4 * V;  // bytes per vector
   constexpr int KM = KC ? KC : kMaxTopk;
   const int K = KC ? KC : p.topk;
-  const int row = 2 * (HC ? HC : p.hidden);
+  const int row = RB ? RB : p.row_bytes;
   const int t = blockIdx.x;
   const uint8_t* xr = static_cast<const uint8_t*>(p.x) + static_cast<int64_t>(t) * row;
   uint8_t* rx = static_cast<uint8_t*>(p.recv_x);
   const int32_t* sl = p.dst_slot + static_cast<int64_t>(t) * K;
 
-  constexpr int CH = HC ? 2 * HC / UNIT : 0;
-  constexpr int T = HC ? threads_for(CH) : 0;
+  constexpr int CH = RB ? RB / UNIT : 0;
+  constexpr int T = RB ? threads_for(CH) : 0;
   if constexpr (T != 0) {
     constexpr int PER = CH / T;
     Vec<V> v[PER];
@@ -117,11 +144,12 @@ __global__ void __launch_bounds__(HC ? (threads_for(2 * HC / (4 * V)) ? threads_
     }
   } else {
     const int chunks = row / UNIT;
+    const int nt = blockDim.x;
     int32_t d[KM];
 #pragma unroll
     for (int k = 0; k < KM; ++k) d[k] = k < K ? __ldg(sl + k) : -1;
-    for (int c0 = threadIdx.x; c0 < chunks; c0 += 2 * kLoopThreads) {
-      const int c1 = c0 + kLoopThreads;
+    for (int c0 = threadIdx.x; c0 < chunks; c0 += 2 * nt) {
+      const int c1 = c0 + nt;
       Vec<V> a, b;
       load_stream<V>(xr + static_cast<int64_t>(c0) * UNIT, a);
       if (c1 < chunks) load_stream<V>(xr + static_cast<int64_t>(c1) * UNIT, b);
@@ -134,6 +162,7 @@ __global__ void __launch_bounds__(HC ? (threads_for(2 * HC / (4 * V)) ? threads_
       }
     }
   }
+  forward_routing(p, t, K, sl);
 }
 
 // ---- FP8 --------------------------------------------------------------------
@@ -196,8 +225,8 @@ __device__ __forceinline__ void store_q(void* p, const uint32_t (&q)[V / 2]) {
 
 template <int HC, int KC, int V>
 __global__ void __launch_bounds__(HC ? (threads_for(2 * HC / (4 * V)) ? threads_for(2 * HC / (4 * V))
-                                                                      : kLoopThreads)
-                                     : kLoopThreads)
+                                                                      : kMaxThreads)
+                                     : kMaxThreads)
     ep_dispatch_fp8_kernel(DispatchParams p) {
   constexpr int UNIT = 4 * V;            // input bytes per vector (2V channels)
   constexpr int LANES = 128 / (2 * V);   // lanes per 128-channel group
@@ -241,7 +270,8 @@ __global__ void __launch_bounds__(HC ? (threads_for(2 * HC / (4 * V)) ? threads_
     int32_t d[KM];
 #pragma unroll
     for (int k = 0; k < KM; ++k) d[k] = k < K ? __ldg(sl + k) : -1;
-    for (int c0 = 0; c0 < chunks; c0 += kLoopThreads) {  // uniform trip count: shuffles see every lane
+    // uniform trip count (blockDim is a multiple of 32): the shuffles see every lane
+    for (int c0 = 0; c0 < chunks; c0 += blockDim.x) {
       const int c = c0 + threadIdx.x;
       const bool in = c < chunks;
       Vec<V> v;
@@ -260,34 +290,40 @@ __global__ void __launch_bounds__(HC ? (threads_for(2 * HC / (4 * V)) ? threads_
       }
     }
   }
+  forward_routing(p, t, K, sl);
 }
 
 // ---- launchers -------------------------------------------------------------
 
-constexpr int block_for(int hidden_c, int v) {
-  return hidden_c ? (threads_for(2 * hidden_c / (4 * v)) ? threads_for(2 * hidden_c / (4 * v))
-                                                         : kLoopThreads)
-                  : kLoopThreads;
-}
-
 inline bool aligned32(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 31u) == 0; }
 
-template <int HC, int KC>
-cudaError_t launch_bf16(const DispatchParams& p, const LaunchGeom&, cudaStream_t s) {
+template <int RB, int KC, int V>
+int copy_block(int row_bytes) {
+  constexpr int T = RB ? threads_for(RB / (4 * V)) : 0;
+  return T ? T : loop_block(row_bytes / (4 * V), 2);
+}
+
+template <int RB, int KC>
+cudaError_t launch_copy(const DispatchParams& p, const LaunchGeom&, cudaStream_t s) {
   if (p.num_tokens == 0) return cudaSuccess;
   // 32-byte vectors when every row start is 32-byte aligned
-  const bool v8 = (p.hidden % 16 == 0) && aligned32(p.x) && aligned32(p.recv_x);
-  if (v8)
-    ep_dispatch_bf16_kernel<HC, KC, 8><<<p.num_tokens, block_for(HC, 8), 0, s>>>(p);
+  if (p.row_bytes % 32 == 0 && aligned32(p.x) && aligned32(p.recv_x))
+    ep_dispatch_copy_kernel<RB, KC, 8><<<p.num_tokens, copy_block<RB, KC, 8>(p.row_bytes), 0, s>>>(p);
   else
-    ep_dispatch_bf16_kernel<HC, KC, 4><<<p.num_tokens, block_for(HC, 4), 0, s>>>(p);
+    ep_dispatch_copy_kernel<RB, KC, 4><<<p.num_tokens, copy_block<RB, KC, 4>(p.row_bytes), 0, s>>>(p);
   return cudaGetLastError();
 }
 
-template <int HC, int KC>
-cudaError_t prepare_bf16(int, int, int, LaunchGeom* g) {
+template <int RB, int KC>
+cudaError_t prepare_copy(int, int, int, LaunchGeom* g) {
   return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-      &g->blocks_per_sm, ep_dispatch_bf16_kernel<HC, KC, 8>, block_for(HC, 8), 0);
+      &g->blocks_per_sm, ep_dispatch_copy_kernel<RB, KC, 8>, kMaxThreads, 0);
+}
+
+template <int HC, int KC, int V>
+int fp8_block(int hidden) {
+  constexpr int T = HC ? threads_for(2 * HC / (4 * V)) : 0;
+  return T ? T : loop_block(2 * hidden / (4 * V), 1);
 }
 
 template <int HC, int KC>
@@ -295,36 +331,50 @@ cudaError_t launch_fp8(const DispatchParams& p, const LaunchGeom&, cudaStream_t 
   if (p.num_tokens == 0) return cudaSuccess;
   // hidden % 128 == 0 here, so 32-byte input vectors only need an aligned x
   if (aligned32(p.x))
-    ep_dispatch_fp8_kernel<HC, KC, 8><<<p.num_tokens, block_for(HC, 8), 0, s>>>(p);
+    ep_dispatch_fp8_kernel<HC, KC, 8><<<p.num_tokens, fp8_block<HC, KC, 8>(p.hidden), 0, s>>>(p);
   else
-    ep_dispatch_fp8_kernel<HC, KC, 4><<<p.num_tokens, block_for(HC, 4), 0, s>>>(p);
+    ep_dispatch_fp8_kernel<HC, KC, 4><<<p.num_tokens, fp8_block<HC, KC, 4>(p.hidden), 0, s>>>(p);
   return cudaGetLastError();
 }
 
 template <int HC, int KC>
 cudaError_t prepare_fp8(int, int, int, LaunchGeom* g) {
   return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-      &g->blocks_per_sm, ep_dispatch_fp8_kernel<HC, KC, 8>, block_for(HC, 8), 0);
+      &g->blocks_per_sm, ep_dispatch_fp8_kernel<HC, KC, 8>, kMaxThreads, 0);
 }
 
 }  // namespace
 
 Variant<DispatchLaunch> FindDispatch(int hidden, int topk, EpDType dtype) {
-  if (dtype == EpDType::Bf16) {
-#define EPG_CASE(H, K)                                                         \
-  if (hidden == H && topk == K)                                                \
-    return {"ep_dispatch_bf16_h" #H "_k" #K, launch_bf16<H, K>, prepare_bf16<H, K>};
-    EPG_SHAPE_LIST(EPG_CASE)
+  switch (dtype) {
+    case EpDType::Bf16:
+#define EPG_CASE(H, K)                                                            \
+  if (hidden == H && topk == K)                                                   \
+    return {"ep_dispatch_bf16_h" #H "_k" #K, launch_copy<2 * H, K>, prepare_copy<2 * H, K>};
+      EPG_SHAPE_LIST(EPG_CASE)
 #undef EPG_CASE
-    return {"ep_dispatch_bf16_generic", launch_bf16<0, 0>, prepare_bf16<0, 0>};
-  }
-  if (dtype == EpDType::Fp8) {
+      return {"ep_dispatch_bf16_generic", launch_copy<0, 0>, prepare_copy<0, 0>};
+    case EpDType::Fp32:
+#define EPG_CASE(H, K)                                                            \
+  if (hidden == H && topk == K)                                                   \
+    return {"ep_dispatch_fp32_h" #H "_k" #K, launch_copy<4 * H, K>, prepare_copy<4 * H, K>};
+      EPG_SHAPE_LIST(EPG_CASE)
+#undef EPG_CASE
+      return {"ep_dispatch_fp32_generic", launch_copy<0, 0>, prepare_copy<0, 0>};
+    case EpDType::Fp4x2:
+#define EPG_CASE(H, K)                                                            \
+  if (hidden == H && topk == K)                                                   \
+    return {"ep_dispatch_fp4x2_h" #H "_k" #K, launch_copy<H / 2, K>, prepare_copy<H / 2, K>};
+      EPG_SHAPE_LIST(EPG_CASE)
+#undef EPG_CASE
+      return {"ep_dispatch_fp4x2_generic", launch_copy<0, 0>, prepare_copy<0, 0>};
+    case EpDType::Fp8:
 #define EPG_CASE(H, K)                                                         \
   if (hidden == H && topk == K)                                                \
     return {"ep_dispatch_fp8_h" #H "_k" #K, launch_fp8<H, K>, prepare_fp8<H, K>};
-    EPG_SHAPE_LIST(EPG_CASE)
+      EPG_SHAPE_LIST(EPG_CASE)
 #undef EPG_CASE
-    return {"ep_dispatch_fp8_generic", launch_fp8<0, 0>, prepare_fp8<0, 0>};
+      return {"ep_dispatch_fp8_generic", launch_fp8<0, 0>, prepare_fp8<0, 0>};
   }
   return {nullptr, nullptr, nullptr};
 }

@@ -38,6 +38,7 @@ struct LayoutParams {
   int32_t* dst_slot;         // [N, K]
   int32_t* meta;             // [rcap, K+2]
   int32_t* err;              // [1]
+  int32_t* topk_i32;         // [N, K] clone of the ids (-1 where skipped), or nullptr
   uint32_t epr_magic;        // RankMagic(num_expert_per_rank)
   // scratch (BindLayoutScratch): per-chunk column histograms, column-major [E+W][C]
   int32_t* chunk_hist;
@@ -46,24 +47,32 @@ struct LayoutParams {
 };
 
 struct DispatchParams {
-  const void* x;             // bf16 [N, H]
-  void* recv_x;              // bf16 or e4m3 [Rcap, H]
+  const void* x;             // [N, row_bytes] (bf16 for FP8 dispatch)
+  void* recv_x;              // [Rcap, row_bytes] (e4m3 [Rcap, H] for FP8)
   float* recv_scales;        // fp32 [Rcap, H/128] (FP8 only)
   const int32_t* dst_slot;   // [N, K]
   int num_tokens;
   int hidden;
   int topk;
+  int row_bytes;             // bytes of one transported row (copy transports)
   int32_t* err;
+  // routing forwarded with the rows (both nullptr: not forwarded)
+  const float* topk_weights;   // fp32 [N, K]
+  const int32_t* topk_i32;     // int32 [N, K] expert ids (the handle's clone)
+  float* recv_topk_weights;    // fp32 [Rcap] or nullptr
+  int32_t* recv_topk_idx;      // int32 [Rcap] or nullptr
 };
 
 struct CombineParams {
   const void* y;             // bf16 [Rcap, H]
   const float* weights;      // fp32 [N, K] or nullptr
-  void* out;                 // bf16 [N, H]
+  const void* bias;          // bf16 [N, H] or nullptr
+  void* out;                 // bf16 or fp32 [N, H]
   const int32_t* dst_slot;   // [N, K]
   int num_tokens;
   int hidden;
   int topk;
+  int out_f32;               // 1: fp32 output, 0: bf16
 };
 
 // Launch geometry of a variant on the current device, filled by its prepare

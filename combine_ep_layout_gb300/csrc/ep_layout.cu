@@ -131,11 +131,13 @@ __global__ void __launch_bounds__(kCountThreads) ep_layout_count_kernel(LayoutPa
 
   allow_dependents();
   bool bad = false;
+  int32_t* clone = p.topk_i32 ? p.topk_i32 + static_cast<int64_t>(t0) * K : nullptr;
   for (int i = tid; i < nent; i += kCountThreads) {
     const int64_t v = topk[i];
     const int e = expert_of(v, E);
     bad |= (e < 0 && v != -1);
     ids[i] = e;
+    if (clone) clone[i] = e;
   }
   for (int i = tid; i < NW * EW; i += kCountThreads) whist[i] = 0;
   for (int i = tid; i < kLayoutTPC; i += kCountThreads) tokmask[i] = 0ull;

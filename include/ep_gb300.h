@@ -23,8 +23,8 @@
  *     handle owns its routing metadata (allocated by ep_handle_create, freed
  *     by ep_handle_free).
  *   - Work is enqueued on `stream` (NULL = the legacy default stream); no
- *     entry point synchronises except ep_handle_status.  ep_layout,
- *     ep_dispatch and ep_combine allocate nothing and can be enqueued while a
+ *     entry point synchronises except ep_handle_status.  The layout,
+ *     dispatch and combine calls allocate nothing and can be enqueued while a
  *     stream is being captured into a CUDA graph.
  *   - Return value 0 on success, else one of the negative EP_E* codes, with
  *     a message available from ep_last_error() on the calling thread.
@@ -45,10 +45,13 @@ extern "C" {
 typedef struct CUstream_st *ep_stream_t;
 
 /* Transport dtype of the dispatched rows; numbering as EpDType in
- * "MORI JIT v2" §3.7 (Bf16 = 0, Fp32 = 1, Fp8 = 2, Fp4x2 = 3).  This library
- * dispatches EP_BF16 (a byte copy) and EP_FP8_E4M3 (a fused cast from bf16 to
- * OCP e4m3 with one fp32 scale per 128 channels); the other two are rejected
- * with EP_EUNSUPPORTED. */
+ * "MORI JIT v2" §3.7 (Bf16 = 0, Fp32 = 1, Fp8 = 2, Fp4x2 = 3).
+ *   EP_BF16, EP_FP32  rows of H bf16 / fp32 values, moved as bytes;
+ *   EP_FP4X2          rows of H packed e2m1 values (H/2 bytes, two per byte),
+ *                     moved as bytes (the payload arrives already packed);
+ *   EP_FP8_E4M3       bf16 rows cast on the way to OCP e4m3, one fp32 scale
+ *                     per 128 channels.
+ * Combine always reduces bf16 expert outputs, whatever was dispatched. */
 typedef enum {
     EP_BF16 = 0,
     EP_FP32 = 1,
@@ -62,7 +65,7 @@ typedef enum {
  *   1 <= num_expert_per_rank, world_size*num_expert_per_rank <= 2048,
  *   1 <= num_expert_per_token <= 16, 1 <= expert_alignment <= 4096,
  *   hidden_dim >= 8, hidden_dim % 8 == 0 (rows are whole 16-byte units), hidden_dim <= 32768;
- *   for EP_FP8_E4M3 also hidden_dim % 128 == 0;
+ *   for EP_FP8_E4M3 also hidden_dim % 128 == 0, for EP_FP4X2 hidden_dim % 32 == 0;
  *   the receive capacity (ep_recv_capacity) must fit in int32. */
 typedef struct {
     int32_t world_size;           /* W: logical ranks */
@@ -96,7 +99,7 @@ int64_t ep_recv_capacity(const ep_cfg_t *cfg) EP_NOEXCEPT;
 /* Validate cfg, pick the compiled kernel variants for it and allocate the
  * handle's device metadata on the current device (cudaMalloc; sized for W*T
  * tokens).  *out receives the handle.  Errors: EP_EINVAL (bad cfg or NULL),
- * EP_EUNSUPPORTED (dispatch dtype not served), EP_ENOMEM, EP_ECUDA. */
+ * EP_EUNSUPPORTED, EP_ENOMEM, EP_ECUDA. */
 int ep_handle_create(const ep_cfg_t *cfg, ep_handle_t *out) EP_NOEXCEPT;
 
 /* Layout.  topk_idx: device int64 [num_tokens, K] row-major, token t of
@@ -120,18 +123,31 @@ int ep_handle_create(const ep_cfg_t *cfg, ep_handle_t *out) EP_NOEXCEPT;
 int ep_layout(ep_handle_t h, const int64_t *topk_idx, int32_t num_tokens, ep_stream_t stream) EP_NOEXCEPT;
 
 /* Dispatch ("Dispatch data flow": token data + scale factors to the receive
- * buffer).  x: device bf16 [N, H] row-major (16-byte aligned).
- * EP_BF16:     recv_x device bf16 [Rcap, H]; recv_x[dst_slot[t][k]] = x[t], bit-exact.
- * EP_FP8_E4M3: recv_x device uint8 (e4m3) [Rcap, H], recv_scales device fp32
+ * buffer).  x: device [N, row] row-major, 16-byte aligned.
+ * EP_BF16 / EP_FP32 / EP_FP4X2: x holds bf16 / fp32 / packed-e2m1 rows and
+ *              recv_x [Rcap, row] receives recv_x[dst_slot[t][k]] = x[t], bit-exact.
+ * EP_FP8_E4M3: x bf16 [N, H]; recv_x device uint8 (e4m3) [Rcap, H], recv_scales device fp32
  *              [Rcap, H/128]; per token and 128-channel group g:
  *              s = amax|x[t, g]| / 448 (fp32), q = e4m3_rn_satfinite(x / s),
  *              s = 0 and q = 0 when amax = 0; written to every row dst_slot[t][k].
- * recv_scales must be NULL for EP_BF16 and non-NULL for EP_FP8_E4M3.  Rows
+ * recv_scales must be non-NULL for EP_FP8_E4M3 and NULL otherwise.  Rows
  * that receive no token are not written.  Uses the routing of the last
  * ep_layout call on this handle (same stream, or ordered after it).
  * Buffers must be 16-byte aligned, else EP_EINVAL. */
 int ep_dispatch(ep_handle_t h, const void *x, void *recv_x, float *recv_scales,
                 ep_stream_t stream) EP_NOEXCEPT;
+
+/* Dispatch that also forwards the routing with each received row (the copy
+ * epilogue of the "Dispatch data flow" fills recv_topk_idx and
+ * recv_topk_weights).  Same as ep_dispatch, and for every received (t, k):
+ *   recv_topk_weights[dst_slot[t][k]] = topk_weights[t][k]   (fp32 [Rcap])
+ *   recv_topk_idx[dst_slot[t][k]]     = topk_idx[t][k]       (int32 [Rcap], global expert id)
+ * Either output may be NULL (then it is not written); topk_weights (device
+ * fp32 [N, K]) is required when recv_topk_weights is given.  Rows that
+ * receive nothing are not written. */
+int ep_dispatch_fwd(ep_handle_t h, const void *x, void *recv_x, float *recv_scales,
+                    const float *topk_weights, float *recv_topk_weights, int32_t *recv_topk_idx,
+                    ep_stream_t stream) EP_NOEXCEPT;
 
 /* Combine ("Combine data flow": reduce weighted by topk_weights back to token
  * order).  y: device bf16 [Rcap, H] expert outputs, in the receive layout;
@@ -181,6 +197,15 @@ int ep_layout_noalloc(const ep_cfg_t *cfg, const int64_t *topk_idx, int32_t num_
                       int32_t *dst_slot, int32_t *recv_src_metadata, int32_t *device_error,
                       ep_stream_t stream) EP_NOEXCEPT;
 
+/* Combine with a bias and a choice of output ("Combine data flow": reduce
+ * weighted by topk_weights, "+ bias", write back).  As ep_combine, and then
+ *   acc += bias[t][c]            (bias: device bf16 [N, H], or NULL; one fp32 add)
+ *   out[t][c] = acc              (out_dtype EP_FP32: out device fp32 [N, H])
+ *   out[t][c] = bf16_rn(acc)     (out_dtype EP_BF16: out device bf16 [N, H])
+ * Other out_dtype values return EP_EINVAL. */
+int ep_combine_ex(ep_handle_t h, const void *y, const float *topk_weights, const void *bias,
+                  void *out, int32_t out_dtype, ep_stream_t stream) EP_NOEXCEPT;
+
 /* Release the handle and its device memory (cudaFree, which waits for work
  * using it to finish).  NULL is ignored. */
 void ep_handle_free(ep_handle_t h) EP_NOEXCEPT;
@@ -194,7 +219,8 @@ enum {
     EP_FIELD_DST_SLOT = 4,                 /* int32 [N, K] (N of the last layout) */
     EP_FIELD_RECV_SRC_METADATA = 5,        /* int32 [Rcap, K+2] */
     EP_FIELD_NUM_RECV = 6,                 /* int32 [1] */
-    EP_FIELD_DEVICE_ERROR = 7              /* int32 [1], sticky error bits */
+    EP_FIELD_DEVICE_ERROR = 7,             /* int32 [1], sticky error bits */
+    EP_FIELD_TOPK_IDX = 8                  /* int32 [N, K] copy of topk_idx (-1 where skipped) */
 };
 
 /* Device pointer and element count of one handle field (the handle keeps
@@ -202,9 +228,9 @@ enum {
 int ep_handle_get(ep_handle_t h, int32_t field, void **dev_ptr, int64_t *numel) EP_NOEXCEPT;
 
 /* Synchronise the handle's last stream, read and clear the sticky device
- * error word.  Bits: 1 = a topk id outside [-1, E) was skipped; 2 = a kernel
- * gave up waiting on one of its own copies (the kernel returned early and its
- * outputs are incomplete).  Returns EP_ECUDA if the synchronisation fails. */
+ * error word.  Bits: 1 = a topk id outside [-1, E) was skipped; 2 is reserved
+ * for a kernel that gave up a bounded wait (no kernel of this version waits).
+ * Returns EP_ECUDA if the synchronisation fails. */
 int ep_handle_status(ep_handle_t h, int32_t *device_error) EP_NOEXCEPT;
 
 /* Name of the kernel variant chosen for a step (0 = layout, 1 = dispatch,

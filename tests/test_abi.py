@@ -23,7 +23,7 @@ def built():
 
 def test_exports_every_declared_symbol():
     names = ep.declared_symbols()
-    assert len(names) == 11
+    assert len(names) == 13
     L = ep.load_library()
     for n in names:
         assert hasattr(L, n), n
@@ -70,13 +70,16 @@ def test_invalid_configs_are_rejected_on_the_host(bad):
     assert L.ep_recv_capacity(ctypes.byref(cfg)) == ep.EP_EINVAL
 
 
-@pytest.mark.parametrize("dt", [ep.EP_FP32, ep.EP_FP4X2])
-def test_unserved_dtypes_are_unsupported(dt):
-    cfg = ep.make_cfg(8, 7168, 128, 8, 8, 1, dt, True)
+def test_transport_dtypes_are_validated():
+    L = ep.load_library()
+    # fp32 and packed fp4 rows are served (capacity is answered without a GPU)
+    for dt in (ep.EP_FP32, ep.EP_FP4X2):
+        assert L.ep_recv_capacity(ctypes.byref(ep.make_cfg(8, 7168, 128, 8, 8, 1, dt, True))) > 0
+    # an fp4 row must be a whole number of 16-byte units: hidden % 32 == 0
+    bad = ep.make_cfg(8, 7176, 128, 8, 8, 1, ep.EP_FP4X2, True)
     h = ctypes.c_void_p()
-    assert ep.load_library().ep_handle_create(ctypes.byref(cfg), ctypes.byref(h)) == \
-        ep.EP_EUNSUPPORTED
-    assert "dtype" in ep.ep_last_error()
+    assert L.ep_handle_create(ctypes.byref(bad), ctypes.byref(h)) == ep.EP_EINVAL
+    assert "FP4x2" in ep.ep_last_error()
 
 
 def test_null_arguments_are_errors_not_crashes():
