@@ -36,8 +36,10 @@ WORKLOAD = "prefill"
 WORKLOAD_DESC = ("prefill: 8 logical ranks x 4096 tokens = 32768 tokens, hidden 7168 bf16 ~N(0,1), "
                  "256 experts (32/rank), top-8 uniform distinct, softmax weights, expert_alignment "
                  "128; dispatch bf16 and FP8 e4m3 (per-128 fp32 scales); combine bf16 with fp32 fma")
-KERNEL_SOURCES = ["ep_layout.cu", "ep_dispatch.cu", "ep_combine.cu", "ep_ptx.cuh", "ep_cfg.hpp",
-                  "ep_kernels.hpp"]
+SHARED_SOURCES = ["ep_ptx.cuh", "ep_cfg.hpp", "ep_kernels.hpp"]
+KERNEL_FILES = {"ep_dispatch_copy_kernel": "ep_dispatch.cu", "ep_dispatch_fp8_kernel": "ep_dispatch.cu",
+                "ep_combine_kernel": "ep_combine.cu", "ep_layout_count_kernel": "ep_layout.cu",
+                "ep_layout_spine_kernel": "ep_layout.cu", "ep_layout_slots_kernel": "ep_layout.cu"}
 
 
 # ----------------------------------------------------------------- helpers
@@ -82,9 +84,10 @@ def measured_peaks():
         return 6800.0, "fallback"
 
 
-def kernel_source_digest():
+def kernel_source_digest(kernel):
+    """Digest of the source file that holds `kernel` and the headers it includes."""
     h = hashlib.sha256()
-    for n in KERNEL_SOURCES:
+    for n in [KERNEL_FILES[kernel]] + SHARED_SOURCES:
         with open(os.path.join(ROOT, "combine_ep_layout_gb300", "csrc", n), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -96,13 +99,12 @@ def ncu_traffic(kernel):
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     try:
         with open(path) as f:
-            d = json.load(f)
+            k = json.load(f).get("kernels", {}).get(kernel)
     except Exception:
         return None
-    if d.get("source_digest") != kernel_source_digest():
+    if k is None or k.get("source_digest") != kernel_source_digest(kernel):
         return None
-    k = d.get("kernels", {}).get(kernel)
-    return None if k is None else k.get("dram_bytes_per_launch")
+    return k.get("dram_bytes_per_launch")
 
 
 class ClockSampler:
@@ -267,7 +269,7 @@ def run_ours(args, rank, local_rank, world):
                       "frac_of_peak": round(gbs / peak, 4),
                       "frac_of_8tbs": round(gbs / 8000.0, 4)}
     dom = max(["dispatch_bf16", "combine", "dispatch_fp8"], key=lambda n: avg[n])
-    kname = {"dispatch_bf16": "ep_dispatch_bf16_kernel", "combine": "ep_combine_kernel",
+    kname = {"dispatch_bf16": "ep_dispatch_copy_kernel", "combine": "ep_combine_kernel",
              "dispatch_fp8": "ep_dispatch_fp8_kernel"}[dom]
     roof = {"bound": "hbm", "kernel": dom, "achieved": kernels[dom]["gbs"], "peak": peak,
             "peak_kind": peak_kind + " hbm_gbs (burst copy)", "unit": "GB/s",
