@@ -361,6 +361,77 @@ def run_e2e(args, ep, torch, dev, wl, topk_cpu, w_cpu, x, handles, bufs, step_by
             "d2h_bytes_per_step": out_h.numel() * 2}
 
 
+# ------------------------------------------------------------- all configs
+
+def run_all_configs(args):
+    """Per workload (tiny, decode, prefill bf16, prefill FP8, skewed): layout,
+    dispatch and combine timed separately with CUDA events, L2 flushed (a 256 MB
+    write) before every step and outside the timed events; medians over
+    args.steps steps.  One JSON line per workload."""
+    import torch
+
+    import combine_ep_layout_gb300 as ep
+    import synth
+
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    peak, peak_kind = measured_peaks()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    s = torch.cuda.Stream(device=dev)
+    for name, wl in synth.WORKLOADS.items():
+        N, H, K, R = wl.num_tokens, wl.hidden, wl.topk, wl.recv_capacity
+        cfg = ep.make_cfg(wl.world_size, H, wl.max_tok_per_rank, wl.num_expert_per_rank, K,
+                          wl.alignment, wl.dispatch_dtype, wl.use_weights)
+        h = ep.EpHandle(cfg)
+        topk = synth.gen_topk(wl).to(dev)
+        w = synth.gen_weights(wl).to(dev)
+        x = synth.gen_x(wl, device=dev)
+        fp8 = wl.dispatch_dtype == "fp8"
+        recv = torch.empty((R, H), dtype=torch.uint8 if fp8 else torch.bfloat16, device=dev)
+        scales = torch.empty((R, H // 128), dtype=torch.float32, device=dev) if fp8 else None
+        # combine reads bf16 expert outputs: the dispatched rows (identity experts), or
+        # for the FP8 workload an independent bf16 N(0,1) [Rcap, H]
+        y = synth.gen_y(wl, device=dev) if fp8 else recv
+        out = torch.empty((N, H), dtype=torch.bfloat16, device=dev)
+        times = {"layout": [], "dispatch": [], "combine": []}
+        for i in range(args.warmup + args.steps):
+            with torch.cuda.stream(s):
+                flush.fill_(i & 0xFF)
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+            ev[0].record(s)
+            h.layout(topk, stream=s)
+            ev[1].record(s)
+            h.dispatch(x, recv, scales, stream=s)
+            ev[2].record(s)
+            h.combine(y, w, out, stream=s)
+            ev[3].record(s)
+            s.synchronize()
+            if i >= args.warmup:
+                for j, k in enumerate(times):
+                    times[k].append(ev[j].elapsed_time(ev[j + 1]) * 1e3)
+        assert h.status() == 0
+        nb = algorithmic_bytes(N, H, K, R)
+        dkey = "dispatch_fp8" if fp8 else "dispatch_bf16"
+        line = {"workload": name, "tokens": N, "hidden": H, "experts": wl.num_experts, "topk": K,
+                "alignment": wl.alignment, "dispatch_dtype": wl.dispatch_dtype,
+                "routing": wl.routing, "l2": "flushed before every step (256 MB write)",
+                "steps": args.steps, "peak_gbs": peak, "peak_kind": peak_kind}
+        for k, b in (("layout", nb["layout"]), ("dispatch", nb[dkey]), ("combine", nb["combine"])):
+            us = statistics.median(times[k])
+            line[k] = {"us_median": round(us, 2), "us_min": round(min(times[k]), 2),
+                       "us_max": round(max(times[k]), 2), "algorithmic_bytes": b,
+                       "gbs": round(b / (us * 1e-6) / 1e9, 1),
+                       "frac_of_peak": round(b / (us * 1e-6) / 1e9 / peak, 4),
+                       "frac_of_8tbs": round(b / (us * 1e-6) / 1e9 / 8000.0, 4),
+                       "tokens_per_s": round(N / (us * 1e-6), 1),
+                       "variant": h.variant({"layout": 0, "dispatch": 1, "combine": 2}[k])}
+        print(json.dumps(line), flush=True)
+        h.free()
+        del recv, scales, y, out, x
+        torch.cuda.empty_cache()
+    return 0
+
+
 # ------------------------------------------------------------- CPU oracle
 
 def oracle_step_sample(wl, topk_np, w_np, x_bits, tok0, ntok, bufs):
@@ -463,6 +534,8 @@ def main(argv=None):
     ap.add_argument("--ref-block", type=int, default=256)
     ap.add_argument("--tokens", type=int, default=None,
                     help="tokens of a smaller case of the prefill shape (profiling only)")
+    ap.add_argument("--all-configs", action="store_true",
+                    help="time layout / dispatch / combine on every workload (one line each)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -472,6 +545,10 @@ def main(argv=None):
         if line is not None:
             print(json.dumps(line), flush=True)
         return 0
+    if args.all_configs:
+        import __graft_entry__
+        __graft_entry__.build()
+        return run_all_configs(args)
     import torch
     import torch.distributed as dist
     if world > 1:
