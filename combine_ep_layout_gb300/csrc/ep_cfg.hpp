@@ -66,7 +66,7 @@ constexpr int64_t RecvCapacity(int64_t max_tokens, int topk, int num_experts, in
 
 // Layout chunking: the count and slot kernels give each CTA kLayoutTPC tokens.
 constexpr int kLayoutTPC = 128;
-constexpr int kLayoutCountWarps = 8;
+constexpr int kLayoutCountWarps = 16;
 constexpr int NumLayoutChunks(int num_tokens) { return (num_tokens + kLayoutTPC - 1) / kLayoutTPC; }
 
 // Limits checked when a handle is built ("MORI JIT v2" §3.5: a configuration

@@ -119,8 +119,6 @@ __global__ void __launch_bounds__(kCountThreads) ep_layout_count_kernel(LayoutPa
   extern __shared__ int32_t sm[];
   int32_t* whist = sm;                                     // [NW][EW]
   int32_t* ids = whist + NW * EW;                          // [TPC*K] expert ids, -1 = skip
-  unsigned long long* tokmask =                            // [TPC] ranks touched by a token
-      reinterpret_cast<unsigned long long*>(ids + ((kLayoutTPC * K + 1) & ~1));
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int c = blockIdx.x;
@@ -140,7 +138,6 @@ __global__ void __launch_bounds__(kCountThreads) ep_layout_count_kernel(LayoutPa
     if (clone) clone[i] = e;
   }
   for (int i = tid; i < NW * EW; i += kCountThreads) whist[i] = 0;
-  for (int i = tid; i < kLayoutTPC; i += kCountThreads) tokmask[i] = 0ull;
   __syncthreads();
 
   // per-warp histogram over a contiguous run of entries (whole 32-entry batches)
@@ -152,17 +149,16 @@ __global__ void __launch_bounds__(kCountThreads) ep_layout_count_kernel(LayoutPa
     const int e = ids[i];
     if (e >= 0) atomicAdd(&wh[e], 1);
   }
-  // ranks touched by each token
-  for (int i = tid; i < nent; i += kCountThreads) {
-    const int e = ids[i];
-    if (e >= 0) atomicOr(&tokmask[i / K], 1ull << rank_of(e, p.epr_magic));
-  }
-  __syncthreads();
-
-  // tokens per rank: warp ballots over the token masks
+  // tokens per rank: each thread builds its token's rank mask in registers
+  // (no atomics: all K entries of a token would hit one word), warp ballots count
   for (int tl0 = warp * 32; tl0 < ntok; tl0 += kCountThreads) {
     const int tl = tl0 + lane;
-    const unsigned long long mask = tl < ntok ? tokmask[tl] : 0ull;
+    unsigned long long mask = 0ull;
+    if (tl < ntok)
+      for (int k = 0; k < K; ++k) {
+        const int e = ids[tl * K + k];
+        if (e >= 0) mask |= 1ull << rank_of(e, p.epr_magic);
+      }
     for (int r = 0; r < W; ++r) {
       const int n = __popc(__ballot_sync(0xffffffffu, (mask >> r) & 1ull));
       if (lane == 0 && n) atomicAdd(&whist[E + r], n);
@@ -331,13 +327,25 @@ __global__ void __launch_bounds__(kSlotThreads) ep_layout_slots_kernel(LayoutPar
   // concatenated rows; rows of one expert are contiguous in memory.
   if (has_tokens) {
     const int nvalid = cx[E];
-    const int nwords = nvalid * KW;
-    for (int f = threadIdx.x; f < nwords; f += kSlotThreads) {
-      const int q = f / KW, col = f - q * KW;
-      const int entry = sorted[q];
-      const int tl = entry / K;
-      const int v = col < 2 ? src[2 * tl + col] : slots_s[tl * K + col - 2];
-      p.meta[static_cast<int64_t>(slots_s[entry]) * KW + col] = v;
+    if ((KW & 1) == 0) {
+      // even row width: word pairs (8-byte stores; rows start 8-byte aligned)
+      const int hw = KW / 2;
+      for (int f = threadIdx.x; f < nvalid * hw; f += kSlotThreads) {
+        const int q = f / hw, c2 = f - q * hw;
+        const int entry = sorted[q];
+        const int tl = entry / K;
+        const int2 v = c2 == 0 ? make_int2(src[2 * tl], src[2 * tl + 1])
+                               : make_int2(slots_s[tl * K + 2 * c2 - 2], slots_s[tl * K + 2 * c2 - 1]);
+        reinterpret_cast<int2*>(p.meta + static_cast<int64_t>(slots_s[entry]) * KW)[c2] = v;
+      }
+    } else {
+      for (int f = threadIdx.x; f < nvalid * KW; f += kSlotThreads) {
+        const int q = f / KW, col = f - q * KW;
+        const int entry = sorted[q];
+        const int tl = entry / K;
+        const int v = col < 2 ? src[2 * tl + col] : slots_s[tl * K + col - 2];
+        p.meta[static_cast<int64_t>(slots_s[entry]) * KW + col] = v;
+      }
     }
   }
 
@@ -375,9 +383,8 @@ cudaError_t launch_dependent(Kern kernel, int grid, int block, size_t smem, cuda
 }
 
 size_t count_smem(int topk, int cols) {
-  const size_t ids = (static_cast<size_t>(kLayoutTPC) * topk + 1) & ~static_cast<size_t>(1);
-  return sizeof(int32_t) * (static_cast<size_t>(kLayoutCountWarps) * cols + ids) +
-         sizeof(unsigned long long) * kLayoutTPC;
+  return sizeof(int32_t) * (static_cast<size_t>(kLayoutCountWarps) * cols +
+                            static_cast<size_t>(kLayoutTPC) * topk);
 }
 
 size_t slots_smem(int E, int topk) {
