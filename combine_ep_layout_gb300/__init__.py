@@ -10,5 +10,5 @@ from ._native import (  # noqa: F401
     EpError, EpHandle, ep_cfg_t, make_cfg, load_library, declared_symbols,
     ep_recv_capacity, ep_handle_create, ep_layout, ep_dispatch, ep_combine, ep_handle_free,
     ep_handle_get, ep_handle_status, ep_handle_variant, ep_last_error,
-    ep_layout_noalloc, NOALLOC_OUTPUTS, ep_dispatch_fwd, ep_combine_ex,
+    ep_layout_noalloc, NOALLOC_OUTPUTS, ep_dispatch_fwd, ep_combine_ex, ep_jit_precompile,
 )

@@ -78,6 +78,8 @@ def load_library():
     L.ep_handle_variant.argtypes = [vp, i32, c.c_char_p, i32]
     L.ep_last_error.restype = c.c_char_p
     L.ep_last_error.argtypes = []
+    L.ep_jit_precompile.restype = c.c_int
+    L.ep_jit_precompile.argtypes = [c.POINTER(ep_cfg_t), c.c_char_p, c.c_char_p, i32]
     L.ep_layout_noalloc.restype = c.c_int
     L.ep_layout_noalloc.argtypes = [c.POINTER(ep_cfg_t), vp, i32] + [vp] * 8 + [vp]
     _lib = L
@@ -283,3 +285,14 @@ def ep_layout_noalloc(cfg, topk_idx, out, stream=None):
     _check(load_library().ep_layout_noalloc(
         ctypes.byref(cfg), _ptr(topk_idx) if n else None, n,
         *[_ptr(out[k]) for k in NOALLOC_OUTPUTS], _stream_ptr(stream, topk_idx.device)))
+
+
+def ep_jit_precompile(cfg, arch=None):
+    """Compile (or find in the disk cache) the run-time specialisations cfg would
+    use; returns (number compiled now, report lines).  Needs NVRTC, not a GPU."""
+    buf = ctypes.create_string_buffer(8192)
+    rc = load_library().ep_jit_precompile(ctypes.byref(cfg), arch.encode() if arch else None,
+                                          buf, 8192)
+    if rc < 0:
+        raise EpError(rc, ep_last_error())
+    return rc, buf.value.decode().splitlines()

@@ -17,6 +17,7 @@
 
 #include "ep_cfg.hpp"
 #include "ep_gb300.h"
+#include "ep_jit.hpp"
 #include "ep_kernels.hpp"
 
 using namespace epg;
@@ -95,9 +96,32 @@ struct ep_handle {
   Variant<DispatchLaunch> dispatch{};
   Variant<CombineLaunch> combine{};
   LaunchGeom g_layout{}, g_dispatch{}, g_combine{};
+  // run-time specialisations for shapes outside the compiled table (function
+  // null when not used); they serve 32-byte-aligned buffers, the compiled
+  // generic variant everything else
+  jit::Kernel jit_dispatch, jit_combine;
 };
 
 namespace {
+
+bool is_generic(const char* name) {
+  const size_t n = std::strlen(name);
+  return n >= 8 && std::strcmp(name + n - 8, "_generic") == 0;
+}
+
+jit::Request dispatch_request(const ep_cfg_t* c) {
+  const EpDType dt = static_cast<EpDType>(c->dispatch_dtype);
+  if (dt == EpDType::Fp8)
+    return {jit::Request::kFp8, 0, c->hidden_dim, c->num_expert_per_token, false};
+  return {jit::Request::kCopy, static_cast<int>(RowBytes(c->hidden_dim, dt)), c->hidden_dim,
+          c->num_expert_per_token, false};
+}
+
+jit::Request combine_request(const ep_cfg_t* c) {
+  return {jit::Request::kCombine, 0, c->hidden_dim, c->num_expert_per_token, c->use_weights != 0};
+}
+
+bool aligned32(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 31u) == 0; }
 
 int check_device(const ep_handle* h) {
   int dev = -1;
@@ -170,6 +194,14 @@ int ep_handle_create(const ep_cfg_t* cfg, ep_handle_t* out) noexcept {
       return bail(fail(EP_EUNSUPPORTED, "dispatch kernel does not fit on an SM for this hidden_dim"));
     if ((e = h->combine.prepare(h->H, h->K, 0, &h->g_combine)) != cudaSuccess)
       return bail(fail_cuda(e, "combine kernel set-up"));
+    // shapes outside the compiled table: specialise at run time when possible;
+    // when not (no NVRTC, switched off), the compiled generic variants serve
+    if (jit::Enabled()) {
+      std::string why;
+      const jit::Request dr = dispatch_request(cfg), cr = combine_request(cfg);
+      if (is_generic(h->dispatch.name) && jit::Worthwhile(dr)) jit::Load(dr, &h->jit_dispatch, &why);
+      if (is_generic(h->combine.name) && jit::Worthwhile(cr)) jit::Load(cr, &h->jit_combine, &why);
+    }
 
     // one allocation, 256-byte aligned sub-buffers
     auto al = [](size_t b) { return (b + 255) & ~static_cast<size_t>(255); };
@@ -294,7 +326,9 @@ int ep_dispatch_fwd(ep_handle_t h, const void* x, void* recv_x, float* recv_scal
     p.recv_topk_weights = recv_topk_weights;
     p.recv_topk_idx = recv_topk_idx;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    cudaError_t e = h->dispatch.launch(p, h->g_dispatch, s);
+    const bool jit_ok = h->jit_dispatch.function && aligned32(x) && aligned32(recv_x);
+    cudaError_t e = jit_ok ? jit::Launch(h->jit_dispatch, p.num_tokens, &p, s)
+                           : h->dispatch.launch(p, h->g_dispatch, s);
     if (e != cudaSuccess) return fail_cuda(e, "dispatch launch");
     h->last_stream = s;
     return EP_OK;
@@ -338,7 +372,10 @@ int ep_combine_ex(ep_handle_t h, const void* y, const float* topk_weights, const
     p.topk = h->K;
     p.out_f32 = out_dtype == EP_FP32 ? 1 : 0;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    cudaError_t e = h->combine.launch(p, h->g_combine, s);
+    const bool jit_ok = h->jit_combine.function && !bias && p.out_f32 == 0 && aligned32(y) &&
+                        aligned32(out);
+    cudaError_t e = jit_ok ? jit::Launch(h->jit_combine, p.num_tokens, &p, s)
+                           : h->combine.launch(p, h->g_combine, s);
     if (e != cudaSuccess) return fail_cuda(e, "combine launch");
     h->last_stream = s;
     return EP_OK;
@@ -408,12 +445,53 @@ int ep_handle_variant(ep_handle_t h, int32_t step, char* buf, int32_t len) noexc
   try {
     if (!h || !buf || len < 1) return fail(EP_EINVAL, "NULL argument");
     const char* name = step == 0 ? h->layout.name
-                     : step == 1 ? h->dispatch.name
-                     : step == 2 ? h->combine.name
+                     : step == 1 ? (h->jit_dispatch.function ? h->jit_dispatch.name.c_str()
+                                                             : h->dispatch.name)
+                     : step == 2 ? (h->jit_combine.function ? h->jit_combine.name.c_str()
+                                                            : h->combine.name)
                                  : nullptr;
     if (!name) return fail(EP_EINVAL, "step must be 0, 1 or 2");
     std::snprintf(buf, static_cast<size_t>(len), "%s", name);
     return EP_OK;
+  } catch (...) {
+    return fail(EP_EINVAL, "unknown exception");
+  }
+}
+
+int ep_jit_precompile(const ep_cfg_t* cfg, const char* arch, char* report, int32_t len) noexcept {
+  try {
+    int rc = validate(cfg);
+    if (rc != EP_OK) return rc;
+    std::string rep;
+    int compiled_now = 0;
+    const std::string a = arch && *arch ? arch : "sm_103a";
+    const Variant<DispatchLaunch> dv =
+        FindDispatch(cfg->hidden_dim, cfg->num_expert_per_token,
+                     static_cast<EpDType>(cfg->dispatch_dtype));
+    const Variant<CombineLaunch> cv =
+        FindCombine(cfg->hidden_dim, cfg->num_expert_per_token, cfg->use_weights != 0);
+    const jit::Request reqs[2] = {dispatch_request(cfg), combine_request(cfg)};
+    const char* names[2] = {dv.name, cv.name};
+    for (int i = 0; i < 2; ++i) {
+      if (!is_generic(names[i])) {
+        rep += std::string(names[i]) + " compiled-in\n";
+        continue;
+      }
+      if (!jit::Worthwhile(reqs[i])) {
+        rep += std::string(names[i]) + " generic\n";
+        continue;
+      }
+      bool compiled = false;
+      std::string dir, err;
+      if (!jit::Prepare(reqs[i], a, &compiled, &dir, &err))
+        return fail(err.find("not available") != std::string::npos ? EP_EUNSUPPORTED : EP_ECUDA, err);
+      compiled_now += compiled ? 1 : 0;
+      rep += jit::EntryName(reqs[i]) + (compiled ? " compiled " : " cached ") + dir + "\n";
+    }
+    if (report && len > 0) std::snprintf(report, static_cast<size_t>(len), "%s", rep.c_str());
+    return compiled_now;
+  } catch (const std::exception& ex) {
+    return fail(EP_EINVAL, ex.what());
   } catch (...) {
     return fail(EP_EINVAL, "unknown exception");
   }

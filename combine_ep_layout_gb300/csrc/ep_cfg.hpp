@@ -17,7 +17,20 @@
 // they only enter the layout, which is integer work on a few MB.
 #pragma once
 
+#if defined(__CUDACC_RTC__)
+// NVRTC compiles the kernel bodies at run time without the C library headers.
+typedef signed char int8_t;
+typedef unsigned char uint8_t;
+typedef short int16_t;
+typedef unsigned short uint16_t;
+typedef int int32_t;
+typedef unsigned int uint32_t;
+typedef long long int64_t;
+typedef unsigned long long uint64_t;
+typedef unsigned long long uintptr_t;
+#else
 #include <cstdint>
+#endif
 
 namespace epg {
 
@@ -62,6 +75,17 @@ constexpr int64_t AlignUp(int64_t v, int64_t a) { return (v + a - 1) / a * a; }
 // Rows of the receive buffer for any routing of max_tokens tokens.
 constexpr int64_t RecvCapacity(int64_t max_tokens, int topk, int num_experts, int alignment) {
   return max_tokens * topk + (int64_t)num_experts * (alignment - 1);
+}
+
+// Threads per CTA of the row kernels for a row of `chunks` vectors: the largest
+// multiple of 32 that divides it and is at most 256 (every thread owns the same
+// number of vectors, at most 8); 0 when there is none (the row is walked in a
+// loop by kRowLoopThreads-or-fewer threads).
+constexpr int kRowMaxThreads = 256;
+constexpr int RowThreads(int chunks) {
+  for (int t = kRowMaxThreads; t >= 32; t -= 32)
+    if (chunks % t == 0 && chunks / t <= 8) return t;
+  return 0;
 }
 
 // Layout chunking: the count and slot kernels give each CTA kLayoutTPC tokens.

@@ -1,0 +1,249 @@
+// ep_dispatch_body.cuh -- device code of the dispatch kernels (row copy for
+// the bf16 / fp32 / packed-fp4 transports, fused FP8 cast, routing
+// forwarding).  Included by ep_dispatch.cu, which instantiates the compiled
+// variants, and rendered into the run-time specialisations (ep_jit.cpp); it
+// therefore includes only headers NVRTC can compile.
+#pragma once
+
+#include "ep_cfg.hpp"
+#include "ep_types.cuh"
+
+namespace epg {
+
+// ---- vector access ---------------------------------------------------------
+
+template <int V>
+__device__ __forceinline__ void load_stream(const void* p, Vec<V>& r) {
+  if constexpr (V == 8) {
+    asm volatile("ld.global.nc.L1::no_allocate.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(r.w[0]), "=r"(r.w[1]), "=r"(r.w[2]), "=r"(r.w[3]), "=r"(r.w[4]),
+                   "=r"(r.w[5]), "=r"(r.w[6]), "=r"(r.w[7])
+                 : "l"(p));
+  } else {
+    asm volatile("ld.global.nc.L1::no_allocate.v4.b32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.w[0]), "=r"(r.w[1]), "=r"(r.w[2]), "=r"(r.w[3])
+                 : "l"(p));
+  }
+}
+
+template <int V>
+__device__ __forceinline__ void store(void* p, const Vec<V>& r) {
+  if constexpr (V == 8) {
+    asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(r.w[0]),
+                 "r"(r.w[1]), "r"(r.w[2]), "r"(r.w[3]), "r"(r.w[4]), "r"(r.w[5]), "r"(r.w[6]),
+                 "r"(r.w[7])
+                 : "memory");
+  } else {
+    asm volatile("st.global.v4.b32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(r.w[0]), "r"(r.w[1]),
+                 "r"(r.w[2]), "r"(r.w[3])
+                 : "memory");
+  }
+}
+
+// ---- geometry ----------------------------------------------------------------
+
+// Threads per CTA of the copy kernel (RB row bytes, V words per vector) and of
+// the FP8 kernel (HC channels); 0 row bytes / channels: the runtime-shape
+// variant, kRowMaxThreads threads walking the row in a loop.
+constexpr int CopyThreads(int rb, int v) {
+  return rb ? (RowThreads(rb / (4 * v)) ? RowThreads(rb / (4 * v)) : kRowMaxThreads) : kRowMaxThreads;
+}
+constexpr int Fp8Threads(int hc, int v) {
+  return hc ? (RowThreads(2 * hc / (4 * v)) ? RowThreads(2 * hc / (4 * v)) : kRowMaxThreads)
+            : kRowMaxThreads;
+}
+
+// Forward the routing with the rows (the dispatch copy epilogue's
+// recv_topk_weights / recv_topk_idx): row dst_slot[t][k] gets topk_weights[t][k]
+// and the expert id of (t, k).
+__device__ __forceinline__ void forward_routing(const DispatchParams& p, int t, int K,
+                                                const int32_t* sl) {
+  if (p.recv_topk_weights == nullptr && p.recv_topk_idx == nullptr) return;
+  for (int k = threadIdx.x; k < K; k += blockDim.x) {
+    const int32_t d = sl[k];
+    if (d < 0) continue;
+    const int64_t i = static_cast<int64_t>(t) * K + k;
+    if (p.recv_topk_weights) p.recv_topk_weights[d] = p.topk_weights[i];
+    if (p.recv_topk_idx) p.recv_topk_idx[d] = p.topk_i32[i];
+  }
+}
+
+// ---- copy (bf16, fp32 and packed-fp4 transports) ------------------------------
+
+template <int RB, int KC, int V>
+__device__ __forceinline__ void dispatch_copy_body(const DispatchParams& p) {
+  constexpr int UNIT = 4 * V;  // bytes per vector
+  constexpr int KM = KC ? KC : kMaxTopk;
+  const int K = KC ? KC : p.topk;
+  const int row = RB ? RB : p.row_bytes;
+  const int t = blockIdx.x;
+  const uint8_t* xr = static_cast<const uint8_t*>(p.x) + static_cast<int64_t>(t) * row;
+  uint8_t* rx = static_cast<uint8_t*>(p.recv_x);
+  const int32_t* sl = p.dst_slot + static_cast<int64_t>(t) * K;
+
+  constexpr int CH = RB ? RB / UNIT : 0;
+  constexpr int T = RB ? RowThreads(CH) : 0;
+  if constexpr (T != 0) {
+    constexpr int PER = CH / T;
+    Vec<V> v[PER];
+#pragma unroll
+    for (int u = 0; u < PER; ++u)
+      load_stream<V>(xr + static_cast<int64_t>(threadIdx.x + u * T) * UNIT, v[u]);
+#pragma unroll
+    for (int k = 0; k < KM; ++k) {
+      if (k >= K) break;
+      const int32_t d = __ldg(sl + k);
+      if (d < 0) continue;
+      uint8_t* dr = rx + static_cast<int64_t>(d) * row;
+#pragma unroll
+      for (int u = 0; u < PER; ++u) store<V>(dr + static_cast<int64_t>(threadIdx.x + u * T) * UNIT, v[u]);
+    }
+  } else {
+    const int chunks = row / UNIT;
+    const int nt = blockDim.x;
+    int32_t d[KM];
+#pragma unroll
+    for (int k = 0; k < KM; ++k) d[k] = k < K ? __ldg(sl + k) : -1;
+    for (int c0 = threadIdx.x; c0 < chunks; c0 += 2 * nt) {
+      const int c1 = c0 + nt;
+      Vec<V> a, b;
+      load_stream<V>(xr + static_cast<int64_t>(c0) * UNIT, a);
+      if (c1 < chunks) load_stream<V>(xr + static_cast<int64_t>(c1) * UNIT, b);
+#pragma unroll
+      for (int k = 0; k < KM; ++k) {
+        if (d[k] < 0) continue;
+        uint8_t* dr = rx + static_cast<int64_t>(d[k]) * row;
+        store<V>(dr + static_cast<int64_t>(c0) * UNIT, a);
+        if (c1 < chunks) store<V>(dr + static_cast<int64_t>(c1) * UNIT, b);
+      }
+    }
+  }
+  forward_routing(p, t, K, sl);
+}
+
+// ---- FP8 --------------------------------------------------------------------
+
+// Two fp32 values to packed e4m3 (round to nearest even, saturate to +-448);
+// `lo` lands in the low byte.
+__device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Quantise the 2V bf16 values of one vector with the scale of its 128-channel
+// group; `lanes` consecutive lanes (a power of two) hold the group.  Every lane
+// of the warp must call this (the reduction is a full-warp shuffle).
+template <int V>
+__device__ __forceinline__ void quantise(const Vec<V>& in, int lanes, uint32_t (&q)[V / 2],
+                                         float& scale) {
+  float f[2 * V];
+#pragma unroll
+  for (int i = 0; i < V; ++i) {
+    f[2 * i] = __uint_as_float(in.w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(in.w[i] & 0xffff0000u);
+  }
+  uint32_t a = 0;
+#pragma unroll
+  for (int i = 0; i < 2 * V; ++i) {
+    uint32_t b = __float_as_uint(f[i]) & 0x7fffffffu;
+    b = b > 0x7f800000u ? 0u : b;  // NaN does not take part in the maximum
+    a = b > a ? b : a;
+  }
+  for (int o = 1; o < lanes; o <<= 1) {
+    const uint32_t other = __shfl_xor_sync(0xffffffffu, a, o);
+    a = other > a ? other : a;
+  }
+  scale = 0.0f;
+#pragma unroll
+  for (int i = 0; i < V / 2; ++i) q[i] = 0u;
+  if (a != 0u) {
+    scale = __fdiv_rn(__uint_as_float(a), 448.0f);
+#pragma unroll
+    for (int i = 0; i < V / 2; ++i) {
+      const float r0 = __fdiv_rn(f[4 * i], scale), r1 = __fdiv_rn(f[4 * i + 1], scale);
+      const float r2 = __fdiv_rn(f[4 * i + 2], scale), r3 = __fdiv_rn(f[4 * i + 3], scale);
+      q[i] = cvt_e4m3x2(r0, r1) | (cvt_e4m3x2(r2, r3) << 16);
+    }
+  }
+}
+
+template <int V>
+__device__ __forceinline__ void store_q(void* p, const uint32_t (&q)[V / 2]) {
+  if constexpr (V == 8) {
+    asm volatile("st.global.v4.b32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(q[0]), "r"(q[1]), "r"(q[2]),
+                 "r"(q[3])
+                 : "memory");
+  } else {
+    asm volatile("st.global.v2.b32 [%0], {%1,%2};" ::"l"(p), "r"(q[0]), "r"(q[1]) : "memory");
+  }
+}
+
+template <int HC, int KC, int V>
+__device__ __forceinline__ void dispatch_fp8_body(const DispatchParams& p) {
+  constexpr int UNIT = 4 * V;            // input bytes per vector (2V channels)
+  constexpr int LANES = 128 / (2 * V);   // lanes per 128-channel group
+  constexpr int KM = KC ? KC : kMaxTopk;
+  const int H = HC ? HC : p.hidden;
+  const int K = KC ? KC : p.topk;
+  const int G = H / kScaleGroup;
+  const int t = blockIdx.x;
+  const uint8_t* xr = static_cast<const uint8_t*>(p.x) + static_cast<int64_t>(t) * 2 * H;
+  uint8_t* rq = static_cast<uint8_t*>(p.recv_x);
+  float* rs = p.recv_scales;
+  const int32_t* sl = p.dst_slot + static_cast<int64_t>(t) * K;
+  const bool leader = (threadIdx.x % LANES) == 0;
+
+  constexpr int CH = HC ? 2 * HC / UNIT : 0;
+  constexpr int T = HC ? RowThreads(CH) : 0;
+  if constexpr (T != 0) {
+    constexpr int PER = CH / T;
+    Vec<V> v[PER];
+#pragma unroll
+    for (int u = 0; u < PER; ++u)
+      load_stream<V>(xr + static_cast<int64_t>(threadIdx.x + u * T) * UNIT, v[u]);
+    uint32_t q[PER][V / 2];
+    float s[PER];
+#pragma unroll
+    for (int u = 0; u < PER; ++u) quantise<V>(v[u], LANES, q[u], s[u]);
+#pragma unroll
+    for (int k = 0; k < KM; ++k) {
+      if (k >= K) break;
+      const int32_t d = __ldg(sl + k);
+      if (d < 0) continue;
+#pragma unroll
+      for (int u = 0; u < PER; ++u) {
+        const int c = threadIdx.x + u * T;
+        store_q<V>(rq + static_cast<int64_t>(d) * H + static_cast<int64_t>(c) * (2 * V), q[u]);
+        if (leader) rs[static_cast<int64_t>(d) * G + c / LANES] = s[u];
+      }
+    }
+  } else {
+    const int chunks = 2 * H / UNIT;
+    int32_t d[KM];
+#pragma unroll
+    for (int k = 0; k < KM; ++k) d[k] = k < K ? __ldg(sl + k) : -1;
+    // uniform trip count (blockDim is a multiple of 32): the shuffles see every lane
+    for (int c0 = 0; c0 < chunks; c0 += blockDim.x) {
+      const int c = c0 + threadIdx.x;
+      const bool in = c < chunks;
+      Vec<V> v;
+#pragma unroll
+      for (int i = 0; i < V; ++i) v.w[i] = 0u;
+      if (in) load_stream<V>(xr + static_cast<int64_t>(c) * UNIT, v);
+      uint32_t q[V / 2];
+      float s;
+      quantise<V>(v, LANES, q, s);
+      if (!in) continue;
+#pragma unroll
+      for (int k = 0; k < KM; ++k) {
+        if (d[k] < 0) continue;
+        store_q<V>(rq + static_cast<int64_t>(d[k]) * H + static_cast<int64_t>(c) * (2 * V), q);
+        if (leader) rs[static_cast<int64_t>(d[k]) * G + c / LANES] = s;
+      }
+    }
+  }
+  forward_routing(p, t, K, sl);
+}
+
+}  // namespace epg

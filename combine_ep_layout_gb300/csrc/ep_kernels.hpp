@@ -11,12 +11,10 @@
 #include <cstdint>
 
 #include "ep_cfg.hpp"
+#include "ep_types.cuh"
 
 namespace epg {
 
-// Device error bits (sticky, read and cleared by ep_handle_status).
-constexpr int32_t kErrBadExpert = 1;   // a topk id outside [-1, E) was skipped
-constexpr int32_t kErrTimeout = 2;     // a bounded wait on a kernel's own copy ran out
 
 struct LayoutParams {
   const int64_t* topk_idx;   // [N, K]
@@ -44,35 +42,6 @@ struct LayoutParams {
   int32_t* chunk_hist;
   int32_t* chunk_off;        // exclusive prefix over chunks, [E+W][C]
   int32_t* col_total;        // [E+W]
-};
-
-struct DispatchParams {
-  const void* x;             // [N, row_bytes] (bf16 for FP8 dispatch)
-  void* recv_x;              // [Rcap, row_bytes] (e4m3 [Rcap, H] for FP8)
-  float* recv_scales;        // fp32 [Rcap, H/128] (FP8 only)
-  const int32_t* dst_slot;   // [N, K]
-  int num_tokens;
-  int hidden;
-  int topk;
-  int row_bytes;             // bytes of one transported row (copy transports)
-  int32_t* err;
-  // routing forwarded with the rows (both nullptr: not forwarded)
-  const float* topk_weights;   // fp32 [N, K]
-  const int32_t* topk_i32;     // int32 [N, K] expert ids (the handle's clone)
-  float* recv_topk_weights;    // fp32 [Rcap] or nullptr
-  int32_t* recv_topk_idx;      // int32 [Rcap] or nullptr
-};
-
-struct CombineParams {
-  const void* y;             // bf16 [Rcap, H]
-  const float* weights;      // fp32 [N, K] or nullptr
-  const void* bias;          // bf16 [N, H] or nullptr
-  void* out;                 // bf16 or fp32 [N, H]
-  const int32_t* dst_slot;   // [N, K]
-  int num_tokens;
-  int hidden;
-  int topk;
-  int out_f32;               // 1: fp32 output, 0: bf16
 };
 
 // Launch geometry of a variant on the current device, filled by its prepare

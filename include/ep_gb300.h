@@ -239,6 +239,25 @@ int ep_handle_status(ep_handle_t h, int32_t *device_error) EP_NOEXCEPT;
  * "..._generic" when no specialisation for the shape was compiled. */
 int ep_handle_variant(ep_handle_t h, int32_t step, char *buf, int32_t len) EP_NOEXCEPT;
 
+/* Run-time specialisation ("MORI JIT v2" §1-§3.4, §6 precompile; the JIT
+ * flow of "DeepEP overall architecture analysis").  A configuration whose
+ * (hidden, top-k) has no compiled variant gets one at ep_handle_create: the
+ * kernel bodies are rendered into source text for that shape, compiled with
+ * NVRTC for the device, and kept in an on-disk cache keyed by SHA-256 of the
+ * entry name, compiler version, flags, kernel-body headers and source text
+ * (directory $EP_GB300_JIT_CACHE, default ~/.cache/ep_gb300/jit; entries
+ * published by an atomic rename, so concurrent processes agree).  Such a
+ * kernel serves 32-byte-aligned buffers (combine: without bias, bf16 output);
+ * the compiled generic variant serves the rest, and everything when NVRTC is
+ * missing or EP_GB300_JIT=0.  ep_handle_variant reports which ran.
+ * ep_jit_precompile fills the cache for cfg without a GPU, for architecture
+ * `arch` (NULL or "" = "sm_103a"), and writes one line per step to report
+ * ("<name> compiled-in|generic|compiled <dir>|cached <dir>").  Returns the
+ * number of kernels it compiled (0 when all were cached or compiled in), or
+ * EP_EINVAL, EP_EUNSUPPORTED (no NVRTC), EP_ECUDA (compile or file error, with
+ * the compiler log in ep_last_error()). */
+int ep_jit_precompile(const ep_cfg_t *cfg, const char *arch, char *report, int32_t len) EP_NOEXCEPT;
+
 /* Message of the last failed call on this thread ("" if none). */
 const char *ep_last_error(void) EP_NOEXCEPT;
 

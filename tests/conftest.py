@@ -10,6 +10,10 @@ if ROOT not in sys.path:
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (GB300, sm_103a)")
+    # run-time specialisations compiled by the tests go to a private cache
+    if "EP_GB300_JIT_CACHE" not in os.environ:
+        import tempfile
+        os.environ["EP_GB300_JIT_CACHE"] = tempfile.mkdtemp(prefix="ep_gb300_jit_")
 
 
 def pytest_collection_modifyitems(config, items):

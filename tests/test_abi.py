@@ -23,7 +23,7 @@ def built():
 
 def test_exports_every_declared_symbol():
     names = ep.declared_symbols()
-    assert len(names) == 13
+    assert len(names) == 14
     L = ep.load_library()
     for n in names:
         assert hasattr(L, n), n
