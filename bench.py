@@ -36,10 +36,13 @@ WORKLOAD = "prefill"
 WORKLOAD_DESC = ("prefill: 8 logical ranks x 4096 tokens = 32768 tokens, hidden 7168 bf16 ~N(0,1), "
                  "256 experts (32/rank), top-8 uniform distinct, softmax weights, expert_alignment "
                  "128; dispatch bf16 and FP8 e4m3 (per-128 fp32 scales); combine bf16 with fp32 fma")
-SHARED_SOURCES = ["ep_ptx.cuh", "ep_cfg.hpp", "ep_kernels.hpp"]
-KERNEL_FILES = {"ep_dispatch_copy_kernel": "ep_dispatch.cu", "ep_dispatch_fp8_kernel": "ep_dispatch.cu",
-                "ep_combine_kernel": "ep_combine.cu", "ep_layout_count_kernel": "ep_layout.cu",
-                "ep_layout_spine_kernel": "ep_layout.cu", "ep_layout_slots_kernel": "ep_layout.cu"}
+SHARED_SOURCES = ["ep_ptx.cuh", "ep_cfg.hpp", "ep_kernels.hpp", "ep_types.cuh"]
+KERNEL_FILES = {"ep_dispatch_copy_kernel": ["ep_dispatch_body.cuh", "ep_dispatch.cu"],
+                "ep_dispatch_fp8_kernel": ["ep_dispatch_body.cuh", "ep_dispatch.cu"],
+                "ep_combine_kernel": ["ep_combine_body.cuh", "ep_combine.cu"],
+                "ep_layout_count_kernel": ["ep_layout.cu"],
+                "ep_layout_spine_kernel": ["ep_layout.cu"],
+                "ep_layout_slots_kernel": ["ep_layout.cu"]}
 
 
 # ----------------------------------------------------------------- helpers
@@ -87,7 +90,7 @@ def measured_peaks():
 def kernel_source_digest(kernel):
     """Digest of the source file that holds `kernel` and the headers it includes."""
     h = hashlib.sha256()
-    for n in [KERNEL_FILES[kernel]] + SHARED_SOURCES:
+    for n in KERNEL_FILES[kernel] + SHARED_SOURCES:
         with open(os.path.join(ROOT, "combine_ep_layout_gb300", "csrc", n), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
