@@ -64,6 +64,15 @@ def lib():
     L.oracle_combine_ex.restype = None
     L.oracle_combine_ex.argtypes = [c.c_int, c.c_int, c.c_int, _u16p, _i32p, c.c_void_p,
                                     c.c_void_p, c.c_void_p, c.c_void_p]
+    L.oracle_recv_capacity_nonexpand.restype = c.c_int64
+    L.oracle_recv_capacity_nonexpand.argtypes = [c.c_int, c.c_int, c.c_int]
+    L.oracle_layout_nonexpand.restype = c.c_int
+    L.oracle_layout_nonexpand.argtypes = [c.c_int, c.c_int, c.c_int, c.c_int, c.c_int,
+                                          _i64p, c.c_int, _i32p, _i32p, _i32p, _i32p,
+                                          _i32p, _i32p, _i32p, c.c_int64, _i32p, _i32p]
+    L.oracle_forward_routing_nonexpand.restype = None
+    L.oracle_forward_routing_nonexpand.argtypes = [c.c_int, c.c_int, _i64p, c.c_void_p, _i32p,
+                                                   _i32p, c.c_void_p, c.c_void_p]
     _lib = L
     return L
 
@@ -220,3 +229,54 @@ def combine_ex(y_bits, dst_slot, weights=None, bias_bits=None, out_dtype="bf16")
         lib().oracle_combine_ex(N, H, K, np.ascontiguousarray(y_bits), dst_slot, _vp(w), _vp(b),
                                 _vp(out), None)
     return out
+
+
+def recv_capacity_nonexpand(max_tokens, topk, world_size):
+    """Rows a non-expand receive buffer needs: one per (token, rank), min(K, W) per token."""
+    return int(lib().oracle_recv_capacity_nonexpand(max_tokens, topk, world_size))
+
+
+def layout_nonexpand(topk_idx, world_size, max_tok_per_rank, num_expert_per_rank,
+                     alignment, rcap=None):
+    """Non-expand layout (one receive row per (token, destination rank)).  Same
+    keys as layout(), plus send_slot [N, K] (the token's distinct rows,
+    ascending, then -1); psum_rank / num_recv / meta describe the rank rows."""
+    topk_idx = np.ascontiguousarray(topk_idx, dtype=np.int64)
+    N, K = topk_idx.shape
+    W, T, Epr, A = world_size, max_tok_per_rank, num_expert_per_rank, alignment
+    E = W * Epr
+    if rcap is None:
+        rcap = recv_capacity_nonexpand(W * T, K, W)
+    out = dict(
+        cnt=np.zeros(E, np.int32), tok_per_rank=np.zeros(W, np.int32),
+        psum_expert=np.zeros(E + 1, np.int32), psum_rank=np.zeros(W + 1, np.int32),
+        dst_slot=np.zeros((N, K), np.int32), send_slot=np.zeros((N, K), np.int32),
+        meta=np.zeros((rcap, K + 2), np.int32),
+    )
+    num_recv = np.zeros(1, np.int32)
+    err = np.zeros(1, np.int32)
+    rc = lib().oracle_layout_nonexpand(W, T, Epr, K, A, topk_idx.reshape(-1), N,
+                                       out["cnt"], out["tok_per_rank"], out["psum_expert"],
+                                       out["psum_rank"], out["dst_slot"].reshape(-1),
+                                       out["send_slot"].reshape(-1), out["meta"].reshape(-1),
+                                       rcap, num_recv, err)
+    if rc != 0:
+        raise ValueError("oracle non-expand layout: receive capacity exceeded")
+    out["num_recv"] = int(num_recv[0])
+    out["err"] = int(err[0])
+    out["rcap"] = int(rcap)
+    return out
+
+
+def forward_routing_nonexpand(topk_idx, weights, dst_slot, send_slot, recv_w=None, recv_idx=None):
+    """K-wide routing rows of the non-expand layout, in place: recv_w fp32 [rows, K],
+    recv_idx int32 [rows, K] (either may be None)."""
+    topk_idx = np.ascontiguousarray(topk_idx, np.int64)
+    N, K = topk_idx.shape
+    w = None if weights is None else np.ascontiguousarray(weights, np.float32)
+    for a, dt in ((recv_w, np.float32), (recv_idx, np.int32)):
+        assert a is None or (a.dtype == dt and a.flags.c_contiguous and a.shape[-1] == K)
+    lib().oracle_forward_routing_nonexpand(N, K, topk_idx, _vp(w),
+                                           np.ascontiguousarray(dst_slot, np.int32),
+                                           np.ascontiguousarray(send_slot, np.int32),
+                                           _vp(recv_w), _vp(recv_idx))

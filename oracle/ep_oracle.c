@@ -433,3 +433,148 @@ void oracle_combine_ex(int N, int H, int K, const uint16_t *y, const int32_t *ds
         }
     }
 }
+
+/* ------------------------------------------------------ non-expand layout */
+
+/* Receive rows for the non-expand layout (EPHandle do_expand = false in
+ * "DeepEP overall architecture analysis"): every token is received once by
+ * each rank that owns one of its experts, so at most min(K, W) rows per token.
+ * Reading of the pages, which name the mode only: one row per (token,
+ * destination rank); no expert alignment applies (the rows are not grouped by
+ * expert). */
+int64_t oracle_recv_capacity_nonexpand(int max_tokens, int K, int W)
+{
+    return (int64_t)max_tokens * (K < W ? K : W);
+}
+
+/* Non-expand layout.  Same arguments and outputs as oracle_layout, with these
+ * differences (the expert counts cnt / psum_expert are computed as there: they
+ * are what the receiving ranks' expert computation needs):
+ *   psum_rank[W+1]    exclusive prefix sum of tok_per_rank (no alignment)
+ *   num_recv[1]       R = psum_rank[W], the number of (token, rank) rows
+ *   rows              rank r owns rows [psum_rank[r], psum_rank[r+1]); its
+ *                     tokens appear once each, in ascending token order
+ *   dst_slot[N][K]    the row that carries (t,k): the row of t on the rank of
+ *                     expert topk_idx[t][k]; -1 when skipped.  Entries of one
+ *                     token whose experts share a rank share the row.
+ *   send_slot[N][K]   the distinct rows of t in ascending order (= ascending
+ *                     rank), then -1: the rows dispatch writes and combine reads
+ *   meta[rcap][K+2]   {t / T, t mod T, dst_slot[t][0..K-1]} per row, -1 rows
+ *                     where nothing is received
+ * Returns 0, or -1 when R would exceed rcap. */
+int oracle_layout_nonexpand(int W, int T, int Epr, int K, int A,
+                            const int64_t *topk_idx, int N,
+                            int32_t *cnt, int32_t *tok_per_rank,
+                            int32_t *psum_expert, int32_t *psum_rank,
+                            int32_t *dst_slot, int32_t *send_slot, int32_t *meta, int64_t rcap,
+                            int32_t *num_recv, int32_t *err)
+{
+    const int E = W * Epr;
+    *err = 0;
+    for (int e = 0; e < E; ++e)
+        cnt[e] = 0;
+    for (int r = 0; r < W; ++r)
+        tok_per_rank[r] = 0;
+
+    /* per token: which ranks it touches; per expert: how many entries */
+    char *touched = (char *)calloc((size_t)N * (size_t)(W > 0 ? W : 1) + 1, 1);
+    for (int t = 0; t < N; ++t) {
+        for (int k = 0; k < K; ++k) {
+            int64_t e = topk_idx[(int64_t)t * K + k];
+            if (e == -1)
+                continue;
+            if (e < -1 || e >= E) {
+                *err |= 1;
+                continue;
+            }
+            cnt[e] += 1;
+            touched[(size_t)t * W + (size_t)(e / Epr)] = 1;
+        }
+        for (int r = 0; r < W; ++r)
+            tok_per_rank[r] += touched[(size_t)t * W + r];
+    }
+
+    psum_expert[0] = 0;
+    for (int e = 0; e < E; ++e) {
+        int32_t padded = ((cnt[e] + A - 1) / A) * A;
+        psum_expert[e + 1] = psum_expert[e] + padded;
+    }
+    psum_rank[0] = 0;
+    for (int r = 0; r < W; ++r)
+        psum_rank[r + 1] = psum_rank[r] + tok_per_rank[r];
+    *num_recv = psum_rank[W];
+    if ((int64_t)psum_rank[W] > rcap) {
+        free(touched);
+        return -1;
+    }
+
+    /* rows: a running cursor per rank, walking the tokens in order and, for
+     * each token, its ranks in ascending order */
+    int32_t *cursor = (int32_t *)malloc(sizeof(int32_t) * (size_t)(W > 0 ? W : 1));
+    int32_t *row_of = (int32_t *)malloc(sizeof(int32_t) * (size_t)(W > 0 ? W : 1));
+    for (int r = 0; r < W; ++r)
+        cursor[r] = psum_rank[r];
+    for (int t = 0; t < N; ++t) {
+        int j = 0;
+        for (int r = 0; r < W; ++r) {
+            row_of[r] = -1;
+            if (touched[(size_t)t * W + r]) {
+                row_of[r] = cursor[r];
+                cursor[r] += 1;
+                send_slot[(int64_t)t * K + j] = row_of[r];
+                j += 1;
+            }
+        }
+        for (; j < K; ++j)
+            send_slot[(int64_t)t * K + j] = -1;
+        for (int k = 0; k < K; ++k) {
+            int64_t e = topk_idx[(int64_t)t * K + k];
+            dst_slot[(int64_t)t * K + k] = (e < 0 || e >= E) ? -1 : row_of[e / Epr];
+        }
+    }
+    free(row_of);
+    free(cursor);
+    free(touched);
+
+    for (int64_t i = 0; i < rcap * (K + 2); ++i)
+        meta[i] = -1;
+    for (int t = 0; t < N; ++t) {
+        for (int j = 0; j < K; ++j) {
+            int32_t s = send_slot[(int64_t)t * K + j];
+            if (s < 0)
+                break;
+            int32_t *row = meta + (int64_t)s * (K + 2);
+            row[0] = t / T;
+            row[1] = t % T;
+            for (int k = 0; k < K; ++k)
+                row[2 + k] = dst_slot[(int64_t)t * K + k];
+        }
+    }
+    return 0;
+}
+
+/* Routing forwarded with the non-expand rows (the copy epilogue's
+ * recv_topk_idx / recv_topk_weights, one K-wide row per received row): for each
+ * row s of token t and each k,
+ *   recv_idx[s][k] = topk_idx[t][k] and recv_w[s][k] = w[t][k]  when (t,k) is carried by s,
+ *   recv_idx[s][k] = -1             and recv_w[s][k] = 0.0f     otherwise.
+ * Rows that receive nothing are untouched; either output may be NULL. */
+void oracle_forward_routing_nonexpand(int N, int K, const int64_t *topk_idx, const float *w,
+                                      const int32_t *dst_slot, const int32_t *send_slot,
+                                      float *recv_w, int32_t *recv_idx)
+{
+    for (int t = 0; t < N; ++t)
+        for (int j = 0; j < K; ++j) {
+            int32_t s = send_slot[(int64_t)t * K + j];
+            if (s < 0)
+                break;
+            for (int k = 0; k < K; ++k) {
+                int64_t i = (int64_t)t * K + k;
+                int mine = dst_slot[i] == s;
+                if (recv_w)
+                    recv_w[(int64_t)s * K + k] = mine ? w[i] : 0.0f;
+                if (recv_idx)
+                    recv_idx[(int64_t)s * K + k] = mine ? (int32_t)topk_idx[i] : -1;
+            }
+        }
+}
