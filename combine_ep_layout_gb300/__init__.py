@@ -6,7 +6,7 @@ from ._native import (  # noqa: F401
     EP_OK, EP_EINVAL, EP_EUNSUPPORTED, EP_ECUDA, EP_ENOMEM,
     FIELD_NUM_UNALIGNED_PER_EXPERT, FIELD_NUM_TOKENS_PER_RANK, FIELD_PSUM_PER_EXPERT,
     FIELD_PSUM_PER_RANK, FIELD_DST_SLOT, FIELD_RECV_SRC_METADATA, FIELD_NUM_RECV,
-    FIELD_DEVICE_ERROR, FIELD_TOPK_IDX, ERR_BAD_EXPERT, ERR_TIMEOUT,
+    FIELD_DEVICE_ERROR, FIELD_TOPK_IDX, FIELD_SEND_SLOT, ERR_BAD_EXPERT, ERR_TIMEOUT,
     EpError, EpHandle, ep_cfg_t, make_cfg, load_library, declared_symbols,
     ep_recv_capacity, ep_handle_create, ep_layout, ep_dispatch, ep_combine, ep_handle_free,
     ep_handle_get, ep_handle_status, ep_handle_variant, ep_last_error,

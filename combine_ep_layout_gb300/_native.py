@@ -20,7 +20,7 @@ EP_BF16, EP_FP32, EP_FP8_E4M3, EP_FP4X2 = 0, 1, 2, 3
 EP_OK, EP_EINVAL, EP_EUNSUPPORTED, EP_ECUDA, EP_ENOMEM = 0, -1, -2, -3, -4
 (FIELD_NUM_UNALIGNED_PER_EXPERT, FIELD_NUM_TOKENS_PER_RANK, FIELD_PSUM_PER_EXPERT,
  FIELD_PSUM_PER_RANK, FIELD_DST_SLOT, FIELD_RECV_SRC_METADATA, FIELD_NUM_RECV,
- FIELD_DEVICE_ERROR, FIELD_TOPK_IDX) = range(9)
+ FIELD_DEVICE_ERROR, FIELD_TOPK_IDX, FIELD_SEND_SLOT) = range(10)
 ERR_BAD_EXPERT, ERR_TIMEOUT = 1, 2
 
 _DTYPES = {"bf16": EP_BF16, "fp32": EP_FP32, "fp8": EP_FP8_E4M3, "fp8_e4m3": EP_FP8_E4M3,
@@ -31,7 +31,8 @@ class ep_cfg_t(ctypes.Structure):
     _fields_ = [("world_size", ctypes.c_int32), ("hidden_dim", ctypes.c_int32),
                 ("max_tok_per_rank", ctypes.c_int32), ("num_expert_per_rank", ctypes.c_int32),
                 ("num_expert_per_token", ctypes.c_int32), ("expert_alignment", ctypes.c_int32),
-                ("dispatch_dtype", ctypes.c_int32), ("use_weights", ctypes.c_int32)]
+                ("dispatch_dtype", ctypes.c_int32), ("use_weights", ctypes.c_int32),
+                ("no_expand", ctypes.c_int32)]
 
 
 class EpError(RuntimeError):
@@ -103,10 +104,11 @@ def _check(rc):
 
 
 def make_cfg(world_size, hidden_dim, max_tok_per_rank, num_expert_per_rank, num_expert_per_token,
-             expert_alignment=1, dispatch_dtype="bf16", use_weights=True):
+             expert_alignment=1, dispatch_dtype="bf16", use_weights=True, no_expand=False):
     dt = _DTYPES[dispatch_dtype] if isinstance(dispatch_dtype, str) else int(dispatch_dtype)
     return ep_cfg_t(world_size, hidden_dim, max_tok_per_rank, num_expert_per_rank,
-                    num_expert_per_token, expert_alignment, dt, int(bool(use_weights)))
+                    num_expert_per_token, expert_alignment, dt, int(bool(use_weights)),
+                    int(bool(no_expand)))
 
 
 def ep_recv_capacity(cfg):
@@ -197,7 +199,7 @@ class EpHandle:
         _check(load_library().ep_handle_get(self.ptr, field, ctypes.byref(p), ctypes.byref(n)))
         K = self.cfg.num_expert_per_token
         shape = (n.value,)
-        if field == FIELD_DST_SLOT:
+        if field in (FIELD_DST_SLOT, FIELD_SEND_SLOT):
             shape = (n.value // K, K)
         elif field == FIELD_TOPK_IDX:
             shape = (n.value // K, K)

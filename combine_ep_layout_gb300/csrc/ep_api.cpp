@@ -57,6 +57,10 @@ int validate(const ep_cfg_t* c) {
   if (c->hidden_dim < 8 || c->hidden_dim > kMaxHidden || c->hidden_dim % 8 != 0)
     return fail(EP_EINVAL, "hidden_dim must be a multiple of 8 in [8, 32768] (16-byte rows)");
   if (c->use_weights != 0 && c->use_weights != 1) return fail(EP_EINVAL, "use_weights must be 0 or 1");
+  if (c->no_expand != 0 && c->no_expand != 1) return fail(EP_EINVAL, "no_expand must be 0 or 1");
+  if (c->no_expand && c->use_weights)
+    return fail(EP_EINVAL,
+                "the non-expand layout combines rank rows unweighted: use_weights must be 0 with no_expand");
   switch (c->dispatch_dtype) {
     case EP_BF16: break;
     case EP_FP8_E4M3:
@@ -76,6 +80,15 @@ int validate(const ep_cfg_t* c) {
   return EP_OK;
 }
 
+// Receive rows of a valid configuration: per (token, expert) plus padding for
+// the expand layout, per (token, rank) for the non-expand layout.
+int64_t recv_rows(const ep_cfg_t* c) {
+  const int64_t max_tokens = static_cast<int64_t>(c->world_size) * c->max_tok_per_rank;
+  if (c->no_expand) return RecvCapacityNonExpand(max_tokens, c->num_expert_per_token, c->world_size);
+  return RecvCapacity(max_tokens, c->num_expert_per_token, c->world_size * c->num_expert_per_rank,
+                      c->expert_alignment);
+}
+
 }  // namespace
 
 int epg::RecordError(int code, const char* msg) { return fail(code, msg ? msg : ""); }
@@ -89,9 +102,13 @@ struct ep_handle {
   int num_tokens = 0;
   cudaStream_t last_stream = nullptr;
   void* block = nullptr;
+  bool no_expand = false;
   int32_t *cnt = nullptr, *tok_per_rank = nullptr, *psum_expert = nullptr, *psum_rank = nullptr,
           *num_recv = nullptr, *err = nullptr, *dst_slot = nullptr, *meta = nullptr,
           *topk_i32 = nullptr, *scratch = nullptr;
+  // rows each token is written to / read from: dst_slot for the expand layout,
+  // the token's distinct rank rows for the non-expand one
+  int32_t* send_slot = nullptr;
   Variant<LayoutLaunch> layout{};
   Variant<DispatchLaunch> dispatch{};
   Variant<CombineLaunch> combine{};
@@ -140,9 +157,7 @@ int64_t ep_recv_capacity(const ep_cfg_t* cfg) noexcept {
   try {
     int rc = validate(cfg);
     if (rc != EP_OK && rc != EP_EUNSUPPORTED) return rc;
-    return RecvCapacity(static_cast<int64_t>(cfg->world_size) * cfg->max_tok_per_rank,
-                        cfg->num_expert_per_token, cfg->world_size * cfg->num_expert_per_rank,
-                        cfg->expert_alignment);
+    return recv_rows(cfg);
   } catch (const std::exception& ex) {
     return fail(EP_EINVAL, ex.what());
   } catch (...) {
@@ -166,7 +181,8 @@ int ep_handle_create(const ep_cfg_t* cfg, ep_handle_t* out) noexcept {
     h->H = cfg->hidden_dim;
     h->A = cfg->expert_alignment;
     h->max_tokens = static_cast<int64_t>(h->W) * h->T;
-    h->rcap = RecvCapacity(h->max_tokens, h->K, h->E, h->A);
+    h->no_expand = cfg->no_expand != 0;
+    h->rcap = recv_rows(cfg);
     h->max_chunks = NumLayoutChunks(static_cast<int>(h->max_tokens));
 
     auto bail = [&](int code) {
@@ -180,7 +196,7 @@ int ep_handle_create(const ep_cfg_t* cfg, ep_handle_t* out) noexcept {
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, h->device);
     if (e != cudaSuccess) return bail(fail_cuda(e, "cudaDeviceGetAttribute"));
 
-    h->layout = FindLayout(h->K);
+    h->layout = FindLayout(h->K, h->no_expand);
     h->dispatch = FindDispatch(h->H, h->K, static_cast<EpDType>(cfg->dispatch_dtype));
     h->combine = FindCombine(h->H, h->K, cfg->use_weights != 0);
     if (!h->dispatch.launch) return bail(fail(EP_EUNSUPPORTED, "no dispatch kernel for this dtype"));
@@ -209,7 +225,8 @@ int ep_handle_create(const ep_cfg_t* cfg, ep_handle_t* out) noexcept {
     const size_t n_slot = al(4 * static_cast<size_t>(h->max_tokens) * h->K);  // dst_slot, and the id clone
     const size_t n_meta = al(4 * static_cast<size_t>(h->rcap) * (h->K + 2));
     const size_t n_scr = al(sizeof(int32_t) * static_cast<size_t>(LayoutScratchInts(h->max_chunks, cols)));
-    const size_t total = n_small + 2 * n_slot + n_meta + n_scr;
+    const size_t n_send = h->no_expand ? n_slot : 0;
+    const size_t total = n_small + 2 * n_slot + n_meta + n_scr + n_send;
     e = cudaMalloc(&h->block, total);
     if (e != cudaSuccess) {
       cudaGetLastError();
@@ -228,6 +245,8 @@ int ep_handle_create(const ep_cfg_t* cfg, ep_handle_t* out) noexcept {
     h->topk_i32 = reinterpret_cast<int32_t*>(b + n_small + n_slot);
     h->meta = reinterpret_cast<int32_t*>(b + n_small + 2 * n_slot);
     h->scratch = reinterpret_cast<int32_t*>(b + n_small + 2 * n_slot + n_meta);
+    h->send_slot = h->no_expand ? reinterpret_cast<int32_t*>(b + n_small + 2 * n_slot + n_meta + n_scr)
+                                : h->dst_slot;
     if ((e = cudaMemset(h->block, 0, total)) != cudaSuccess)
       return bail(fail_cuda(e, "cudaMemset"));
     if ((e = cudaDeviceSynchronize()) != cudaSuccess) return bail(fail_cuda(e, "cudaDeviceSynchronize"));
@@ -260,6 +279,7 @@ int ep_layout(ep_handle_t h, const int64_t* topk_idx, int32_t num_tokens, ep_str
     p.num_experts = h->E;
     p.alignment = h->A;
     p.rcap = h->rcap;
+    p.no_expand = h->no_expand ? 1 : 0;
     p.num_chunks = NumLayoutChunks(num_tokens);
     p.cnt = h->cnt;
     p.tok_per_rank = h->tok_per_rank;
@@ -267,6 +287,7 @@ int ep_layout(ep_handle_t h, const int64_t* topk_idx, int32_t num_tokens, ep_str
     p.psum_rank = h->psum_rank;
     p.num_recv = h->num_recv;
     p.dst_slot = h->dst_slot;
+    p.send_slot = h->send_slot;
     p.meta = h->meta;
     p.err = h->err;
     p.topk_i32 = h->topk_i32;
@@ -315,7 +336,8 @@ int ep_dispatch_fwd(ep_handle_t h, const void* x, void* recv_x, float* recv_scal
     p.x = x;
     p.recv_x = recv_x;
     p.recv_scales = recv_scales;
-    p.dst_slot = h->dst_slot;
+    p.dst_slot = h->send_slot;
+    p.entry_slot = h->no_expand ? h->dst_slot : nullptr;
     p.num_tokens = h->num_tokens;
     p.hidden = h->H;
     p.topk = h->K;
@@ -366,7 +388,7 @@ int ep_combine_ex(ep_handle_t h, const void* y, const float* topk_weights, const
     p.weights = weighted ? topk_weights : nullptr;
     p.bias = bias;
     p.out = out;
-    p.dst_slot = h->dst_slot;
+    p.dst_slot = h->send_slot;
     p.num_tokens = h->num_tokens;
     p.hidden = h->H;
     p.topk = h->K;
@@ -412,6 +434,10 @@ int ep_handle_get(ep_handle_t h, int32_t field, void** dev_ptr, int64_t* numel) 
       case EP_FIELD_DEVICE_ERROR: *dev_ptr = h->err; *numel = 1; break;
       case EP_FIELD_TOPK_IDX:
         *dev_ptr = h->topk_i32;
+        *numel = static_cast<int64_t>(h->num_tokens) * h->K;
+        break;
+      case EP_FIELD_SEND_SLOT:
+        *dev_ptr = h->send_slot;
         *numel = static_cast<int64_t>(h->num_tokens) * h->K;
         break;
       default: return fail(EP_EINVAL, "unknown field");

@@ -77,6 +77,12 @@ constexpr int64_t RecvCapacity(int64_t max_tokens, int topk, int num_experts, in
   return max_tokens * topk + (int64_t)num_experts * (alignment - 1);
 }
 
+// Rows of the non-expand receive buffer (one per (token, destination rank)):
+// a token reaches at most min(K, W) ranks.
+constexpr int64_t RecvCapacityNonExpand(int64_t max_tokens, int topk, int world_size) {
+  return max_tokens * (topk < world_size ? topk : world_size);
+}
+
 // Threads per CTA of the row kernels for a row of `chunks` vectors: the largest
 // multiple of 32 that divides it and is at most 256 (every thread owns the same
 // number of vectors, at most 8); 0 when there is none (the row is walked in a

@@ -54,11 +54,27 @@ constexpr int Fp8Threads(int hc, int v) {
 }
 
 // Forward the routing with the rows (the dispatch copy epilogue's
-// recv_topk_weights / recv_topk_idx): row dst_slot[t][k] gets topk_weights[t][k]
-// and the expert id of (t, k).
+// recv_topk_weights / recv_topk_idx).  Expand layout: row dst_slot[t][k] gets
+// topk_weights[t][k] and the expert id of (t, k).  Non-expand layout: each row
+// s of the token gets K entries, (id, weight) of the entries it carries
+// (entry_slot[t][k] == s) and (-1, 0) for the others.
 __device__ __forceinline__ void forward_routing(const DispatchParams& p, int t, int K,
                                                 const int32_t* sl) {
   if (p.recv_topk_weights == nullptr && p.recv_topk_idx == nullptr) return;
+  if (p.entry_slot != nullptr) {
+    const int32_t* es = p.entry_slot + static_cast<int64_t>(t) * K;
+    for (int i = threadIdx.x; i < K * K; i += blockDim.x) {
+      const int j = i / K, k = i - j * K;
+      const int32_t d = sl[j];
+      if (d < 0) continue;
+      const bool mine = es[k] == d;
+      const int64_t src = static_cast<int64_t>(t) * K + k;
+      const int64_t dst = static_cast<int64_t>(d) * K + k;
+      if (p.recv_topk_weights) p.recv_topk_weights[dst] = mine ? p.topk_weights[src] : 0.0f;
+      if (p.recv_topk_idx) p.recv_topk_idx[dst] = mine ? p.topk_i32[src] : -1;
+    }
+    return;
+  }
   for (int k = threadIdx.x; k < K; k += blockDim.x) {
     const int32_t d = sl[k];
     if (d < 0) continue;

@@ -26,6 +26,7 @@ struct LayoutParams {
   int num_experts;           // E
   int alignment;             // A
   int64_t rcap;              // receive capacity (rows of meta)
+  int no_expand;             // 1: one row per (token, rank) (EPHandle do_expand = false)
   int num_chunks;            // C = ceil(N / kLayoutTPC)
   // outputs (handle)
   int32_t* cnt;              // [E]
@@ -34,6 +35,7 @@ struct LayoutParams {
   int32_t* psum_rank;        // [W+1]
   int32_t* num_recv;         // [1]
   int32_t* dst_slot;         // [N, K]
+  int32_t* send_slot;        // [N, K] non-expand: the token's distinct rows, ascending
   int32_t* meta;             // [rcap, K+2]
   int32_t* err;              // [1]
   int32_t* topk_i32;         // [N, K] clone of the ids (-1 where skipped), or nullptr
@@ -65,7 +67,7 @@ struct Variant {
   PrepareFn prepare;
 };
 
-Variant<LayoutLaunch> FindLayout(int topk);
+Variant<LayoutLaunch> FindLayout(int topk, bool no_expand);
 Variant<DispatchLaunch> FindDispatch(int hidden, int topk, EpDType dtype);
 Variant<CombineLaunch> FindCombine(int hidden, int topk, bool use_weights);
 

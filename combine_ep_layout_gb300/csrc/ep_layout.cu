@@ -30,6 +30,12 @@
 //          chunk are contiguous, so consecutive threads write consecutive words.
 //          Every CTA also writes -1 into its share of the rows that receive
 //          nothing (expert padding and [R, capacity)).
+//
+// Non-expand layout (EPHandle do_expand = false): one row per (token,
+// destination rank).  count and spine are shared (the rank columns of the
+// table already count each chunk's tokens per rank); a second slots kernel
+// places rank r's tokens in ascending order from psum_rank[r] on, using warp
+// ballots over the tokens' rank masks for the position inside the chunk.
 // No kernel waits on another CTA.
 #include <cuda_runtime.h>
 
@@ -179,9 +185,9 @@ __global__ void __launch_bounds__(kCountThreads) ep_layout_count_kernel(LayoutPa
   }
   __syncthreads();
 
-  // stable rank of each entry within the chunk
+  // stable rank of each entry within the chunk (the expand layout's slots)
   int32_t* local = p.dst_slot + static_cast<int64_t>(t0) * K;
-  for (int i = wbeg; i < wend; i += 32) {
+  for (int i = wbeg; i < wend && !p.no_expand; i += 32) {
     const int idx = i + lane;
     const int e = idx < wend ? ids[idx] : -1;
     const unsigned peers = __match_any_sync(0xffffffffu, e);
@@ -364,6 +370,184 @@ __global__ void __launch_bounds__(kSlotThreads) ep_layout_slots_kernel(LayoutPar
   for (int64_t f = sbeg + threadIdx.x; f < send; f += kSlotThreads) p.meta[f] = -1;
 }
 
+// ---------------------------------------------------------------- slots, non-expand
+
+constexpr int kTokenWarps = kLayoutTPC / 32;
+
+// Exclusive scan of v[r] over r < n <= 64 by one warp (two values per lane)
+// into out[0..n] (out[n] = total).
+__device__ __forceinline__ void warp_scan64(const int32_t* v, int n, int32_t* out) {
+  const int lane = threadIdx.x & 31;
+  const int r0 = 2 * lane, r1 = r0 + 1;
+  const int v0 = r0 < n ? v[r0] : 0, v1 = r1 < n ? v[r1] : 0;
+  int incl = v0 + v1;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  const int ex = incl - v0 - v1;
+  if (r0 < n) out[r0] = ex;
+  if (r1 < n) out[r1] = ex + v0;
+  if (lane == 31) out[n] = incl;
+}
+
+// Rank r's rows are its tokens in ascending order: the row of (t, r) is
+// psum_rank[r] + chunk_off[r][chunk] + (tokens of the chunk before t that reach
+// r).  Threads 0..127 own the chunk's tokens; each rank's positions come from
+// a ballot per token warp and an exclusive scan over the four warps.
+template <int KC>
+__global__ void __launch_bounds__(kSlotThreads) ep_layout_slots_ne_kernel(LayoutParams p) {
+  constexpr int KM = KC ? KC : kMaxTopk;
+  constexpr int TW = kTokenWarps;
+  const int K = KC ? KC : p.topk;
+  const int KW = K + 2;
+  const int E = p.num_experts, W = p.world_size, C = p.num_chunks;
+  const int T = p.max_tok_per_rank;
+  const int RM = K < W ? K : W;            // rows per token at most
+  extern __shared__ int32_t sm[];
+  int2* sorted = reinterpret_cast<int2*>(sm);          // [TPC*RM] (token, row) by (rank, token)
+  int32_t* prank = sm + 2 * kLayoutTPC * RM;          // [W+1] exclusive prefix of tokens per rank
+  int32_t* tpr = prank + W + 1;                        // [W]   tokens per rank
+  int32_t* rcl = tpr + W;                              // [W]   this chunk's tokens per rank
+  int32_t* rbase = rcl + W;                            // [W]   first row of this chunk per rank
+  int32_t* rcx = rbase + W;                            // [W+1] exclusive scan of rcl over ranks
+  int32_t* woff = rcx + W + 1;                         // [TW][W] per-warp counts, then offsets
+  int32_t* warp_tot = woff + TW * W;                   // [33]
+  int32_t* dslot = warp_tot + 33;                      // [TPC*K] row of each (t, k)
+  int32_t* src = dslot + kLayoutTPC * K;               // [2*TPC] {t / T, t mod T}
+  int32_t* cnt_s = src + 2 * kLayoutTPC;               // [E]   (CTA 0)
+  int32_t* psum_s = cnt_s + E;                         // [E+1] (CTA 0)
+
+  const int c = blockIdx.x;
+  const bool has_tokens = c < C;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  wait_for_preceding_grid();
+  for (int r = tid; r < W; r += kSlotThreads) {
+    tpr[r] = p.col_total[E + r];
+    if (has_tokens) {
+      rcl[r] = p.chunk_hist[static_cast<int64_t>(E + r) * C + c];
+      rbase[r] = p.chunk_off[static_cast<int64_t>(E + r) * C + c];
+    }
+  }
+  __syncthreads();
+  if (warp == 0) warp_scan64(tpr, W, prank);
+  if (warp == 1 && has_tokens) warp_scan64(rcl, W, rcx);
+  __syncthreads();
+  for (int r = tid; r < W && has_tokens; r += kSlotThreads) rbase[r] += prank[r];
+
+  if (c == 0) {  // the counts and prefix sums (the expert ones as in the expand layout)
+    for (int e = tid; e < E; e += kSlotThreads) cnt_s[e] = p.col_total[e];
+    __syncthreads();
+    block_exclusive_scan(cnt_s, E, p.alignment, psum_s, warp_tot);
+    for (int e = tid; e <= E; e += kSlotThreads) {
+      p.psum_expert[e] = psum_s[e];
+      if (e < E) p.cnt[e] = cnt_s[e];
+    }
+    for (int r = tid; r <= W; r += kSlotThreads) {
+      p.psum_rank[r] = prank[r];
+      if (r < W) p.tok_per_rank[r] = tpr[r];
+    }
+    if (tid == 0) *p.num_recv = prank[W];
+  }
+
+  const int t0 = c * kLayoutTPC;
+  const int ntok = has_tokens ? min(p.num_tokens, t0 + kLayoutTPC) - t0 : 0;
+  const int tl = tid;                      // token of this thread (token warps only)
+  unsigned long long mask = 0ull;
+  int rk[KM];                              // rank of each entry, -1 when skipped
+#pragma unroll
+  for (int k = 0; k < KM; ++k) {
+    rk[k] = -1;
+    if (k < K && warp < TW && tl < ntok) {
+      const int e = expert_of(p.topk_idx[static_cast<int64_t>(t0 + tl) * K + k], E);
+      if (e >= 0) {
+        rk[k] = rank_of(e, p.epr_magic);
+        mask |= 1ull << rk[k];
+      }
+    }
+  }
+  if (warp < TW)
+    for (int r = 0; r < W; ++r) {
+      const unsigned b = __ballot_sync(0xffffffffu, (mask >> r) & 1ull);
+      if (lane == 0) woff[warp * W + r] = __popc(b);
+    }
+  __syncthreads();
+  for (int r = tid; r < W; r += kSlotThreads) {
+    int run = 0;
+#pragma unroll
+    for (int w = 0; w < TW; ++w) {
+      const int v = woff[w * W + r];
+      woff[w * W + r] = run;
+      run += v;
+    }
+  }
+  __syncthreads();
+
+  if (warp < TW && has_tokens) {
+    int32_t* ss = p.send_slot + static_cast<int64_t>(t0 + tl) * K;
+    int j = 0;
+    for (int r = 0; r < W; ++r) {
+      const bool has = (mask >> r) & 1ull;
+      const unsigned b = __ballot_sync(0xffffffffu, has);
+      if (has) {
+        const int pos = woff[warp * W + r] + __popc(b & lanemask_lt());
+        const int row = rbase[r] + pos;
+        ss[j++] = row;
+        sorted[rcx[r] + pos] = make_int2(tl, row);
+#pragma unroll
+        for (int k = 0; k < KM; ++k)
+          if (k < K && rk[k] == r) dslot[tl * K + k] = row;
+      }
+    }
+    if (tl < ntok) {
+      for (; j < K; ++j) ss[j] = -1;
+      int32_t* ds = p.dst_slot + static_cast<int64_t>(t0 + tl) * K;
+#pragma unroll
+      for (int k = 0; k < KM; ++k)
+        if (k < K) {
+          if (rk[k] < 0) dslot[tl * K + k] = -1;
+          ds[k] = dslot[tl * K + k];
+        }
+      const int t = t0 + tl, sr = t / T;
+      src[2 * tl] = sr;
+      src[2 * tl + 1] = t - sr * T;
+    }
+  }
+  __syncthreads();
+
+  // metadata rows of this chunk in (rank, token) order: the rows of one rank
+  // from one chunk are contiguous, so consecutive threads write consecutive words
+  if (has_tokens) {
+    const int nvalid = rcx[W];
+    if ((KW & 1) == 0) {
+      const int hw = KW / 2;
+      for (int f = tid; f < nvalid * hw; f += kSlotThreads) {
+        const int q = f / hw, c2 = f - q * hw;
+        const int2 e = sorted[q];
+        const int2 v = c2 == 0 ? make_int2(src[2 * e.x], src[2 * e.x + 1])
+                               : make_int2(dslot[e.x * K + 2 * c2 - 2], dslot[e.x * K + 2 * c2 - 1]);
+        reinterpret_cast<int2*>(p.meta + static_cast<int64_t>(e.y) * KW)[c2] = v;
+      }
+    } else {
+      for (int f = tid; f < nvalid * KW; f += kSlotThreads) {
+        const int q = f / KW, col = f - q * KW;
+        const int2 e = sorted[q];
+        const int v = col < 2 ? src[2 * e.x + col] : dslot[e.x * K + col - 2];
+        p.meta[static_cast<int64_t>(e.y) * KW + col] = v;
+      }
+    }
+  }
+
+  // this CTA's slice of the rows that receive nothing, [R, capacity)
+  const int64_t tail_beg = static_cast<int64_t>(prank[W]) * KW;
+  const int64_t tail_words = p.rcap * KW - tail_beg;
+  const int64_t per = (tail_words + gridDim.x - 1) / gridDim.x;
+  const int64_t sbeg = tail_beg + per * c;
+  const int64_t send = sbeg + per < p.rcap * KW ? sbeg + per : p.rcap * KW;
+  for (int64_t f = sbeg + tid; f < send; f += kSlotThreads) p.meta[f] = -1;
+}
+
 // ---------------------------------------------------------------- launch
 
 template <class Kern>
@@ -392,7 +576,15 @@ size_t slots_smem(int E, int topk) {
                             2 * kLayoutTPC);
 }
 
-template <int KC>
+size_t slots_ne_smem(int E, int W, int topk) {
+  const size_t rm = static_cast<size_t>(topk < W ? topk : W);
+  return sizeof(int32_t) * (2 * kLayoutTPC * rm + 5 * static_cast<size_t>(W) + 2 +
+                            static_cast<size_t>(kTokenWarps) * W + 33 +
+                            static_cast<size_t>(kLayoutTPC) * topk + 2 * kLayoutTPC +
+                            2 * static_cast<size_t>(E) + 1);
+}
+
+template <int KC, bool NE>
 cudaError_t launch_layout(const LayoutParams& p, const LaunchGeom& g, cudaStream_t s) {
   const int EW = p.num_experts + p.world_size;
   if (p.num_chunks > 0)
@@ -403,22 +595,30 @@ cudaError_t launch_layout(const LayoutParams& p, const LaunchGeom& g, cudaStream
                        kSpineWarps * 32, 0, s, p);
   if (e != cudaSuccess) return e;
   const int grid = p.num_chunks > g.num_sms ? p.num_chunks : g.num_sms;
-  return launch_dependent(ep_layout_slots_kernel<KC>, grid, kSlotThreads,
-                          slots_smem(p.num_experts, p.topk), s, p);
+  if constexpr (NE)
+    return launch_dependent(ep_layout_slots_ne_kernel<KC>, grid, kSlotThreads,
+                            slots_ne_smem(p.num_experts, p.world_size, p.topk), s, p);
+  else
+    return launch_dependent(ep_layout_slots_kernel<KC>, grid, kSlotThreads,
+                            slots_smem(p.num_experts, p.topk), s, p);
 }
 
 // Shared-memory limits are set to what the largest launch can need (every E+W
 // and, for the generic variant, every top-k the library accepts), so that
 // handles with different shapes never lower them for each other.
-template <int KC>
+template <int KC, bool NE>
 cudaError_t prepare_layout(int, int, int, LaunchGeom* g) {
   const int kmax = KC ? KC : kMaxTopk;
   cudaError_t e = cudaFuncSetAttribute(ep_layout_count_kernel<KC>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(count_smem(kmax, kMaxExperts + kMaxWorld)));
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(ep_layout_slots_kernel<KC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(slots_smem(kMaxExperts, kmax)));
+  if constexpr (NE)
+    e = cudaFuncSetAttribute(ep_layout_slots_ne_kernel<KC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(slots_ne_smem(kMaxExperts, kMaxWorld, kmax)));
+  else
+    e = cudaFuncSetAttribute(ep_layout_slots_kernel<KC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(slots_smem(kMaxExperts, kmax)));
   if (e != cudaSuccess) return e;
   g->blocks_per_sm = 1;
   return cudaSuccess;
@@ -445,12 +645,18 @@ uint32_t RankMagic(int num_expert_per_rank) {
   return static_cast<uint32_t>((1ull << 32) / static_cast<uint64_t>(num_expert_per_rank) + 1ull);
 }
 
-Variant<LayoutLaunch> FindLayout(int topk) {
+Variant<LayoutLaunch> FindLayout(int topk, bool no_expand) {
+  if (no_expand) switch (topk) {
+      case 4: return {"ep_layout_nonexpand_k4", launch_layout<4, true>, prepare_layout<4, true>};
+      case 6: return {"ep_layout_nonexpand_k6", launch_layout<6, true>, prepare_layout<6, true>};
+      case 8: return {"ep_layout_nonexpand_k8", launch_layout<8, true>, prepare_layout<8, true>};
+      default: return {"ep_layout_nonexpand_generic", launch_layout<0, true>, prepare_layout<0, true>};
+    }
   switch (topk) {
-    case 4: return {"ep_layout_k4", launch_layout<4>, prepare_layout<4>};
-    case 6: return {"ep_layout_k6", launch_layout<6>, prepare_layout<6>};
-    case 8: return {"ep_layout_k8", launch_layout<8>, prepare_layout<8>};
-    default: return {"ep_layout_generic", launch_layout<0>, prepare_layout<0>};
+    case 4: return {"ep_layout_k4", launch_layout<4, false>, prepare_layout<4, false>};
+    case 6: return {"ep_layout_k6", launch_layout<6, false>, prepare_layout<6, false>};
+    case 8: return {"ep_layout_k8", launch_layout<8, false>, prepare_layout<8, false>};
+    default: return {"ep_layout_generic", launch_layout<0, false>, prepare_layout<0, false>};
   }
 }
 

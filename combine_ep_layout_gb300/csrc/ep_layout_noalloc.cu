@@ -66,7 +66,7 @@ void setup_device(DeviceSetup* s) {
   const int topks[] = {4, 6, 8, 0};
   for (int k : topks) {
     LaunchGeom g{s->num_sms, 1};
-    if ((e = FindLayout(k).prepare(0, k, kMaxExperts + kMaxWorld, &g)) != cudaSuccess) {
+    if ((e = FindLayout(k, false).prepare(0, k, kMaxExperts + kMaxWorld, &g)) != cudaSuccess) {
       s->err = e;
       return;
     }
@@ -93,6 +93,8 @@ extern "C" int ep_layout_noalloc(const ep_cfg_t* cfg, const int64_t* topk_idx, i
   try {
     const int64_t rcap = ep_recv_capacity(cfg);  // validates cfg and records the message
     if (rcap < 0) return static_cast<int>(rcap);
+    if (cfg->no_expand)
+      return RecordError(EP_EUNSUPPORTED, "ep_layout_noalloc serves the expand layout only");
     const int W = cfg->world_size, E = W * cfg->num_expert_per_rank, K = cfg->num_expert_per_token;
     const int64_t max_tokens = static_cast<int64_t>(W) * cfg->max_tok_per_rank;
     if (num_tokens < 0 || num_tokens > max_tokens)
@@ -152,7 +154,7 @@ extern "C" int ep_layout_noalloc(const ep_cfg_t* cfg, const int64_t* topk_idx, i
     p.epr_magic = RankMagic(cfg->num_expert_per_rank);
     BindLayoutScratch(&p, s->scratch, Cs, cols);
     const LaunchGeom g{s->num_sms, 1};
-    if ((e = FindLayout(K).launch(p, g, st)) != cudaSuccess) return err_cuda(e, "layout launch");
+    if ((e = FindLayout(K, false).launch(p, g, st)) != cudaSuccess) return err_cuda(e, "layout launch");
     return EP_OK;
   } catch (...) {
     return RecordError(EP_EINVAL, "unknown exception");

@@ -30,8 +30,11 @@ struct DispatchParams {
   // routing forwarded with the rows (both nullptr: not forwarded)
   const float* topk_weights;   // fp32 [N, K]
   const int32_t* topk_i32;     // int32 [N, K] expert ids (the handle's clone)
-  float* recv_topk_weights;    // fp32 [Rcap] or nullptr
-  int32_t* recv_topk_idx;      // int32 [Rcap] or nullptr
+  float* recv_topk_weights;    // fp32 [Rcap] (non-expand: [Rcap, K]) or nullptr
+  int32_t* recv_topk_idx;      // int32 [Rcap] (non-expand: [Rcap, K]) or nullptr
+  // non-expand layout: dst_slot above holds the token's distinct rows and this
+  // the row of each (t, k); nullptr for the expand layout
+  const int32_t* entry_slot;   // [N, K]
 };
 
 struct CombineParams {

@@ -76,6 +76,12 @@ typedef struct {
     int32_t expert_alignment;     /* A: each expert's receive segment is padded to a multiple of A */
     int32_t dispatch_dtype;       /* ep_dtype_t */
     int32_t use_weights;          /* 1: combine weights rows by topk_weights; 0: plain sum */
+    int32_t no_expand;            /* 0: expand layout (EPHandle do_expand = true): one receive
+                                   *    row per (token, expert), grouped by expert, padded to A;
+                                   * 1: non-expand layout (do_expand = false): one receive row per
+                                   *    (token, destination rank), grouped by rank, no padding;
+                                   *    requires use_weights = 0 (the rank's experts apply the
+                                   *    weights; combine sums the rank rows) */
 } ep_cfg_t;
 
 enum {
@@ -91,15 +97,16 @@ enum {
 typedef struct ep_handle *ep_handle_t;
 
 /* Receive-buffer rows needed for any routing of up to W*T tokens:
- * Rcap = W*T*K + E*(A-1) (every (token, k) gets a row; each expert segment
- * adds at most A-1 padding rows).  Returns a negative EP_E* code for an
- * invalid configuration. */
+ * expand layout Rcap = W*T*K + E*(A-1) (every (token, k) gets a row; each
+ * expert segment adds at most A-1 padding rows); non-expand layout
+ * Rcap = W*T*min(K, W) (a token reaches at most min(K, W) ranks).  Returns a
+ * negative EP_E* code for an invalid configuration. */
 int64_t ep_recv_capacity(const ep_cfg_t *cfg) EP_NOEXCEPT;
 
 /* Validate cfg, pick the compiled kernel variants for it and allocate the
  * handle's device metadata on the current device (cudaMalloc; sized for W*T
- * tokens).  *out receives the handle.  Errors: EP_EINVAL (bad cfg or NULL),
- * EP_EUNSUPPORTED, EP_ENOMEM, EP_ECUDA. */
+ * tokens).  *out receives the handle.  Errors: EP_EINVAL (bad cfg or NULL;
+ * no_expand = 1 with use_weights = 1), EP_EUNSUPPORTED, EP_ENOMEM, EP_ECUDA. */
 int ep_handle_create(const ep_cfg_t *cfg, ep_handle_t *out) EP_NOEXCEPT;
 
 /* Layout.  topk_idx: device int64 [num_tokens, K] row-major, token t of
@@ -117,7 +124,20 @@ int ep_handle_create(const ep_cfg_t *cfg, ep_handle_t *out) EP_NOEXCEPT;
  *   recv_src_metadata [Rcap, K+2]              for each received row:
  *                                              {t / T, t mod T, dst_slot[t][0..K-1]};
  *                                              -1 in every row that receives nothing
+ *   send_slot [num_tokens, K]                  the rows dispatch writes token t to and
+ *                                              combine reads it from (expand: dst_slot)
  * (EPHandle listing of "DeepEP overall architecture analysis").
+ * Non-expand layout (cfg.no_expand = 1; the EPHandle's do_expand = false): the
+ * counts and psum_num_recv_tokens_per_expert are as above (the receiving
+ * experts' token counts), and
+ *   psum_num_recv_tokens_per_rank [W+1]        exclusive prefix sum of num_tokens_per_rank
+ *   num_recv_tokens [1]                        R = psum_rank[W], one row per (token, rank)
+ *   rows                                       rank r owns [psum_rank[r], psum_rank[r+1]),
+ *                                              its tokens once each, ascending
+ *   dst_slot [num_tokens, K]                   the row of t on the rank of topk_idx[t][k]
+ *                                              (entries on one rank share it), -1 if skipped
+ *   send_slot [num_tokens, K]                  t's distinct rows, ascending, then -1
+ *   recv_src_metadata [Rcap, K+2]              {t / T, t mod T, dst_slot[t][0..K-1]} per row
  * 0 <= num_tokens <= W*T, else EP_EINVAL.  The number of tokens is kept in the
  * handle for the following ep_dispatch / ep_combine calls. */
 int ep_layout(ep_handle_t h, const int64_t *topk_idx, int32_t num_tokens, ep_stream_t stream) EP_NOEXCEPT;
@@ -130,6 +150,7 @@ int ep_layout(ep_handle_t h, const int64_t *topk_idx, int32_t num_tokens, ep_str
  *              [Rcap, H/128]; per token and 128-channel group g:
  *              s = amax|x[t, g]| / 448 (fp32), q = e4m3_rn_satfinite(x / s),
  *              s = 0 and q = 0 when amax = 0; written to every row dst_slot[t][k].
+ * Non-expand layout: x[t] is written once to each row send_slot[t][j] >= 0.
  * recv_scales must be non-NULL for EP_FP8_E4M3 and NULL otherwise.  Rows
  * that receive no token are not written.  Uses the routing of the last
  * ep_layout call on this handle (same stream, or ordered after it).
@@ -142,6 +163,9 @@ int ep_dispatch(ep_handle_t h, const void *x, void *recv_x, float *recv_scales,
  * recv_topk_weights).  Same as ep_dispatch, and for every received (t, k):
  *   recv_topk_weights[dst_slot[t][k]] = topk_weights[t][k]   (fp32 [Rcap])
  *   recv_topk_idx[dst_slot[t][k]]     = topk_idx[t][k]       (int32 [Rcap], global expert id)
+ * Non-expand layout: every received row s of token t gets K entries,
+ *   recv_topk_idx[s][k]     = topk_idx[t][k] if (t, k) is carried by s (dst_slot[t][k] == s), else -1
+ *   recv_topk_weights[s][k] = topk_weights[t][k] if so, else 0.0f   (both [Rcap, K])
  * Either output may be NULL (then it is not written); topk_weights (device
  * fp32 [N, K]) is required when recv_topk_weights is given.  Rows that
  * receive nothing are not written. */
@@ -156,6 +180,8 @@ int ep_dispatch_fwd(ep_handle_t h, const void *x, void *recv_x, float *recv_scal
  *   acc = +0.0f; for k = 0..K-1 with dst_slot[t][k] >= 0:
  *       acc = fmaf(w[t][k], y[dst_slot[t][k]][c], acc)     (acc += y without weights)
  *   out[t][c] = bf16 round-to-nearest-even(acc).
+ * Non-expand layout: acc = +0.0f; acc = acc + y[send_slot[t][j]][c] for the
+ * token's rows in ascending order (ascending rank); no weights.
  * Padding rows of y are never read.  Buffers must be 16-byte aligned. */
 int ep_combine(ep_handle_t h, const void *y, const float *topk_weights, void *out,
                ep_stream_t stream) EP_NOEXCEPT;
@@ -171,7 +197,8 @@ int ep_combine(ep_handle_t h, const void *y, const float *topk_weights, void *ou
  * compiled into the library (held by every GPU that loads the library until
  * the process exits).
  *   cfg                       as for ep_handle_create (dispatch_dtype,
- *                             hidden_dim and use_weights are checked but unused)
+ *                             hidden_dim and use_weights are checked but unused;
+ *                             no_expand = 1 returns EP_EUNSUPPORTED)
  *   topk_idx                  device int64 [num_tokens, K], 8-byte aligned
  *   num_unaligned_per_expert  device int32 [E]
  *   num_tokens_per_rank       device int32 [W]
@@ -220,7 +247,8 @@ enum {
     EP_FIELD_RECV_SRC_METADATA = 5,        /* int32 [Rcap, K+2] */
     EP_FIELD_NUM_RECV = 6,                 /* int32 [1] */
     EP_FIELD_DEVICE_ERROR = 7,             /* int32 [1], sticky error bits */
-    EP_FIELD_TOPK_IDX = 8                  /* int32 [N, K] copy of topk_idx (-1 where skipped) */
+    EP_FIELD_TOPK_IDX = 8,                 /* int32 [N, K] copy of topk_idx (-1 where skipped) */
+    EP_FIELD_SEND_SLOT = 9                 /* int32 [N, K] rows of each token (expand: dst_slot) */
 };
 
 /* Device pointer and element count of one handle field (the handle keeps

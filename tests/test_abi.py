@@ -52,6 +52,8 @@ BAD = [
     dict(dispatch_dtype=2, hidden_dim=7176),   # FP8 needs hidden % 128 == 0
     dict(dispatch_dtype=9), dict(use_weights=2),
     dict(max_tok_per_rank=1 << 22),            # W*T > 2^24
+    dict(no_expand=2),
+    dict(no_expand=1, use_weights=1),          # rank rows are combined unweighted
 ]
 
 
@@ -68,6 +70,26 @@ def test_invalid_configs_are_rejected_on_the_host(bad):
     assert h.value is None
     assert ep.ep_last_error()
     assert L.ep_recv_capacity(ctypes.byref(cfg)) == ep.EP_EINVAL
+
+
+@pytest.mark.parametrize("name", list(synth.WORKLOADS))
+def test_nonexpand_recv_capacity_matches_the_oracle(name):
+    wl = synth.WORKLOADS[name]
+    cfg = ep.make_cfg(wl.world_size, wl.hidden, wl.max_tok_per_rank, wl.num_expert_per_rank,
+                      wl.topk, wl.alignment, wl.dispatch_dtype, False, no_expand=True)
+    want = oracle.recv_capacity_nonexpand(wl.world_size * wl.max_tok_per_rank, wl.topk,
+                                          wl.world_size)
+    assert ep.ep_recv_capacity(cfg) == want == wl.world_size * wl.max_tok_per_rank * min(
+        wl.topk, wl.world_size)
+
+
+def test_noalloc_layout_refuses_the_nonexpand_layout():
+    L = ep.load_library()
+    cfg = ep.make_cfg(4, 1024, 32, 8, 4, 1, "bf16", False, no_expand=True)
+    rc = L.ep_layout_noalloc(ctypes.byref(cfg), None, 0, None, None, None, None, None, None, None,
+                             None, None)
+    assert rc == ep.EP_EUNSUPPORTED
+    assert "expand" in ep.ep_last_error()
 
 
 def test_transport_dtypes_are_validated():
