@@ -78,6 +78,16 @@ def algorithmic_bytes(N, H, K, rcap, valid_entries=None):
     }
 
 
+def algorithmic_bytes_nonexpand(N, H, K, rows, rcap, fp8):
+    """Bytes of the non-expand layout's kernels: `rows` (token, rank) rows received."""
+    G = H // 128
+    return {
+        "layout": N * K * 8 + 2 * N * K * 4 + rcap * (K + 2) * 4,
+        "dispatch": N * H * 2 + N * K * 4 + rows * (H + G * 4 if fp8 else 2 * H),
+        "combine": rows * H * 2 + N * K * 4 + N * H * 2,
+    }
+
+
 def measured_peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -387,10 +397,11 @@ def run_e2e(args, ep, torch, dev, wl, topk_cpu, w_cpu, x, handles, bufs, step_by
 # ------------------------------------------------------------- all configs
 
 def run_all_configs(args):
-    """Per workload (tiny, decode, prefill bf16, prefill FP8, skewed): layout,
-    dispatch and combine timed separately with CUDA events, L2 flushed (a 256 MB
-    write) before every step and outside the timed events; medians over
-    args.steps steps.  One JSON line per workload."""
+    """Per workload (tiny, decode, prefill bf16, prefill FP8, skewed) and layout
+    (expand, then non-expand: one row per (token, rank), unweighted combine):
+    layout, dispatch and combine timed separately with CUDA events, L2 flushed
+    (a 256 MB write) before every step and outside the timed events; medians
+    over args.steps steps.  One JSON line per workload and layout."""
     import torch
 
     import combine_ep_layout_gb300 as ep
@@ -401,10 +412,11 @@ def run_all_configs(args):
     peak, peak_kind = measured_peaks()
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     s = torch.cuda.Stream(device=dev)
-    for name, wl in synth.WORKLOADS.items():
-        N, H, K, R = wl.num_tokens, wl.hidden, wl.topk, wl.recv_capacity
+    for name, wl, ne in [(n, w, ne) for ne in (False, True) for n, w in synth.WORKLOADS.items()]:
+        N, H, K = wl.num_tokens, wl.hidden, wl.topk
         cfg = ep.make_cfg(wl.world_size, H, wl.max_tok_per_rank, wl.num_expert_per_rank, K,
-                          wl.alignment, wl.dispatch_dtype, wl.use_weights)
+                          wl.alignment, wl.dispatch_dtype, wl.use_weights and not ne, no_expand=ne)
+        R = ep.ep_recv_capacity(cfg)
         h = ep.EpHandle(cfg)
         topk = synth.gen_topk(wl).to(dev)
         w = synth.gen_weights(wl).to(dev)
@@ -426,16 +438,22 @@ def run_all_configs(args):
             ev[1].record(s)
             h.dispatch(x, recv, scales, stream=s)
             ev[2].record(s)
-            h.combine(y, w, out, stream=s)
+            h.combine(y, None if ne else w, out, stream=s)
             ev[3].record(s)
             s.synchronize()
             if i >= args.warmup:
                 for j, k in enumerate(times):
                     times[k].append(ev[j].elapsed_time(ev[j + 1]) * 1e3)
         assert h.status() == 0
-        nb = algorithmic_bytes(N, H, K, R)
-        dkey = "dispatch_fp8" if fp8 else "dispatch_bf16"
-        line = {"workload": name, "tokens": N, "hidden": H, "experts": wl.num_experts, "topk": K,
+        if ne:
+            rows = int(h.field(ep.FIELD_NUM_RECV).cpu()[0])
+            nb = algorithmic_bytes_nonexpand(N, H, K, rows, R, fp8)
+            dkey = "dispatch"
+        else:
+            nb = algorithmic_bytes(N, H, K, R)
+            dkey = "dispatch_fp8" if fp8 else "dispatch_bf16"
+        line = {"workload": name, "layout_kind": "non-expand" if ne else "expand",
+                "tokens": N, "hidden": H, "experts": wl.num_experts, "topk": K,
                 "alignment": wl.alignment, "dispatch_dtype": wl.dispatch_dtype,
                 "routing": wl.routing, "l2": "flushed before every step (256 MB write)",
                 "steps": args.steps, "peak_gbs": peak, "peak_kind": peak_kind}
