@@ -45,6 +45,9 @@ KERNEL_FILES = {"ep_dispatch_copy_kernel": ["ep_dispatch_body.cuh", "ep_dispatch
                 "ep_layout_slots_kernel": ["ep_layout.cu"]}
 
 
+# GPU cycles of the pre-roll sleep before each --all-configs step (~100 us at 2 GHz)
+SLEEP_CYCLES = 200_000
+
 # ----------------------------------------------------------------- helpers
 
 def dist_env():
@@ -401,7 +404,11 @@ def run_all_configs(args):
     (expand, then non-expand: one row per (token, rank), unweighted combine):
     layout, dispatch and combine timed separately with CUDA events, L2 flushed
     (a 256 MB write) before every step and outside the timed events; medians
-    over args.steps steps.  One JSON line per workload and layout."""
+    over args.steps steps.  One JSON line per workload and layout.  Each step
+    starts behind a ~100 us device-side sleep, so that the host has enqueued
+    the whole step before the GPU reaches it: the events then time device work
+    (and the gaps between back-to-back kernels), not Python's launch latency,
+    which is longer than a small workload's kernels."""
     import torch
 
     import combine_ep_layout_gb300 as ep
@@ -432,6 +439,7 @@ def run_all_configs(args):
         for i in range(args.warmup + args.steps):
             with torch.cuda.stream(s):
                 flush.fill_(i & 0xFF)
+                torch.cuda._sleep(SLEEP_CYCLES)
             ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
             ev[0].record(s)
             h.layout(topk, stream=s)
@@ -456,6 +464,7 @@ def run_all_configs(args):
                 "tokens": N, "hidden": H, "experts": wl.num_experts, "topk": K,
                 "alignment": wl.alignment, "dispatch_dtype": wl.dispatch_dtype,
                 "routing": wl.routing, "l2": "flushed before every step (256 MB write)",
+                "timing": "device: step enqueued behind a 100 us GPU sleep",
                 "steps": args.steps, "peak_gbs": peak, "peak_kind": peak_kind}
         for k, b in (("layout", nb["layout"]), ("dispatch", nb[dkey]), ("combine", nb["combine"])):
             us = statistics.median(times[k])

@@ -110,6 +110,7 @@ struct ep_handle {
   // the token's distinct rank rows for the non-expand one
   int32_t* send_slot = nullptr;
   Variant<LayoutLaunch> layout{};
+  std::string layout_ran;  // kernel name of the last ep_layout (cluster or three launches)
   Variant<DispatchLaunch> dispatch{};
   Variant<CombineLaunch> combine{};
   LaunchGeom g_layout{}, g_dispatch{}, g_combine{};
@@ -294,8 +295,11 @@ int ep_layout(ep_handle_t h, const int64_t* topk_idx, int32_t num_tokens, ep_str
     p.epr_magic = RankMagic(h->Epr);
     BindLayoutScratch(&p, h->scratch, h->max_chunks, h->E + h->W);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const bool cluster = LayoutUsesCluster(p, h->g_layout);
     cudaError_t e = h->layout.launch(p, h->g_layout, s);
     if (e != cudaSuccess) return fail_cuda(e, "layout launch");
+    h->layout_ran = h->layout.name;
+    if (cluster) h->layout_ran.insert(h->layout_ran.rfind('_'), "_cluster");  // ..._cluster_k8
     h->num_tokens = num_tokens;
     h->last_stream = s;
     return EP_OK;
@@ -470,7 +474,7 @@ int ep_handle_status(ep_handle_t h, int32_t* device_error) noexcept {
 int ep_handle_variant(ep_handle_t h, int32_t step, char* buf, int32_t len) noexcept {
   try {
     if (!h || !buf || len < 1) return fail(EP_EINVAL, "NULL argument");
-    const char* name = step == 0 ? h->layout.name
+    const char* name = step == 0 ? (h->layout_ran.empty() ? h->layout.name : h->layout_ran.c_str())
                      : step == 1 ? (h->jit_dispatch.function ? h->jit_dispatch.name.c_str()
                                                              : h->dispatch.name)
                      : step == 2 ? (h->jit_combine.function ? h->jit_combine.name.c_str()

@@ -51,6 +51,7 @@ struct LayoutParams {
 struct LaunchGeom {
   int num_sms;        // SMs of the device
   int blocks_per_sm;  // resident CTAs per SM for the variant's block and shared memory
+  int cluster_ok;     // layout: the single-launch cluster kernel can be scheduled
 };
 
 using LayoutLaunch = cudaError_t (*)(const LayoutParams&, const LaunchGeom&, cudaStream_t);
@@ -68,6 +69,9 @@ struct Variant {
 };
 
 Variant<LayoutLaunch> FindLayout(int topk, bool no_expand);
+// True when a layout launch with these parameters runs the single-launch
+// cluster kernel (small batches) rather than count / spine / slots.
+bool LayoutUsesCluster(const LayoutParams& p, const LaunchGeom& g);
 Variant<DispatchLaunch> FindDispatch(int hidden, int topk, EpDType dtype);
 Variant<CombineLaunch> FindCombine(int hidden, int topk, bool use_weights);
 

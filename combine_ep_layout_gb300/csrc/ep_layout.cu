@@ -6,9 +6,12 @@
 //
 // Rows of one expert are ordered by the flat index t*K+k, so the slot of an
 // entry is psum_expert[e] + (number of earlier entries routed to e): a stable
-// counting sort.  Three launches, the last two with programmatic dependent
-// launch so that each is scheduled while its predecessor drains:
+// counting sort.  The tokens are cut into ranges, one per CTA; each range is
+// counted (count_tokens), the ranges' counts are scanned, and each range
+// writes its slots and metadata (slots_*_tokens).  Two ways to run that:
 //
+// Large batches, three launches (the last two with programmatic dependent
+// launch so that each is scheduled while its predecessor drains):
 //   count  one CTA per chunk of kLayoutTPC tokens.  The chunk's ids are staged
 //          in shared memory with one coalesced load and every pass runs from
 //          there.  Per-warp histograms over contiguous runs of entries use
@@ -31,15 +34,26 @@
 //          Every CTA also writes -1 into its share of the rows that receive
 //          nothing (expert padding and [R, capacity)).
 //
+// Small batches (up to kClusterCtas * kClusterMaxTPB tokens), one launch: a
+// single thread-block cluster, one CTA per token range.  Each CTA counts its
+// range into shared memory; after a cluster barrier every CTA reads the other
+// CTAs' column totals through distributed shared memory (its offset inside
+// each column is the sum over the CTAs before it), and goes on to the slots
+// and metadata of its range without another launch.  A second cluster barrier
+// keeps every CTA's shared memory alive until the others have read it.
+//
 // Non-expand layout (EPHandle do_expand = false): one row per (token,
-// destination rank).  count and spine are shared (the rank columns of the
-// table already count each chunk's tokens per rank); a second slots kernel
-// places rank r's tokens in ascending order from psum_rank[r] on, using warp
-// ballots over the tokens' rank masks for the position inside the chunk.
-// No kernel waits on another CTA.
+// destination rank).  The counting is shared (the rank columns already count
+// each range's tokens per rank); the slots step places rank r's tokens in
+// ascending order from psum_rank[r] on, using warp ballots over the tokens'
+// rank masks for the position inside the range.
+//
+// No kernel waits on a flag: the only waits are the cluster barriers, which
+// every thread of every CTA of the cluster reaches unconditionally.
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <cstdlib>
 
 #include "ep_cfg.hpp"
 #include "ep_kernels.hpp"
@@ -52,6 +66,13 @@ namespace {
 constexpr int kCountThreads = kLayoutCountWarps * 32;
 constexpr int kSpineWarps = 8;
 constexpr int kSlotThreads = 256;
+constexpr int kClusterThreads = kCountThreads;   // the cluster kernel counts like count
+constexpr int kClusterCtas = 8;                  // portable cluster size
+constexpr int kClusterMaxTPB = 2 * kLayoutTPC;   // tokens per CTA of the cluster kernel
+// The cluster kernel is used when its padding and tail rows are few (at most
+// this many rows to fill with -1 on kClusterCtas SMs) and its shared memory fits.
+constexpr int64_t kClusterMaxFillRows = 1 << 16;
+constexpr size_t kClusterMaxSmem = 160 * 1024;
 
 __device__ __forceinline__ int expert_of(int64_t v, int E) {
   return (v >= 0 && v < E) ? static_cast<int>(v) : -1;
@@ -73,6 +94,43 @@ __device__ __forceinline__ void allow_dependents() {
 __device__ __forceinline__ void wait_for_preceding_grid() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
 }
+
+// ---- thread-block cluster primitives (sm_90 and later) ----------------------
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t cluster_nctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+  return r;
+}
+
+// Arrive at the cluster barrier (release: this thread's shared-memory writes
+// become visible to the cluster) / wait for every thread of the cluster to
+// arrive (acquire).  Every thread of every CTA executes both, warp-converged.
+__device__ __forceinline__ void cluster_arrive() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Load the int32 at the same shared-memory offset as `local` in CTA `rank` of
+// the cluster (distributed shared memory).
+__device__ __forceinline__ int32_t ld_cluster_shared(const int32_t* local, uint32_t rank) {
+  const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(local));
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(a), "r"(rank));
+  int32_t v;
+  asm volatile("ld.shared::cluster.b32 %0, [%1];" : "=r"(v) : "r"(remote) : "memory");
+  return v;
+}
+
+// ---- scans --------------------------------------------------------------------
 
 // Block-wide exclusive scan of align(v[e], A) for e in [0, n) into out[0..n]
 // (out[n] = total).  warp_tot needs 33 words.  All threads must call it.
@@ -113,27 +171,43 @@ __device__ void block_exclusive_scan(const int32_t* v, int n, int A, int32_t* ou
   __syncthreads();
 }
 
+// Exclusive scan of v[r] over r < n <= 64 by one warp (two values per lane)
+// into out[0..n] (out[n] = total).
+__device__ __forceinline__ void warp_scan64(const int32_t* v, int n, int32_t* out) {
+  const int lane = threadIdx.x & 31;
+  const int r0 = 2 * lane, r1 = r0 + 1;
+  const int v0 = r0 < n ? v[r0] : 0, v1 = r1 < n ? v[r1] : 0;
+  int incl = v0 + v1;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  const int ex = incl - v0 - v1;
+  if (r0 < n) out[r0] = ex;
+  if (r1 < n) out[r1] = ex + v0;
+  if (lane == 31) out[n] = incl;
+}
+
 // ---------------------------------------------------------------- count
 
+// Count the tokens [t0, t0 + ntok) of this CTA (kCountThreads threads, all of
+// which call this).  ids [ntok*K] receives the staged expert ids (-1 = skip);
+// whist [NW][E+W] ends as each warp's exclusive start per column; colcnt[E+W]
+// receives the range's column totals (entries per expert, tokens per rank);
+// loc, when non-null, receives each entry's stable rank among the range's
+// entries of its expert (shared or global memory).
 template <int KC>
-__global__ void __launch_bounds__(kCountThreads) ep_layout_count_kernel(LayoutParams p) {
+__device__ void count_tokens(const LayoutParams& p, int t0, int ntok, int32_t* whist, int32_t* ids,
+                             int32_t* colcnt, int32_t* loc) {
   constexpr int NW = kLayoutCountWarps;
   const int K = KC ? KC : p.topk;
   const int E = p.num_experts, W = p.world_size;
   const int EW = E + W;
-  const int C = p.num_chunks;
-  extern __shared__ int32_t sm[];
-  int32_t* whist = sm;                                     // [NW][EW]
-  int32_t* ids = whist + NW * EW;                          // [TPC*K] expert ids, -1 = skip
-
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int c = blockIdx.x;
-  const int t0 = c * kLayoutTPC;
-  const int ntok = min(p.num_tokens, t0 + kLayoutTPC) - t0;
   const int nent = ntok * K;
   const int64_t* topk = p.topk_idx + static_cast<int64_t>(t0) * K;
 
-  allow_dependents();
   bool bad = false;
   int32_t* clone = p.topk_i32 ? p.topk_i32 + static_cast<int64_t>(t0) * K : nullptr;
   for (int i = tid; i < nent; i += kCountThreads) {
@@ -172,7 +246,7 @@ __global__ void __launch_bounds__(kCountThreads) ep_layout_count_kernel(LayoutPa
   }
   __syncthreads();
 
-  // exclusive scan across warps per column; the column total is the chunk's count
+  // exclusive scan across warps per column; the column total is the range's count
   for (int j = tid; j < EW; j += kCountThreads) {
     int run = 0;
 #pragma unroll
@@ -181,24 +255,43 @@ __global__ void __launch_bounds__(kCountThreads) ep_layout_count_kernel(LayoutPa
       whist[w * EW + j] = run;
       run += v;
     }
-    p.chunk_hist[static_cast<int64_t>(j) * C + c] = run;
+    colcnt[j] = run;
   }
   __syncthreads();
 
-  // stable rank of each entry within the chunk (the expand layout's slots)
-  int32_t* local = p.dst_slot + static_cast<int64_t>(t0) * K;
-  for (int i = wbeg; i < wend && !p.no_expand; i += 32) {
-    const int idx = i + lane;
-    const int e = idx < wend ? ids[idx] : -1;
-    const unsigned peers = __match_any_sync(0xffffffffu, e);
-    const int base = e >= 0 ? wh[e] : 0;
-    const int rank = base + __popc(peers & lanemask_lt());
-    __syncwarp();
-    if (e >= 0 && lane == __ffs(peers) - 1) wh[e] = base + __popc(peers);
-    __syncwarp();
-    if (idx < wend) local[idx] = e >= 0 ? rank : -1;
-  }
+  // stable rank of each entry within the range (the expand layout's slots)
+  if (loc != nullptr)
+    for (int i = wbeg; i < wend; i += 32) {
+      const int idx = i + lane;
+      const int e = idx < wend ? ids[idx] : -1;
+      const unsigned peers = __match_any_sync(0xffffffffu, e);
+      const int base = e >= 0 ? wh[e] : 0;
+      const int rank = base + __popc(peers & lanemask_lt());
+      __syncwarp();
+      if (e >= 0 && lane == __ffs(peers) - 1) wh[e] = base + __popc(peers);
+      __syncwarp();
+      if (idx < wend) loc[idx] = e >= 0 ? rank : -1;
+    }
   if (bad) atomicOr(p.err, kErrBadExpert);
+}
+
+template <int KC>
+__global__ void __launch_bounds__(kCountThreads) ep_layout_count_kernel(LayoutParams p) {
+  const int K = KC ? KC : p.topk;
+  const int EW = p.num_experts + p.world_size;
+  const int C = p.num_chunks;
+  extern __shared__ int32_t sm[];
+  int32_t* whist = sm;                                      // [NW][EW]
+  int32_t* colcnt = whist + kLayoutCountWarps * EW;         // [EW]
+  int32_t* ids = colcnt + EW;                               // [TPC*K]
+  const int c = blockIdx.x;
+  const int t0 = c * kLayoutTPC;
+  const int ntok = min(p.num_tokens, t0 + kLayoutTPC) - t0;
+  allow_dependents();
+  count_tokens<KC>(p, t0, ntok, whist, ids, colcnt,
+                   p.no_expand ? nullptr : p.dst_slot + static_cast<int64_t>(t0) * K);
+  for (int j = threadIdx.x; j < EW; j += kCountThreads)
+    p.chunk_hist[static_cast<int64_t>(j) * C + c] = colcnt[j];
 }
 
 // ---------------------------------------------------------------- spine
@@ -254,15 +347,118 @@ __global__ void __launch_bounds__(kSpineWarps * 32) ep_layout_spine_kernel(Layou
   if (lane == 0) p.col_total[j] = total;
 }
 
-// ---------------------------------------------------------------- slots
+// ---------------------------------------------------------------- slots (expand)
 
+// CTA 0's outputs: counts, aligned expert prefix, rank prefix at each rank's
+// first expert, tokens per rank, number of receive rows.
+__device__ void write_outputs_expand(const LayoutParams& p, const int32_t* cnt_s,
+                                     const int32_t* psum_s, const int32_t* tpr) {
+  const int E = p.num_experts, W = p.world_size;
+  for (int e = threadIdx.x; e <= E; e += blockDim.x) {
+    p.psum_expert[e] = psum_s[e];
+    if (e < E) p.cnt[e] = cnt_s[e];
+  }
+  for (int r = threadIdx.x; r <= W; r += blockDim.x) {
+    p.psum_rank[r] = psum_s[r * p.num_expert_per_rank];
+    if (r < W) p.tok_per_rank[r] = tpr[r];
+  }
+  if (threadIdx.x == 0) *p.num_recv = psum_s[E];
+}
+
+// Slots and metadata of the tokens [t0, t0 + ntok) of this CTA (expand
+// layout; all threads call, token t0 + i is owned by thread i).  psum_s [E+1]
+// is the aligned expert prefix, co[E] the range's offset inside each expert's
+// rows, cx[E+1] the exclusive scan over experts of the range's counts, loc the
+// stable rank of each entry within the range (count_tokens; may alias
+// p.dst_slot, which is overwritten with the slots), ids the staged expert ids
+// or nullptr (then read from topk_idx).  Scratch: slots_s and sorted [ntok*K],
+// src [2*ntok].
 template <int KC>
-__global__ void __launch_bounds__(kSlotThreads) ep_layout_slots_kernel(LayoutParams p) {
+__device__ void slots_expand_tokens(const LayoutParams& p, int t0, int ntok, const int32_t* psum_s,
+                                    const int32_t* co, const int32_t* cx, const int32_t* loc,
+                                    const int32_t* ids, int32_t* slots_s, int32_t* sorted,
+                                    int32_t* src) {
   constexpr int KM = KC ? KC : kMaxTopk;
   const int K = KC ? KC : p.topk;
   const int KW = K + 2;  // metadata row width
+  const int E = p.num_experts, T = p.max_tok_per_rank;
+  const int nthr = blockDim.x;
+  if (threadIdx.x < ntok) {
+    const int tl = threadIdx.x, t = t0 + tl;
+    const int64_t* row = p.topk_idx + static_cast<int64_t>(t) * K;
+    int32_t* ds = p.dst_slot + static_cast<int64_t>(t) * K;
+    int32_t slot[KM];
+#pragma unroll
+    for (int k = 0; k < KM; ++k) {
+      if (k < K) {
+        const int e = ids ? ids[tl * K + k] : expert_of(row[k], E);
+        const int l = loc[tl * K + k];
+        slot[k] = e >= 0 ? psum_s[e] + co[e] + l : -1;
+        if (e >= 0) sorted[cx[e] + l] = tl * K + k;
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < KM; ++k)
+      if (k < K) {
+        ds[k] = slot[k];
+        slots_s[tl * K + k] = slot[k];
+      }
+    const int r = t / T;
+    src[2 * tl] = r;
+    src[2 * tl + 1] = t - r * T;
+  }
+  __syncthreads();
+
+  // metadata rows of this range, in (expert, rank) order: flat words f of the
+  // concatenated rows; rows of one expert are contiguous in memory.
+  const int nvalid = cx[E];
+  if ((KW & 1) == 0) {
+    // even row width: word pairs (8-byte stores; rows start 8-byte aligned)
+    const int hw = KW / 2;
+    for (int f = threadIdx.x; f < nvalid * hw; f += nthr) {
+      const int q = f / hw, c2 = f - q * hw;
+      const int entry = sorted[q];
+      const int tl = entry / K;
+      const int2 v = c2 == 0 ? make_int2(src[2 * tl], src[2 * tl + 1])
+                             : make_int2(slots_s[tl * K + 2 * c2 - 2], slots_s[tl * K + 2 * c2 - 1]);
+      reinterpret_cast<int2*>(p.meta + static_cast<int64_t>(slots_s[entry]) * KW)[c2] = v;
+    }
+  } else {
+    for (int f = threadIdx.x; f < nvalid * KW; f += nthr) {
+      const int q = f / KW, col = f - q * KW;
+      const int entry = sorted[q];
+      const int tl = entry / K;
+      const int v = col < 2 ? src[2 * tl + col] : slots_s[tl * K + col - 2];
+      p.meta[static_cast<int64_t>(slots_s[entry]) * KW + col] = v;
+    }
+  }
+}
+
+// -1 into the rows that receive nothing, share `part` of `parts`: the padding
+// of experts e = part, part + parts, ... (cnt_s non-null: expand layout) and a
+// slice of [R, capacity).
+__device__ void fill_unreceived(const LayoutParams& p, const int32_t* psum_s, const int32_t* cnt_s,
+                                int R, int part, int parts) {
+  const int KW = p.topk + 2;
+  const int nthr = blockDim.x;
+  if (cnt_s != nullptr)
+    for (int e = part; e < p.num_experts; e += parts) {
+      const int64_t beg = static_cast<int64_t>(psum_s[e] + cnt_s[e]) * KW;
+      const int64_t end = static_cast<int64_t>(psum_s[e + 1]) * KW;
+      for (int64_t f = beg + threadIdx.x; f < end; f += nthr) p.meta[f] = -1;
+    }
+  const int64_t tail_beg = static_cast<int64_t>(R) * KW;
+  const int64_t tail_words = p.rcap * KW - tail_beg;
+  const int64_t per = (tail_words + parts - 1) / parts;
+  const int64_t sbeg = tail_beg + per * part;
+  const int64_t send = sbeg + per < p.rcap * KW ? sbeg + per : p.rcap * KW;
+  for (int64_t f = sbeg + threadIdx.x; f < send; f += nthr) p.meta[f] = -1;
+}
+
+template <int KC>
+__global__ void __launch_bounds__(kSlotThreads) ep_layout_slots_kernel(LayoutParams p) {
+  const int K = KC ? KC : p.topk;
   const int E = p.num_experts, C = p.num_chunks;
-  const int T = p.max_tok_per_rank;
   extern __shared__ int32_t sm[];
   int32_t* psum_s = sm;                   // [E+1]
   int32_t* cnt_s = psum_s + E + 1;        // [E]
@@ -287,172 +483,38 @@ __global__ void __launch_bounds__(kSlotThreads) ep_layout_slots_kernel(LayoutPar
   __syncthreads();
   // the aligned exclusive prefix over experts (every CTA; E values)
   block_exclusive_scan(cnt_s, E, p.alignment, psum_s, warp_tot);
-  if (c == 0) {
-    const int W = p.world_size;
-    for (int e = threadIdx.x; e <= E; e += kSlotThreads) {
-      p.psum_expert[e] = psum_s[e];
-      if (e < E) p.cnt[e] = cnt_s[e];
-    }
-    for (int r = threadIdx.x; r <= W; r += kSlotThreads) {
-      p.psum_rank[r] = psum_s[r * p.num_expert_per_rank];
-      if (r < W) p.tok_per_rank[r] = p.col_total[E + r];
-    }
-    if (threadIdx.x == 0) *p.num_recv = psum_s[E];
+  if (c == 0) write_outputs_expand(p, cnt_s, psum_s, p.col_total + E);
+  if (has_tokens) {  // uniform per CTA
+    block_exclusive_scan(cl, E, 1, cx, warp_tot);
+    const int t0 = c * kLayoutTPC;
+    const int ntok = min(p.num_tokens, t0 + kLayoutTPC) - t0;
+    slots_expand_tokens<KC>(p, t0, ntok, psum_s, co, cx, p.dst_slot + static_cast<int64_t>(t0) * K,
+                            nullptr, slots_s, sorted, src);
   }
-  if (has_tokens) block_exclusive_scan(cl, E, 1, cx, warp_tot);  // uniform per CTA
-
-  const int t0 = c * kLayoutTPC;
-  const int ntok = has_tokens ? min(p.num_tokens, t0 + kLayoutTPC) - t0 : 0;
-  if (threadIdx.x < ntok) {
-    const int tl = threadIdx.x, t = t0 + tl;
-    const int64_t* row = p.topk_idx + static_cast<int64_t>(t) * K;
-    int32_t* ds = p.dst_slot + static_cast<int64_t>(t) * K;
-    int32_t slot[KM];
-#pragma unroll
-    for (int k = 0; k < KM; ++k) {
-      if (k < K) {
-        const int e = expert_of(row[k], E);
-        const int loc = ds[k];
-        slot[k] = e >= 0 ? psum_s[e] + co[e] + loc : -1;
-        if (e >= 0) sorted[cx[e] + loc] = tl * K + k;
-      }
-    }
-#pragma unroll
-    for (int k = 0; k < KM; ++k)
-      if (k < K) {
-        ds[k] = slot[k];
-        slots_s[tl * K + k] = slot[k];
-      }
-    const int r = t / T;
-    src[2 * tl] = r;
-    src[2 * tl + 1] = t - r * T;
-  }
-  __syncthreads();
-
-  // metadata rows of this chunk, in (expert, rank) order: flat words f of the
-  // concatenated rows; rows of one expert are contiguous in memory.
-  if (has_tokens) {
-    const int nvalid = cx[E];
-    if ((KW & 1) == 0) {
-      // even row width: word pairs (8-byte stores; rows start 8-byte aligned)
-      const int hw = KW / 2;
-      for (int f = threadIdx.x; f < nvalid * hw; f += kSlotThreads) {
-        const int q = f / hw, c2 = f - q * hw;
-        const int entry = sorted[q];
-        const int tl = entry / K;
-        const int2 v = c2 == 0 ? make_int2(src[2 * tl], src[2 * tl + 1])
-                               : make_int2(slots_s[tl * K + 2 * c2 - 2], slots_s[tl * K + 2 * c2 - 1]);
-        reinterpret_cast<int2*>(p.meta + static_cast<int64_t>(slots_s[entry]) * KW)[c2] = v;
-      }
-    } else {
-      for (int f = threadIdx.x; f < nvalid * KW; f += kSlotThreads) {
-        const int q = f / KW, col = f - q * KW;
-        const int entry = sorted[q];
-        const int tl = entry / K;
-        const int v = col < 2 ? src[2 * tl + col] : slots_s[tl * K + col - 2];
-        p.meta[static_cast<int64_t>(slots_s[entry]) * KW + col] = v;
-      }
-    }
-  }
-
-  // rows that receive nothing: the padding of experts e = c, c + grid, ... and
-  // this CTA's slice of [R, capacity)
-  for (int e = c; e < E; e += gridDim.x) {
-    const int64_t beg = static_cast<int64_t>(psum_s[e] + cnt_s[e]) * KW;
-    const int64_t end = static_cast<int64_t>(psum_s[e + 1]) * KW;
-    for (int64_t f = beg + threadIdx.x; f < end; f += kSlotThreads) p.meta[f] = -1;
-  }
-  const int64_t tail_beg = static_cast<int64_t>(psum_s[E]) * KW;
-  const int64_t tail_words = p.rcap * KW - tail_beg;
-  const int64_t per = (tail_words + gridDim.x - 1) / gridDim.x;
-  const int64_t sbeg = tail_beg + per * c;
-  const int64_t send = sbeg + per < p.rcap * KW ? sbeg + per : p.rcap * KW;
-  for (int64_t f = sbeg + threadIdx.x; f < send; f += kSlotThreads) p.meta[f] = -1;
+  fill_unreceived(p, psum_s, cnt_s, psum_s[E], c, gridDim.x);
 }
 
-// ---------------------------------------------------------------- slots, non-expand
-
-constexpr int kTokenWarps = kLayoutTPC / 32;
-
-// Exclusive scan of v[r] over r < n <= 64 by one warp (two values per lane)
-// into out[0..n] (out[n] = total).
-__device__ __forceinline__ void warp_scan64(const int32_t* v, int n, int32_t* out) {
-  const int lane = threadIdx.x & 31;
-  const int r0 = 2 * lane, r1 = r0 + 1;
-  const int v0 = r0 < n ? v[r0] : 0, v1 = r1 < n ? v[r1] : 0;
-  int incl = v0 + v1;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += y;
-  }
-  const int ex = incl - v0 - v1;
-  if (r0 < n) out[r0] = ex;
-  if (r1 < n) out[r1] = ex + v0;
-  if (lane == 31) out[n] = incl;
-}
+// ---------------------------------------------------------------- slots (non-expand)
 
 // Rank r's rows are its tokens in ascending order: the row of (t, r) is
-// psum_rank[r] + chunk_off[r][chunk] + (tokens of the chunk before t that reach
-// r).  Threads 0..127 own the chunk's tokens; each rank's positions come from
-// a ballot per token warp and an exclusive scan over the four warps.
+// psum_rank[r] + (the range's offset in rank r) + (tokens of the range before
+// t that reach r).  Token warps (threads < tpb, tpb a multiple of 32, token
+// t0 + i owned by thread i) take each rank's positions from a ballot per warp
+// and an exclusive scan over the token warps.  rbase[W] = psum_rank[r] + the
+// range's offset, rcx[W+1] = exclusive scan over ranks of the range's tokens
+// per rank; scratch: woff [tpb/32][W], dslot [tpb*K], src [2*tpb], sorted
+// [tpb*min(K, W)] (8-byte aligned).  All threads call.
 template <int KC>
-__global__ void __launch_bounds__(kSlotThreads) ep_layout_slots_ne_kernel(LayoutParams p) {
+__device__ void slots_nonexpand_tokens(const LayoutParams& p, int t0, int ntok, int tpb,
+                                       const int32_t* rbase, const int32_t* rcx, const int32_t* ids,
+                                       int32_t* woff, int32_t* dslot, int32_t* src, int2* sorted) {
   constexpr int KM = KC ? KC : kMaxTopk;
-  constexpr int TW = kTokenWarps;
   const int K = KC ? KC : p.topk;
   const int KW = K + 2;
-  const int E = p.num_experts, W = p.world_size, C = p.num_chunks;
-  const int T = p.max_tok_per_rank;
-  const int RM = K < W ? K : W;            // rows per token at most
-  extern __shared__ int32_t sm[];
-  int2* sorted = reinterpret_cast<int2*>(sm);          // [TPC*RM] (token, row) by (rank, token)
-  int32_t* prank = sm + 2 * kLayoutTPC * RM;          // [W+1] exclusive prefix of tokens per rank
-  int32_t* tpr = prank + W + 1;                        // [W]   tokens per rank
-  int32_t* rcl = tpr + W;                              // [W]   this chunk's tokens per rank
-  int32_t* rbase = rcl + W;                            // [W]   first row of this chunk per rank
-  int32_t* rcx = rbase + W;                            // [W+1] exclusive scan of rcl over ranks
-  int32_t* woff = rcx + W + 1;                         // [TW][W] per-warp counts, then offsets
-  int32_t* warp_tot = woff + TW * W;                   // [33]
-  int32_t* dslot = warp_tot + 33;                      // [TPC*K] row of each (t, k)
-  int32_t* src = dslot + kLayoutTPC * K;               // [2*TPC] {t / T, t mod T}
-  int32_t* cnt_s = src + 2 * kLayoutTPC;               // [E]   (CTA 0)
-  int32_t* psum_s = cnt_s + E;                         // [E+1] (CTA 0)
-
-  const int c = blockIdx.x;
-  const bool has_tokens = c < C;
+  const int E = p.num_experts, W = p.world_size, T = p.max_tok_per_rank;
+  const int TW = tpb / 32;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  wait_for_preceding_grid();
-  for (int r = tid; r < W; r += kSlotThreads) {
-    tpr[r] = p.col_total[E + r];
-    if (has_tokens) {
-      rcl[r] = p.chunk_hist[static_cast<int64_t>(E + r) * C + c];
-      rbase[r] = p.chunk_off[static_cast<int64_t>(E + r) * C + c];
-    }
-  }
-  __syncthreads();
-  if (warp == 0) warp_scan64(tpr, W, prank);
-  if (warp == 1 && has_tokens) warp_scan64(rcl, W, rcx);
-  __syncthreads();
-  for (int r = tid; r < W && has_tokens; r += kSlotThreads) rbase[r] += prank[r];
-
-  if (c == 0) {  // the counts and prefix sums (the expert ones as in the expand layout)
-    for (int e = tid; e < E; e += kSlotThreads) cnt_s[e] = p.col_total[e];
-    __syncthreads();
-    block_exclusive_scan(cnt_s, E, p.alignment, psum_s, warp_tot);
-    for (int e = tid; e <= E; e += kSlotThreads) {
-      p.psum_expert[e] = psum_s[e];
-      if (e < E) p.cnt[e] = cnt_s[e];
-    }
-    for (int r = tid; r <= W; r += kSlotThreads) {
-      p.psum_rank[r] = prank[r];
-      if (r < W) p.tok_per_rank[r] = tpr[r];
-    }
-    if (tid == 0) *p.num_recv = prank[W];
-  }
-
-  const int t0 = c * kLayoutTPC;
-  const int ntok = has_tokens ? min(p.num_tokens, t0 + kLayoutTPC) - t0 : 0;
+  const int nthr = blockDim.x;
   const int tl = tid;                      // token of this thread (token warps only)
   unsigned long long mask = 0ull;
   int rk[KM];                              // rank of each entry, -1 when skipped
@@ -460,7 +522,8 @@ __global__ void __launch_bounds__(kSlotThreads) ep_layout_slots_ne_kernel(Layout
   for (int k = 0; k < KM; ++k) {
     rk[k] = -1;
     if (k < K && warp < TW && tl < ntok) {
-      const int e = expert_of(p.topk_idx[static_cast<int64_t>(t0 + tl) * K + k], E);
+      const int e = ids ? ids[tl * K + k]
+                        : expert_of(p.topk_idx[static_cast<int64_t>(t0 + tl) * K + k], E);
       if (e >= 0) {
         rk[k] = rank_of(e, p.epr_magic);
         mask |= 1ull << rk[k];
@@ -473,9 +536,8 @@ __global__ void __launch_bounds__(kSlotThreads) ep_layout_slots_ne_kernel(Layout
       if (lane == 0) woff[warp * W + r] = __popc(b);
     }
   __syncthreads();
-  for (int r = tid; r < W; r += kSlotThreads) {
+  for (int r = tid; r < W; r += nthr) {
     int run = 0;
-#pragma unroll
     for (int w = 0; w < TW; ++w) {
       const int v = woff[w * W + r];
       woff[w * W + r] = run;
@@ -484,7 +546,7 @@ __global__ void __launch_bounds__(kSlotThreads) ep_layout_slots_ne_kernel(Layout
   }
   __syncthreads();
 
-  if (warp < TW && has_tokens) {
+  if (warp < TW) {
     int32_t* ss = p.send_slot + static_cast<int64_t>(t0 + tl) * K;
     int j = 0;
     for (int r = 0; r < W; ++r) {
@@ -516,36 +578,194 @@ __global__ void __launch_bounds__(kSlotThreads) ep_layout_slots_ne_kernel(Layout
   }
   __syncthreads();
 
-  // metadata rows of this chunk in (rank, token) order: the rows of one rank
-  // from one chunk are contiguous, so consecutive threads write consecutive words
-  if (has_tokens) {
-    const int nvalid = rcx[W];
-    if ((KW & 1) == 0) {
-      const int hw = KW / 2;
-      for (int f = tid; f < nvalid * hw; f += kSlotThreads) {
-        const int q = f / hw, c2 = f - q * hw;
-        const int2 e = sorted[q];
-        const int2 v = c2 == 0 ? make_int2(src[2 * e.x], src[2 * e.x + 1])
-                               : make_int2(dslot[e.x * K + 2 * c2 - 2], dslot[e.x * K + 2 * c2 - 1]);
-        reinterpret_cast<int2*>(p.meta + static_cast<int64_t>(e.y) * KW)[c2] = v;
-      }
-    } else {
-      for (int f = tid; f < nvalid * KW; f += kSlotThreads) {
-        const int q = f / KW, col = f - q * KW;
-        const int2 e = sorted[q];
-        const int v = col < 2 ? src[2 * e.x + col] : dslot[e.x * K + col - 2];
-        p.meta[static_cast<int64_t>(e.y) * KW + col] = v;
-      }
+  // metadata rows of this range in (rank, token) order: the rows of one rank
+  // from one range are contiguous, so consecutive threads write consecutive words
+  const int nvalid = rcx[W];
+  if ((KW & 1) == 0) {
+    const int hw = KW / 2;
+    for (int f = tid; f < nvalid * hw; f += nthr) {
+      const int q = f / hw, c2 = f - q * hw;
+      const int2 e = sorted[q];
+      const int2 v = c2 == 0 ? make_int2(src[2 * e.x], src[2 * e.x + 1])
+                             : make_int2(dslot[e.x * K + 2 * c2 - 2], dslot[e.x * K + 2 * c2 - 1]);
+      reinterpret_cast<int2*>(p.meta + static_cast<int64_t>(e.y) * KW)[c2] = v;
+    }
+  } else {
+    for (int f = tid; f < nvalid * KW; f += nthr) {
+      const int q = f / KW, col = f - q * KW;
+      const int2 e = sorted[q];
+      const int v = col < 2 ? src[2 * e.x + col] : dslot[e.x * K + col - 2];
+      p.meta[static_cast<int64_t>(e.y) * KW + col] = v;
     }
   }
+}
 
-  // this CTA's slice of the rows that receive nothing, [R, capacity)
-  const int64_t tail_beg = static_cast<int64_t>(prank[W]) * KW;
-  const int64_t tail_words = p.rcap * KW - tail_beg;
-  const int64_t per = (tail_words + gridDim.x - 1) / gridDim.x;
-  const int64_t sbeg = tail_beg + per * c;
-  const int64_t send = sbeg + per < p.rcap * KW ? sbeg + per : p.rcap * KW;
-  for (int64_t f = sbeg + tid; f < send; f += kSlotThreads) p.meta[f] = -1;
+// CTA 0's outputs of the non-expand layout: counts and aligned expert prefix
+// (as in the expand layout), tokens per rank and their exclusive prefix, rows.
+// cnt_s [E] holds the counts; psum_s [E+1] and warp_tot [33] are scratch.
+// All threads of the CTA call.
+__device__ void write_outputs_nonexpand(const LayoutParams& p, const int32_t* cnt_s, int32_t* psum_s,
+                                        const int32_t* prank, const int32_t* tpr, int32_t* warp_tot) {
+  const int E = p.num_experts, W = p.world_size;
+  block_exclusive_scan(cnt_s, E, p.alignment, psum_s, warp_tot);
+  for (int e = threadIdx.x; e <= E; e += blockDim.x) {
+    p.psum_expert[e] = psum_s[e];
+    if (e < E) p.cnt[e] = cnt_s[e];
+  }
+  for (int r = threadIdx.x; r <= W; r += blockDim.x) {
+    p.psum_rank[r] = prank[r];
+    if (r < W) p.tok_per_rank[r] = tpr[r];
+  }
+  if (threadIdx.x == 0) *p.num_recv = prank[W];
+}
+
+// Shared-memory words of slots_nonexpand_tokens' scratch for tpb tokens.
+__host__ __device__ constexpr int NonExpandScratchWords(int tpb, int K, int W) {
+  return 2 * tpb * (K < W ? K : W) + (tpb / 32) * W + tpb * K + 2 * tpb;
+}
+
+template <int KC>
+__global__ void __launch_bounds__(kSlotThreads) ep_layout_slots_ne_kernel(LayoutParams p) {
+  const int K = KC ? KC : p.topk;
+  const int E = p.num_experts, W = p.world_size, C = p.num_chunks;
+  const int RM = K < W ? K : W;
+  extern __shared__ int32_t sm[];
+  int2* sorted = reinterpret_cast<int2*>(sm);          // [TPC*RM]
+  int32_t* woff = sm + 2 * kLayoutTPC * RM;            // [TPC/32][W]
+  int32_t* dslot = woff + (kLayoutTPC / 32) * W;       // [TPC*K]
+  int32_t* src = dslot + kLayoutTPC * K;               // [2*TPC]
+  int32_t* prank = src + 2 * kLayoutTPC;               // [W+1] exclusive prefix of tokens per rank
+  int32_t* tpr = prank + W + 1;                        // [W]   tokens per rank
+  int32_t* rcl = tpr + W;                              // [W]   this chunk's tokens per rank
+  int32_t* rbase = rcl + W;                            // [W]   first row of this chunk per rank
+  int32_t* rcx = rbase + W;                            // [W+1] exclusive scan of rcl over ranks
+  int32_t* warp_tot = rcx + W + 1;                     // [33]
+  int32_t* cnt_s = warp_tot + 33;                      // [E]   (CTA 0)
+  int32_t* psum_s = cnt_s + E;                         // [E+1] (CTA 0)
+
+  const int c = blockIdx.x;
+  const bool has_tokens = c < C;
+  const int tid = threadIdx.x, warp = tid >> 5;
+  wait_for_preceding_grid();
+  for (int r = tid; r < W; r += kSlotThreads) {
+    tpr[r] = p.col_total[E + r];
+    if (has_tokens) {
+      rcl[r] = p.chunk_hist[static_cast<int64_t>(E + r) * C + c];
+      rbase[r] = p.chunk_off[static_cast<int64_t>(E + r) * C + c];
+    }
+  }
+  __syncthreads();
+  if (warp == 0) warp_scan64(tpr, W, prank);
+  if (warp == 1 && has_tokens) warp_scan64(rcl, W, rcx);
+  __syncthreads();
+  for (int r = tid; r < W && has_tokens; r += kSlotThreads) rbase[r] += prank[r];
+
+  if (c == 0) {
+    for (int e = tid; e < E; e += kSlotThreads) cnt_s[e] = p.col_total[e];
+    __syncthreads();
+    write_outputs_nonexpand(p, cnt_s, psum_s, prank, tpr, warp_tot);
+  }
+  if (has_tokens) {  // uniform per CTA
+    __syncthreads();
+    const int t0 = c * kLayoutTPC;
+    const int ntok = min(p.num_tokens, t0 + kLayoutTPC) - t0;
+    slots_nonexpand_tokens<KC>(p, t0, ntok, kLayoutTPC, rbase, rcx, nullptr, woff, dslot, src,
+                               sorted);
+  }
+  fill_unreceived(p, nullptr, nullptr, prank[W], c, gridDim.x);
+}
+
+// ---------------------------------------------------------------- cluster (small batches)
+
+// Words of shared memory of the cluster kernel for E experts, W ranks, top-k K
+// and tpb tokens per CTA (the carve-up at the top of the kernel).
+__host__ __device__ constexpr int ClusterSmemWords(int E, int W, int K, int tpb, bool ne) {
+  const int EW = E + W;
+  return (ne ? NonExpandScratchWords(tpb, K, W) : 0)      // non-expand scratch (first: int2)
+         + kLayoutCountWarps * EW + 3 * EW                // whist, colcnt, tot, off
+         + tpb * K                                        // ids
+         + (ne ? 0 : 3 * tpb * K + 2 * tpb)               // loc, slots_s, sorted, src (expand)
+         + 2 * (E + 1) + 33                               // psum_s, cx, warp_tot
+         + (W + 1) + W + (W + 1) + W;                     // prank, rbase, rcx, tpr
+}
+
+template <int KC, bool NE>
+__global__ void __launch_bounds__(kClusterThreads) ep_layout_cluster_kernel(LayoutParams p, int tpb) {
+  const int K = KC ? KC : p.topk;
+  const int E = p.num_experts, W = p.world_size, EW = E + W;
+  extern __shared__ int32_t sm[];
+  int32_t* base = sm;
+  int2* sorted_ne = reinterpret_cast<int2*>(sm);               // NE: [tpb*RM]
+  int32_t* woff = nullptr;
+  int32_t* dslot = nullptr;
+  int32_t* src_ne = nullptr;
+  if constexpr (NE) {
+    const int RM = K < W ? K : W;
+    woff = sm + 2 * tpb * RM;                                  // [tpb/32][W]
+    dslot = woff + (tpb / 32) * W;                             // [tpb*K]
+    src_ne = dslot + tpb * K;                                  // [2*tpb]
+    base = src_ne + 2 * tpb;
+  }
+  int32_t* whist = base;                                       // [NW][EW]
+  int32_t* colcnt = whist + kLayoutCountWarps * EW;            // [EW] this CTA's totals (read remotely)
+  int32_t* tot = colcnt + EW;                                  // [EW] totals over the cluster
+  int32_t* off = tot + EW;                                     // [EW] sum over the CTAs before this one
+  int32_t* ids = off + EW;                                     // [tpb*K]
+  int32_t* loc = ids + tpb * K;                                // expand: [tpb*K]
+  int32_t* slots_s = loc + (NE ? 0 : tpb * K);                 // expand: [tpb*K]
+  int32_t* sorted = slots_s + (NE ? 0 : tpb * K);              // expand: [tpb*K]
+  int32_t* src = sorted + (NE ? 0 : tpb * K);                  // expand: [2*tpb]
+  int32_t* psum_s = src + (NE ? 0 : 2 * tpb);                  // [E+1]
+  int32_t* cx = psum_s + E + 1;                                // [E+1]
+  int32_t* warp_tot = cx + E + 1;                              // [33]
+  int32_t* prank = warp_tot + 33;                              // [W+1]
+  int32_t* rbase = prank + W + 1;                              // [W]
+  int32_t* rcx = rbase + W;                                    // [W+1]
+  int32_t* tpr = rcx + W + 1;                                  // [W]
+
+  const uint32_t me = cluster_ctarank(), ncta = cluster_nctarank();
+  const int t0 = static_cast<int>(me) * tpb;
+  const int ntok = max(0, min(p.num_tokens, t0 + tpb) - t0);
+  count_tokens<KC>(p, t0, ntok, whist, ids, colcnt, NE ? nullptr : loc);
+
+  // every CTA's column totals are complete: gather the cluster's totals and
+  // this CTA's offsets from the other CTAs' shared memory
+  cluster_arrive();
+  cluster_wait();
+  for (int j = threadIdx.x; j < EW; j += kClusterThreads) {
+    int t = 0, o = 0;
+    for (uint32_t b = 0; b < ncta; ++b) {
+      const int v = b == me ? colcnt[j] : ld_cluster_shared(colcnt + j, b);
+      o += b < me ? v : 0;
+      t += v;
+    }
+    tot[j] = t;
+    off[j] = o;
+  }
+  cluster_arrive();  // this CTA is done reading remote shared memory
+  __syncthreads();
+
+  if constexpr (!NE) {
+    block_exclusive_scan(tot, E, p.alignment, psum_s, warp_tot);
+    if (me == 0) write_outputs_expand(p, tot, psum_s, tot + E);
+    block_exclusive_scan(colcnt, E, 1, cx, warp_tot);
+    slots_expand_tokens<KC>(p, t0, ntok, psum_s, off, cx, loc, ids, slots_s, sorted, src);
+    fill_unreceived(p, psum_s, tot, psum_s[E], static_cast<int>(me), static_cast<int>(ncta));
+  } else {
+    const int warp = threadIdx.x >> 5;
+    for (int r = threadIdx.x; r < W; r += kClusterThreads) tpr[r] = tot[E + r];
+    __syncthreads();
+    if (warp == 0) warp_scan64(tpr, W, prank);
+    if (warp == 1) warp_scan64(colcnt + E, W, rcx);
+    __syncthreads();
+    for (int r = threadIdx.x; r < W; r += kClusterThreads) rbase[r] = prank[r] + off[E + r];
+    if (me == 0) write_outputs_nonexpand(p, tot, psum_s, prank, tpr, warp_tot);
+    __syncthreads();
+    slots_nonexpand_tokens<KC>(p, t0, ntok, tpb, rbase, rcx, ids, woff, dslot, src_ne, sorted_ne);
+    fill_unreceived(p, nullptr, nullptr, prank[W], static_cast<int>(me), static_cast<int>(ncta));
+  }
+  // keep this CTA's shared memory until every CTA has finished reading it
+  cluster_wait();
 }
 
 // ---------------------------------------------------------------- launch
@@ -567,7 +787,7 @@ cudaError_t launch_dependent(Kern kernel, int grid, int block, size_t smem, cuda
 }
 
 size_t count_smem(int topk, int cols) {
-  return sizeof(int32_t) * (static_cast<size_t>(kLayoutCountWarps) * cols +
+  return sizeof(int32_t) * (static_cast<size_t>(kLayoutCountWarps) * cols + cols +
                             static_cast<size_t>(kLayoutTPC) * topk);
 }
 
@@ -577,15 +797,48 @@ size_t slots_smem(int E, int topk) {
 }
 
 size_t slots_ne_smem(int E, int W, int topk) {
-  const size_t rm = static_cast<size_t>(topk < W ? topk : W);
-  return sizeof(int32_t) * (2 * kLayoutTPC * rm + 5 * static_cast<size_t>(W) + 2 +
-                            static_cast<size_t>(kTokenWarps) * W + 33 +
-                            static_cast<size_t>(kLayoutTPC) * topk + 2 * kLayoutTPC +
-                            2 * static_cast<size_t>(E) + 1);
+  return sizeof(int32_t) * (static_cast<size_t>(NonExpandScratchWords(kLayoutTPC, topk, W)) +
+                            5 * static_cast<size_t>(W) + 2 + 33 + 2 * static_cast<size_t>(E) + 1);
+}
+
+size_t cluster_smem(int E, int W, int topk, int tpb, bool ne) {
+  return sizeof(int32_t) * static_cast<size_t>(ClusterSmemWords(E, W, topk, tpb, ne));
+}
+
+// Tokens per CTA of the cluster kernel for this launch, or 0 when the batch is
+// served by the three-launch path.
+int cluster_tpb(const LayoutParams& p, const LaunchGeom& g) {
+  if (!g.cluster_ok || p.num_tokens <= 0 || p.num_tokens > kClusterCtas * kClusterMaxTPB) return 0;
+  const int64_t fill = p.rcap - static_cast<int64_t>(p.num_tokens) * p.topk;
+  if (fill > kClusterMaxFillRows) return 0;
+  const int tpb = p.num_tokens <= kClusterCtas * kLayoutTPC ? kLayoutTPC : kClusterMaxTPB;
+  if (cluster_smem(p.num_experts, p.world_size, p.topk, tpb, p.no_expand != 0) > kClusterMaxSmem)
+    return 0;
+  return tpb;
+}
+
+template <int KC, bool NE>
+cudaError_t launch_cluster(const LayoutParams& p, int tpb, cudaStream_t s) {
+  const int ncta = (p.num_tokens + tpb - 1) / tpb;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(ncta);
+  cfg.blockDim = dim3(kClusterThreads);
+  cfg.dynamicSmemBytes = cluster_smem(p.num_experts, p.world_size, p.topk, tpb, NE);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(ncta);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, ep_layout_cluster_kernel<KC, NE>, p, tpb);
 }
 
 template <int KC, bool NE>
 cudaError_t launch_layout(const LayoutParams& p, const LaunchGeom& g, cudaStream_t s) {
+  const int tpb = cluster_tpb(p, g);
+  if (tpb > 0) return launch_cluster<KC, NE>(p, tpb, s);
   const int EW = p.num_experts + p.world_size;
   if (p.num_chunks > 0)
     ep_layout_count_kernel<KC><<<p.num_chunks, kCountThreads, count_smem(p.topk, EW), s>>>(p);
@@ -605,7 +858,10 @@ cudaError_t launch_layout(const LayoutParams& p, const LaunchGeom& g, cudaStream
 
 // Shared-memory limits are set to what the largest launch can need (every E+W
 // and, for the generic variant, every top-k the library accepts), so that
-// handles with different shapes never lower them for each other.
+// handles with different shapes never lower them for each other.  The cluster
+// kernel's limit is kClusterMaxSmem (larger requests take the three-launch
+// path); it is used only if a cluster of kClusterCtas CTAs with that much
+// shared memory can be resident, and not when EP_GB300_LAYOUT_CLUSTER=0.
 template <int KC, bool NE>
 cudaError_t prepare_layout(int, int, int, LaunchGeom* g) {
   const int kmax = KC ? KC : kMaxTopk;
@@ -621,10 +877,37 @@ cudaError_t prepare_layout(int, int, int, LaunchGeom* g) {
                              static_cast<int>(slots_smem(kMaxExperts, kmax)));
   if (e != cudaSuccess) return e;
   g->blocks_per_sm = 1;
+  g->cluster_ok = 0;
+  e = cudaFuncSetAttribute(ep_layout_cluster_kernel<KC, NE>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(kClusterMaxSmem));
+  if (e != cudaSuccess) return e;
+  const char* env = std::getenv("EP_GB300_LAYOUT_CLUSTER");
+  if (env != nullptr && env[0] == '0') return cudaSuccess;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(kClusterCtas);
+  cfg.blockDim = dim3(kClusterThreads);
+  cfg.dynamicSmemBytes = kClusterMaxSmem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kClusterCtas;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int clusters = 0;
+  e = cudaOccupancyMaxActiveClusters(&clusters, ep_layout_cluster_kernel<KC, NE>, &cfg);
+  if (e != cudaSuccess) {
+    cudaGetLastError();  // not schedulable as a cluster here: the three-launch path serves
+    return cudaSuccess;
+  }
+  g->cluster_ok = clusters > 0 ? 1 : 0;
   return cudaSuccess;
 }
 
 }  // namespace
+
+bool LayoutUsesCluster(const LayoutParams& p, const LaunchGeom& g) { return cluster_tpb(p, g) > 0; }
 
 int64_t LayoutScratchInts(int max_chunks, int columns) {
   return 2LL * columns * (max_chunks > 0 ? max_chunks : 1) + columns;

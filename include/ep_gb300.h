@@ -264,7 +264,11 @@ int ep_handle_status(ep_handle_t h, int32_t *device_error) EP_NOEXCEPT;
 /* Name of the kernel variant chosen for a step (0 = layout, 1 = dispatch,
  * 2 = combine) written to buf (NUL-terminated, truncated to len).  A name
  * carries the compile-time shape, e.g. "ep_dispatch_bf16_h7168_k8", or
- * "..._generic" when no specialisation for the shape was compiled. */
+ * "..._generic" when no specialisation for the shape was compiled.  For the
+ * layout it names what the last ep_layout ran: "ep_layout_cluster_k8" for
+ * the single-launch thread-block-cluster kernel that serves batches of up to
+ * 2048 tokens (unless EP_GB300_LAYOUT_CLUSTER=0 when the handle was created),
+ * "ep_layout_k8" for the three launches (count, spine, slots). */
 int ep_handle_variant(ep_handle_t h, int32_t step, char *buf, int32_t len) EP_NOEXCEPT;
 
 /* Run-time specialisation ("MORI JIT v2" §1-§3.4, §6 precompile; the JIT

@@ -486,3 +486,37 @@ def test_sixteen_byte_aligned_buffers_take_the_16_byte_path(name):
     oracle.dispatch_fp8(synth.bits16(case["x"]), ref["dst_slot"], q, s)
     assert np.array_equal(rq.cpu().numpy(), q)
     assert np.array_equal(rs.cpu().numpy().view(np.uint32), s.view(np.uint32))
+
+
+# Small batches run the single-launch cluster layout; EP_GB300_LAYOUT_CLUSTER=0
+# (read when the handle is built) forces the three-launch path.  Both must give
+# the oracle's bytes.
+SMALL = {
+    "tiny": dict(base="tiny"),
+    "decode_masked": dict(base="decode", mask_frac=0.2),
+    "ragged_1000": dict(base="decode", num_tokens=1000),
+    "two_ranges_1500": dict(base="decode", max_tok_per_rank=256, num_tokens=1500),
+    "full_2048": dict(base="decode", max_tok_per_rank=256, num_tokens=2048),
+    "generic_k5": dict(base="tiny", topk=5, hidden=384, alignment=3),
+    "align16": dict(base="decode", alignment=16),
+    "w64": dict(base="tiny", world_size=64, num_expert_per_rank=4, max_tok_per_rank=16,
+                num_tokens=1024, topk=8),
+    "epr7": dict(base="tiny", world_size=3, num_expert_per_rank=7, max_tok_per_rank=64,
+                 num_tokens=150, alignment=5),
+}
+
+
+@pytest.mark.parametrize("path", ["cluster", "launches"])
+@pytest.mark.parametrize("case", list(SMALL))
+def test_small_batch_layout_both_paths(case, path, monkeypatch):
+    monkeypatch.setenv("EP_GB300_LAYOUT_CLUSTER", "1" if path == "cluster" else "0")
+    wl, mask = edge_wl(SMALL[case])
+    topk = synth.gen_topk(wl, mask_frac=mask)
+    h, got, ref = layout_case(wl, topk)
+    assert_layout_equal(got, ref)
+    assert h.status() == 0
+    assert ("_cluster_" in h.variant(0)) == (path == "cluster"), h.variant(0)
+    # a second, different routing on the same handle
+    topk2 = synth.gen_topk(wl.with_(seed=wl.seed + 1), mask_frac=0.1)
+    h.layout(topk2.cuda())
+    assert_layout_equal(gpu_fields(h), oracle_layout(wl, topk2.numpy()))
