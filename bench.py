@@ -390,11 +390,45 @@ def run_e2e(args, ep, torch, dev, wl, topk_cpu, w_cpu, x, handles, bufs, step_by
     torch.cuda.synchronize()
     ms, units = reduce_over_ranks(a.elapsed_time(z) / n, step_bytes, world)
     h2d = x_h.numel() * 2 + topk_h.numel() * 8 + w_h.numel() * 4
+    d2h = out_h[0].numel() * 2
+    link = host_link(torch, x_h, x_d[0], out_d[0], out_h[0], s_in, s_out)
+    link["floor_ms_per_step"] = round((h2d + d2h) / (link["bidir_gbs"] * 1e9) * 1e3, 4)
     return {"value": round(units / (ms * 1e-3) / 1e9, 1), "unit": "GB/s",
             "ms_per_step": round(ms, 4), "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": out_h[0].numel() * 2,
+            "d2h_bytes_per_step": d2h, "host_link": link,
             "pipelining": "double-buffered device inputs/outputs; upload, compute and "
                           "read-back on three streams ordered by events"}
+
+
+def host_link(torch, x_h, x_d, out_d, out_h, s_in, s_out, reps=5):
+    """Copy-engine bandwidth of the host link on the e2e buffers: x up alone,
+    the output down alone, and both at once (the floor under the e2e step)."""
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def timed(up, down):
+        torch.cuda.synchronize()
+        a.record(s_in)
+        s_out.wait_event(a)
+        for _ in range(reps):
+            if up:
+                with torch.cuda.stream(s_in):
+                    x_d.copy_(x_h, non_blocking=True)
+            if down:
+                with torch.cuda.stream(s_out):
+                    out_h.copy_(out_d, non_blocking=True)
+        done = torch.cuda.Event()
+        done.record(s_out)
+        s_in.wait_event(done)
+        b.record(s_in)
+        b.synchronize()
+        return a.elapsed_time(b) / reps
+
+    nb_up, nb_down = x_h.numel() * x_h.element_size(), out_d.numel() * out_d.element_size()
+    timed(True, True)
+    up, down, both = timed(True, False), timed(False, True), timed(True, True)
+    return {"h2d_gbs": round(nb_up / up / 1e6, 1), "d2h_gbs": round(nb_down / down / 1e6, 1),
+            "bidir_gbs": round((nb_up + nb_down) / both / 1e6, 1),
+            "how": "cudaMemcpyAsync from / to the pinned e2e buffers, alone and both directions at once"}
 
 
 # ------------------------------------------------------------- all configs
