@@ -8,7 +8,7 @@ from ._native import (  # noqa: F401
     FIELD_PSUM_PER_RANK, FIELD_DST_SLOT, FIELD_RECV_SRC_METADATA, FIELD_NUM_RECV,
     FIELD_DEVICE_ERROR, FIELD_TOPK_IDX, FIELD_SEND_SLOT, ERR_BAD_EXPERT, ERR_TIMEOUT,
     EpError, EpHandle, ep_cfg_t, make_cfg, load_library, declared_symbols,
-    ep_recv_capacity, ep_handle_create, ep_layout, ep_dispatch, ep_combine, ep_handle_free,
+    ep_recv_capacity, ep_handle_create, ep_handle_create_shared, ep_layout, ep_dispatch, ep_combine, ep_handle_free,
     ep_handle_get, ep_handle_status, ep_handle_variant, ep_last_error,
     ep_layout_noalloc, NOALLOC_OUTPUTS, ep_dispatch_fwd, ep_combine_ex, ep_jit_precompile,
 )

@@ -59,6 +59,8 @@ def load_library():
     L.ep_recv_capacity.argtypes = [c.POINTER(ep_cfg_t)]
     L.ep_handle_create.restype = c.c_int
     L.ep_handle_create.argtypes = [c.POINTER(ep_cfg_t), c.POINTER(vp)]
+    L.ep_handle_create_shared.restype = c.c_int
+    L.ep_handle_create_shared.argtypes = [c.POINTER(ep_cfg_t), vp, c.POINTER(vp)]
     L.ep_layout.restype = c.c_int
     L.ep_layout.argtypes = [vp, vp, i32, vp]
     L.ep_dispatch.restype = c.c_int
@@ -140,11 +142,18 @@ class _DevArray:
 class EpHandle:
     """Owner of an ep_handle_t; methods mirror the C entry points."""
 
-    def __init__(self, cfg):
+    def __init__(self, cfg, layout_of=None):
+        """layout_of: another EpHandle whose layout this one uses
+        (ep_handle_create_shared); it must outlive this handle."""
         self.cfg = cfg
         self.device = torch.cuda.current_device()
         h = ctypes.c_void_p()
-        _check(load_library().ep_handle_create(ctypes.byref(cfg), ctypes.byref(h)))
+        if layout_of is None:
+            _check(load_library().ep_handle_create(ctypes.byref(cfg), ctypes.byref(h)))
+        else:
+            _check(load_library().ep_handle_create_shared(ctypes.byref(cfg), layout_of.ptr,
+                                                          ctypes.byref(h)))
+        self._layout_of = layout_of          # keeps the layout's owner alive
         self._h = h
         self.recv_capacity = ep_recv_capacity(cfg)
         self.num_tokens = 0
@@ -234,6 +243,10 @@ class EpHandle:
 # Function-style API with the C names.
 def ep_handle_create(cfg):
     return EpHandle(cfg)
+
+
+def ep_handle_create_shared(cfg, layout_src):
+    return EpHandle(cfg, layout_of=layout_src)
 
 
 def ep_layout(h, topk_idx, num_tokens=None, stream=None):

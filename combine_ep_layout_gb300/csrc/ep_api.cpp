@@ -103,6 +103,9 @@ struct ep_handle {
   cudaStream_t last_stream = nullptr;
   void* block = nullptr;
   bool no_expand = false;
+  // non-null: this handle uses the routing of that handle's ep_layout (its own
+  // metadata pointers below stay null)
+  ep_handle* src = nullptr;
   int32_t *cnt = nullptr, *tok_per_rank = nullptr, *psum_expert = nullptr, *psum_rank = nullptr,
           *num_recv = nullptr, *err = nullptr, *dst_slot = nullptr, *meta = nullptr,
           *topk_i32 = nullptr, *scratch = nullptr;
@@ -141,6 +144,9 @@ jit::Request combine_request(const ep_cfg_t* c) {
 
 bool aligned32(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 31u) == 0; }
 
+// The handle whose ep_layout produced the routing h uses.
+const ep_handle* owner(const ep_handle* h) { return h->src ? h->src : h; }
+
 int check_device(const ep_handle* h) {
   int dev = -1;
   cudaError_t e = cudaGetDevice(&dev);
@@ -166,13 +172,31 @@ int64_t ep_recv_capacity(const ep_cfg_t* cfg) noexcept {
   }
 }
 
-int ep_handle_create(const ep_cfg_t* cfg, ep_handle_t* out) noexcept {
+}  // extern "C"
+
+namespace {
+
+// ep_handle_create (src null) and ep_handle_create_shared (src: the handle
+// whose layout the new one uses; nothing of the layout is allocated).
+int create_handle(const ep_cfg_t* cfg, ep_handle* src, ep_handle_t* out) {
   try {
     if (!out) return fail(EP_EINVAL, "out is NULL");
     *out = nullptr;
     int rc = validate(cfg);
     if (rc != EP_OK) return rc;
+    if (src) {
+      const ep_cfg_t& c = src->cfg;
+      if (cfg->world_size != c.world_size || cfg->max_tok_per_rank != c.max_tok_per_rank ||
+          cfg->num_expert_per_rank != c.num_expert_per_rank ||
+          cfg->num_expert_per_token != c.num_expert_per_token ||
+          cfg->expert_alignment != c.expert_alignment || cfg->no_expand != c.no_expand)
+        return fail(EP_EINVAL,
+                    "a shared layout needs the world_size, max_tok_per_rank, num_expert_per_rank, "
+                    "num_expert_per_token, expert_alignment and no_expand of layout_src");
+      if ((rc = check_device(src)) != EP_OK) return rc;
+    }
     ep_handle* h = new ep_handle();
+    h->src = src;
     h->cfg = *cfg;
     h->W = cfg->world_size;
     h->T = cfg->max_tok_per_rank;
@@ -220,6 +244,10 @@ int ep_handle_create(const ep_cfg_t* cfg, ep_handle_t* out) noexcept {
       if (is_generic(h->combine.name) && jit::Worthwhile(cr)) jit::Load(cr, &h->jit_combine, &why);
     }
 
+    if (src) {  // the routing, its metadata and the error word are src's
+      *out = h;
+      return EP_OK;
+    }
     // one allocation, 256-byte aligned sub-buffers
     auto al = [](size_t b) { return (b + 255) & ~static_cast<size_t>(255); };
     const size_t n_small = al(4 * (h->E + h->W + (h->E + 1) + (h->W + 1) + 2));
@@ -260,9 +288,25 @@ int ep_handle_create(const ep_cfg_t* cfg, ep_handle_t* out) noexcept {
   }
 }
 
+}  // namespace
+
+extern "C" {
+
+int ep_handle_create(const ep_cfg_t* cfg, ep_handle_t* out) noexcept {
+  return create_handle(cfg, nullptr, out);
+}
+
+int ep_handle_create_shared(const ep_cfg_t* cfg, ep_handle_t layout_src, ep_handle_t* out) noexcept {
+  if (out) *out = nullptr;
+  if (!layout_src) return fail(EP_EINVAL, "layout_src is NULL");
+  return create_handle(cfg, layout_src->src ? layout_src->src : layout_src, out);
+}
+
 int ep_layout(ep_handle_t h, const int64_t* topk_idx, int32_t num_tokens, ep_stream_t stream) noexcept {
   try {
     if (!h) return fail(EP_EINVAL, "handle is NULL");
+    if (h->src)
+      return fail(EP_EINVAL, "this handle uses the layout of another handle: call ep_layout on that one");
     if (num_tokens < 0 || num_tokens > h->max_tokens)
       return fail(EP_EINVAL, "num_tokens must be in [0, world_size*max_tok_per_rank]");
     if (num_tokens > 0 && !topk_idx) return fail(EP_EINVAL, "topk_idx is NULL");
@@ -325,7 +369,8 @@ int ep_dispatch_fwd(ep_handle_t h, const void* x, void* recv_x, float* recv_scal
     if (!fp8 && recv_scales) return fail(EP_EINVAL, "recv_scales is only written by FP8 dispatch");
     if (recv_topk_weights && !topk_weights)
       return fail(EP_EINVAL, "recv_topk_weights needs topk_weights");
-    if (h->num_tokens > 0) {
+    const ep_handle* o = owner(h);
+    if (o->num_tokens > 0) {
       if (!x || !recv_x) return fail(EP_EINVAL, "x / recv_x is NULL");
       if (!aligned16(x) || !aligned16(recv_x) || (recv_scales && !aligned16(recv_scales)))
         return fail(EP_EINVAL, "x, recv_x and recv_scales must be 16-byte aligned");
@@ -340,15 +385,15 @@ int ep_dispatch_fwd(ep_handle_t h, const void* x, void* recv_x, float* recv_scal
     p.x = x;
     p.recv_x = recv_x;
     p.recv_scales = recv_scales;
-    p.dst_slot = h->send_slot;
-    p.entry_slot = h->no_expand ? h->dst_slot : nullptr;
-    p.num_tokens = h->num_tokens;
+    p.dst_slot = o->send_slot;
+    p.entry_slot = o->no_expand ? o->dst_slot : nullptr;
+    p.num_tokens = o->num_tokens;
     p.hidden = h->H;
     p.topk = h->K;
     p.row_bytes = static_cast<int>(RowBytes(h->H, static_cast<EpDType>(h->cfg.dispatch_dtype)));
-    p.err = h->err;
+    p.err = o->err;
     p.topk_weights = topk_weights;
-    p.topk_i32 = h->topk_i32;
+    p.topk_i32 = o->topk_i32;
     p.recv_topk_weights = recv_topk_weights;
     p.recv_topk_idx = recv_topk_idx;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -377,7 +422,8 @@ int ep_combine_ex(ep_handle_t h, const void* y, const float* topk_weights, const
     if (out_dtype != EP_BF16 && out_dtype != EP_FP32)
       return fail(EP_EINVAL, "combine output dtype must be EP_BF16 or EP_FP32");
     const bool weighted = h->cfg.use_weights != 0;
-    if (h->num_tokens > 0) {
+    const ep_handle* o = owner(h);
+    if (o->num_tokens > 0) {
       if (!y || !out) return fail(EP_EINVAL, "y / out is NULL");
       if (weighted && !topk_weights) return fail(EP_EINVAL, "use_weights is set but topk_weights is NULL");
       if (!aligned16(y) || !aligned16(out) || (bias && !aligned16(bias)))
@@ -392,8 +438,8 @@ int ep_combine_ex(ep_handle_t h, const void* y, const float* topk_weights, const
     p.weights = weighted ? topk_weights : nullptr;
     p.bias = bias;
     p.out = out;
-    p.dst_slot = h->send_slot;
-    p.num_tokens = h->num_tokens;
+    p.dst_slot = o->send_slot;
+    p.num_tokens = o->num_tokens;
     p.hidden = h->H;
     p.topk = h->K;
     p.out_f32 = out_dtype == EP_FP32 ? 1 : 0;
@@ -424,6 +470,7 @@ void ep_handle_free(ep_handle_t h) noexcept {
 int ep_handle_get(ep_handle_t h, int32_t field, void** dev_ptr, int64_t* numel) noexcept {
   try {
     if (!h || !dev_ptr || !numel) return fail(EP_EINVAL, "NULL argument");
+    h = const_cast<ep_handle*>(owner(h));  // a shared handle shows its layout_src's fields
     switch (field) {
       case EP_FIELD_NUM_UNALIGNED_PER_EXPERT: *dev_ptr = h->cnt; *numel = h->E; break;
       case EP_FIELD_NUM_TOKENS_PER_RANK: *dev_ptr = h->tok_per_rank; *numel = h->W; break;
@@ -460,9 +507,10 @@ int ep_handle_status(ep_handle_t h, int32_t* device_error) noexcept {
     cudaError_t e = cudaStreamSynchronize(h->last_stream);
     if (e != cudaSuccess) return fail_cuda(e, "cudaStreamSynchronize");
     int32_t v = 0;
-    if ((e = cudaMemcpy(&v, h->err, sizeof v, cudaMemcpyDeviceToHost)) != cudaSuccess)
+    int32_t* err = owner(h)->err;
+    if ((e = cudaMemcpy(&v, err, sizeof v, cudaMemcpyDeviceToHost)) != cudaSuccess)
       return fail_cuda(e, "cudaMemcpy");
-    if ((e = cudaMemset(h->err, 0, sizeof v)) != cudaSuccess) return fail_cuda(e, "cudaMemset");
+    if ((e = cudaMemset(err, 0, sizeof v)) != cudaSuccess) return fail_cuda(e, "cudaMemset");
     if ((e = cudaDeviceSynchronize()) != cudaSuccess) return fail_cuda(e, "cudaDeviceSynchronize");
     *device_error = v;
     return EP_OK;
@@ -474,7 +522,8 @@ int ep_handle_status(ep_handle_t h, int32_t* device_error) noexcept {
 int ep_handle_variant(ep_handle_t h, int32_t step, char* buf, int32_t len) noexcept {
   try {
     if (!h || !buf || len < 1) return fail(EP_EINVAL, "NULL argument");
-    const char* name = step == 0 ? (h->layout_ran.empty() ? h->layout.name : h->layout_ran.c_str())
+    const ep_handle* o = owner(h);
+    const char* name = step == 0 ? (o->layout_ran.empty() ? o->layout.name : o->layout_ran.c_str())
                      : step == 1 ? (h->jit_dispatch.function ? h->jit_dispatch.name.c_str()
                                                              : h->dispatch.name)
                      : step == 2 ? (h->jit_combine.function ? h->jit_combine.name.c_str()

@@ -109,6 +109,22 @@ int64_t ep_recv_capacity(const ep_cfg_t *cfg) EP_NOEXCEPT;
  * no_expand = 1 with use_weights = 1), EP_EUNSUPPORTED, EP_ENOMEM, EP_ECUDA. */
 int ep_handle_create(const ep_cfg_t *cfg, ep_handle_t *out) EP_NOEXCEPT;
 
+/* A handle that uses the routing of another handle's ep_layout instead of
+ * computing its own, e.g. an FP8 dispatch fed by the layout that already
+ * serves a bf16 dispatch of the same tokens (one layout per routing, as the
+ * router produces one topk_idx per step).  cfg must equal layout_src's cfg in
+ * world_size, max_tok_per_rank, num_expert_per_rank, num_expert_per_token,
+ * expert_alignment and no_expand; hidden_dim, dispatch_dtype and use_weights
+ * may differ.  The new handle allocates no metadata: ep_dispatch /
+ * ep_combine on it read layout_src's routing as of layout_src's last
+ * ep_layout (order the calls on one stream, or with events), ep_handle_get
+ * returns layout_src's fields, ep_handle_status reads and clears layout_src's
+ * error word, and ep_layout on it returns EP_EINVAL.  layout_src must stay
+ * alive until the new handle is freed; sharing a shared handle shares its
+ * layout_src.  Errors: EP_EINVAL (NULL, bad or mismatched cfg, another
+ * device), EP_EUNSUPPORTED, EP_ECUDA. */
+int ep_handle_create_shared(const ep_cfg_t *cfg, ep_handle_t layout_src, ep_handle_t *out) EP_NOEXCEPT;
+
 /* Layout.  topk_idx: device int64 [num_tokens, K] row-major, token t of
  * logical rank t / T.  Entries equal to -1 are masked (no receive row); any
  * other value outside [0, E) is skipped and sets bit 0 of the device error

@@ -23,7 +23,7 @@ def built():
 
 def test_exports_every_declared_symbol():
     names = ep.declared_symbols()
-    assert len(names) == 14
+    assert len(names) == 15
     L = ep.load_library()
     for n in names:
         assert hasattr(L, n), n
@@ -106,6 +106,10 @@ def test_transport_dtypes_are_validated():
 
 def test_null_arguments_are_errors_not_crashes():
     L = ep.load_library()
+    cfg = ep.make_cfg(4, 1024, 32, 8, 4)
+    h = ctypes.c_void_p(1)
+    assert L.ep_handle_create_shared(ctypes.byref(cfg), None, ctypes.byref(h)) == ep.EP_EINVAL
+    assert h.value is None and "layout_src" in ep.ep_last_error()
     assert L.ep_handle_create(None, None) == ep.EP_EINVAL
     assert L.ep_layout(None, None, 0, None) == ep.EP_EINVAL
     assert L.ep_dispatch(None, None, None, None, None) == ep.EP_EINVAL

@@ -168,3 +168,61 @@ def test_opaque_transports_move_rows_unchanged(name, dtype):
     oracle.dispatch_bytes(x.view(torch.uint8).cpu().numpy(), ref["dst_slot"], want)
     assert np.array_equal(recv.cpu().numpy(), want)
     assert h.variant(1).startswith("ep_dispatch_" + dtype)
+
+
+def test_shared_layout_feeds_other_dtypes_and_widths():
+    # one layout (bf16 handle) serves an FP8 dispatch and a combine of another width
+    wl = synth.WORKLOADS["decode"]
+    case = synth.make_case(wl, device="cuda", mask_frac=0.05)
+    h16 = ep.EpHandle(cfg_of(wl, "bf16"))
+    h8 = ep.EpHandle(cfg_of(wl, "fp8"), layout_of=h16)
+    wide = wl.with_(hidden=2 * wl.hidden)
+    hw = ep.EpHandle(cfg_of(wide, "bf16", use_weights=False), layout_of=h8)   # shares h16's
+    h16.layout(case["topk_idx"].cuda())
+    ref = ref_layout(wl, case["topk_idx"].numpy())
+    R, H = wl.recv_capacity, wl.hidden
+    recv8 = torch.zeros((R, H), dtype=torch.uint8, device="cuda")
+    scales = torch.zeros((R, H // 128), dtype=torch.float32, device="cuda")
+    h8.dispatch(case["x"], recv8, scales)
+    y = synth.gen_bf16_normal(R, 2 * H, seed=9, device="cuda")
+    out = torch.empty((wl.num_tokens, 2 * H), dtype=torch.bfloat16, device="cuda")
+    hw.combine(y, None, out)
+    torch.cuda.synchronize()
+    rq = np.zeros((R, H), np.uint8)
+    rs = np.zeros((R, H // 128), np.float32)
+    oracle.dispatch_fp8(synth.bits16(case["x"]), ref["dst_slot"], rq, rs)
+    assert np.array_equal(recv8.cpu().numpy(), rq)
+    assert np.array_equal(scales.cpu().numpy().view(np.uint32), rs.view(np.uint32))
+    assert np.array_equal(synth.bits16(out), oracle.combine(synth.bits16(y), ref["dst_slot"], None))
+    for f in (ep.FIELD_DST_SLOT, ep.FIELD_RECV_SRC_METADATA, ep.FIELD_PSUM_PER_EXPERT):
+        assert torch.equal(h8.field(f), h16.field(f)) and torch.equal(hw.field(f), h16.field(f))
+    assert h8.variant(0) == h16.variant(0)
+    assert h8.status() == 0
+    # the shared handle computes no layout of its own
+    with pytest.raises(ep.EpError) as e:
+        h8.layout(case["topk_idx"].cuda())
+    assert e.value.code == ep.EP_EINVAL
+    # a new routing on the owner is what the shared handles see next
+    topk2 = synth.gen_topk(wl.with_(seed=wl.seed + 5))
+    h16.layout(topk2.cuda())
+    h8.dispatch(case["x"], recv8, scales)
+    torch.cuda.synchronize()
+    ref2 = ref_layout(wl, topk2.numpy())
+    rq2 = np.zeros((R, H), np.uint8)
+    oracle.dispatch_fp8(synth.bits16(case["x"]), ref2["dst_slot"], rq2, np.zeros_like(rs))
+    got = recv8.cpu().numpy()
+    filled = ref2["meta"][:, 0] >= 0
+    assert np.array_equal(got[filled], rq2[filled])
+
+
+def test_shared_layout_rejects_a_different_routing_shape():
+    wl = synth.WORKLOADS["tiny"]
+    h = ep.EpHandle(cfg_of(wl))
+    for bad in (wl.with_(topk=2), wl.with_(alignment=4), wl.with_(world_size=2, max_tok_per_rank=64)):
+        with pytest.raises(ep.EpError) as e:
+            ep.EpHandle(cfg_of(bad), layout_of=h)
+        assert e.value.code == ep.EP_EINVAL
+    ne = ep.make_cfg(wl.world_size, wl.hidden, wl.max_tok_per_rank, wl.num_expert_per_rank,
+                     wl.topk, wl.alignment, "bf16", False, no_expand=True)
+    with pytest.raises(ep.EpError):
+        ep.EpHandle(ne, layout_of=h)
