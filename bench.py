@@ -21,6 +21,7 @@ import argparse
 import hashlib
 import json
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -186,6 +187,36 @@ class ClockSampler:
 
 # ------------------------------------------------------------- GPU arm
 
+def arm_config(wl, world):
+    """The `config` object of both arms' JSON lines."""
+    N = wl.num_tokens
+    return {"workload": WORKLOAD_DESC if N == 32768 else
+            WORKLOAD_DESC.replace("4096 tokens = 32768", "%d tokens = %d" % (N // 8, N)),
+            "tokens": N, "hidden": wl.hidden, "experts": wl.num_experts,
+            "world_size_logical": wl.world_size, "topk": wl.topk,
+            "expert_alignment": wl.alignment, "recv_capacity": wl.recv_capacity,
+            "step": "layout + dispatch bf16 + combine (identity experts) + dispatch fp8 "
+                    "(the FP8 handle shares the step's layout)",
+            "l2": "no flush: every step's inputs/outputs exceed L2 (x 470 MB, recv_x "
+                  "4.2 GB, recv_x fp8 2.1 GB)",
+            "parallelism": "replicas" if world > 1 else "single GPU"}
+
+
+def host_cpu():
+    """Model name of the host CPU and its hardware threads (for the CPU-baseline record)."""
+    model = platform.processor() or platform.machine()
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                key = line.split(":")[0].strip().lower()
+                if key in ("model name", "cpu part", "hardware"):
+                    model = line.split(":", 1)[1].strip()
+                    break
+    except OSError:
+        pass
+    return {"cpu_model": model, "host_threads": os.cpu_count()}
+
+
 def prefill_workload(tokens=None):
     """The prefill workload, or the same shape with fewer tokens (a smaller case
     for profiler captures: 8 logical ranks x tokens/8)."""
@@ -306,16 +337,7 @@ def run_ours(args, rank, local_rank, world):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded; shapes and distributions of the prefill workload)",
-        "config": {"workload": WORKLOAD_DESC if N == 32768 else
-                   WORKLOAD_DESC.replace("4096 tokens = 32768", "%d tokens = %d" % (N // 8, N)),
-                   "tokens": N, "hidden": H, "experts": wl.num_experts,
-                   "world_size_logical": wl.world_size, "topk": K,
-                   "expert_alignment": wl.alignment, "recv_capacity": R,
-                   "step": "layout + dispatch bf16 + combine (identity experts) + dispatch fp8 "
-                           "(the FP8 handle shares the step's layout)",
-                   "l2": "no flush: every step's inputs/outputs exceed L2 (x 470 MB, recv_x "
-                         "4.2 GB, recv_x fp8 2.1 GB)",
-                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "config": arm_config(wl, world),
         "tokens_per_s": round(toks / (ms * 1e-3), 1),
         "kernels": kernels,
         "roofline": roof,
@@ -517,48 +539,57 @@ def run_all_configs(args):
 
 # ------------------------------------------------------------- CPU oracle
 
-def oracle_step_sample(wl, topk_np, w_np, x_bits, tok0, ntok, bufs):
-    """One oracle pass of the step over tokens [tok0, tok0+ntok) of the prefill
-    workload (layout over the whole batch, the data movement over the sample).
-    Returns the algorithmic bytes it covered."""
+def oracle_bufs(wl, block):
+    """Receive buffers for one oracle sub-batch of `block` tokens."""
+    import numpy as np
     import oracle
+    R = oracle.recv_capacity(block, wl.topk, wl.num_experts, wl.alignment)
+    H = wl.hidden
+    return (np.zeros((R, H), np.uint16), np.zeros((R, H), np.uint8),
+            np.zeros((R, H // 128), np.float32))
+
+
+def oracle_step_sample(wl, topk_np, w_np, x_bits, tok0, ntok, bufs):
+    """One oracle pass of the whole step (layout, dispatch bf16, combine, dispatch
+    fp8) over the sub-batch of tokens [tok0, tok0+ntok) of the prefill workload,
+    taken as a batch of its own (ntok / W tokens per logical rank), so that the
+    layout and the data movement keep the step's per-token proportions.
+    Returns (algorithmic bytes, tokens)."""
+    import oracle
+    W = wl.world_size
+    tk = topk_np[tok0:tok0 + ntok]
     recv16, recv8, scales = bufs
-    lay = oracle.layout(topk_np, wl.world_size, wl.max_tok_per_rank, wl.num_expert_per_rank,
-                        wl.alignment)
-    sl = lay["dst_slot"][tok0:tok0 + ntok]
+    lay = oracle.layout(tk, W, ntok // W, wl.num_expert_per_rank, wl.alignment,
+                        rcap=recv16.shape[0])
+    sl = lay["dst_slot"]
     xs = x_bits[tok0:tok0 + ntok]
     oracle.dispatch_bf16(xs, sl, recv16)
     oracle.combine(recv16, sl, w_np[tok0:tok0 + ntok])
     oracle.dispatch_fp8(xs, sl, recv8, scales)
-    N, H, K = wl.num_tokens, wl.hidden, wl.topk
-    nb_full = algorithmic_bytes(N, H, K, wl.recv_capacity)
-    nb = algorithmic_bytes(ntok, H, K, 0)
-    return nb_full["layout"] + nb["dispatch_bf16"] + nb["combine"] + nb["dispatch_fp8"], ntok
+    nb = algorithmic_bytes(ntok, wl.hidden, wl.topk, lay["rcap"])
+    return nb["layout"] + nb["dispatch_bf16"] + nb["combine"] + nb["dispatch_fp8"], ntok
 
 
 def cpu_baseline(wl, topk_cpu, w_cpu, x, budget_s=15.0, block=512):
-    """The oracle as it stands (single-threaded C), on a bounded sample: blocks of
-    `block` tokens until ~budget_s seconds of CPU work."""
-    import numpy as np
-
+    """The oracle as it stands (single-threaded C), on a bounded sample: sub-batches
+    of `block` tokens until ~budget_s seconds of CPU work."""
     import synth
     x_bits = synth.bits16(x)
     topk_np, w_np = topk_cpu.numpy(), w_cpu.numpy()
-    R, H = wl.recv_capacity, wl.hidden
-    bufs = (np.zeros((R, H), np.uint16), np.zeros((R, H), np.uint8),
-            np.zeros((R, H // 128), np.float32))
+    bufs = oracle_bufs(wl, block)
     t0 = time.perf_counter()
     nbytes, ntoks, tok = 0, 0, 0
-    while time.perf_counter() - t0 < budget_s and tok < wl.num_tokens:
+    while time.perf_counter() - t0 < budget_s and tok + block <= wl.num_tokens:
         b, n = oracle_step_sample(wl, topk_np, w_np, x_bits, tok, block, bufs)
         nbytes += b
         ntoks += n
         tok += block
     dt = time.perf_counter() - t0
     return {"value": round(nbytes / dt / 1e9, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            **host_cpu(),
             "tokens_per_s": round(ntoks / dt, 1),
-            "sample": "%d of %d tokens in blocks of %d (each block: layout of the whole batch + "
-                      "dispatch bf16 + combine + dispatch fp8 of the block), %.1f s" %
+            "sample": "%d of %d tokens as sub-batches of %d (each: layout, dispatch bf16, "
+                      "combine, dispatch fp8 of the sub-batch), %.1f s" %
                       (ntoks, wl.num_tokens, block, dt)}
 
 
@@ -572,22 +603,22 @@ def run_reference(args, rank, world):
     wl = synth.WORKLOADS["prefill_bf16"]
     topk_cpu, w_cpu = synth.gen_topk(wl), synth.gen_weights(wl)
     block = args.ref_block
-    x = synth.gen_bf16_normal(block * max(1, args.steps + args.warmup), wl.hidden,
+    nblk = wl.num_tokens // block
+    # x for the sub-batches the run visits (cycling through the batch)
+    x = synth.gen_bf16_normal(block * min(nblk, args.steps + args.warmup), wl.hidden,
                               wl.seed * 16 + 3)
     x_bits = synth.bits16(x)
-    R, H = wl.recv_capacity, wl.hidden
-    bufs = (np.zeros((R, H), np.uint16), np.zeros((R, H), np.uint8),
-            np.zeros((R, H // 128), np.float32))
+    bufs = oracle_bufs(wl, block)
     topk_np, w_np = topk_cpu.numpy(), w_cpu.numpy()
-    xb_full = np.zeros((wl.num_tokens, H), np.uint16)
+    xb_full = np.zeros((wl.num_tokens, wl.hidden), np.uint16)
     xb_full[:x_bits.shape[0]] = x_bits
     for i in range(args.warmup):
-        oracle_step_sample(wl, topk_np, w_np, xb_full, i * block, block, bufs)
+        oracle_step_sample(wl, topk_np, w_np, xb_full, (i % nblk) * block, block, bufs)
     t0 = time.perf_counter()
     nbytes = ntok = 0
     for i in range(args.steps):
-        b, n = oracle_step_sample(wl, topk_np, w_np, xb_full, (args.warmup + i) * block, block,
-                                  bufs)
+        b, n = oracle_step_sample(wl, topk_np, w_np, xb_full, ((args.warmup + i) % nblk) * block,
+                                  block, bufs)
         nbytes += b
         ntok += n
     dt = time.perf_counter() - t0
@@ -596,10 +627,10 @@ def run_reference(args, rank, world):
             "warmup": args.warmup, "ms_per_step": round(dt / max(1, args.steps) * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic", "impl": "reference",
-            "config": {"workload": WORKLOAD_DESC,
-                       "sample": "each step: layout of the whole 32768-token batch + dispatch "
-                                 "bf16, combine and dispatch fp8 of %d tokens" % block},
-            "cpu_baseline": {"value": v, "unit": "GB/s", "kind": "oracle", "cores": 1,
+            "config": dict(arm_config(wl, 1),
+                           sample="each step: the whole path (layout, dispatch bf16, combine, "
+                                  "dispatch fp8) over a sub-batch of %d of the 32768 tokens" % block),
+            "cpu_baseline": {"value": v, "unit": "GB/s", "kind": "oracle", "cores": 1, **host_cpu(),
                              "sample": "%d tokens per step, %d steps, %.1f s" %
                                        (block, args.steps, dt)},
             "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
