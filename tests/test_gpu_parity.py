@@ -520,3 +520,58 @@ def test_small_batch_layout_both_paths(case, path, monkeypatch):
     topk2 = synth.gen_topk(wl.with_(seed=wl.seed + 1), mask_frac=0.1)
     h.layout(topk2.cuda())
     assert_layout_equal(gpu_fields(h), oracle_layout(wl, topk2.numpy()))
+
+
+def test_layout_multi_million_tokens():
+    # 2^22 tokens over 64 ranks: 32768 chunks, so each spine lane scans a run of
+    # 1024 chunks (the loop path), and receive rows exceed 2^23
+    wl = synth.WORKLOADS["tiny"].with_(world_size=64, max_tok_per_rank=65536,
+                                       num_tokens=1 << 22, num_expert_per_rank=2, topk=2,
+                                       alignment=4)
+    g = torch.Generator().manual_seed(11)
+    topk = torch.randint(-1, wl.num_experts, (wl.num_tokens, wl.topk), generator=g)
+    h, got, ref = layout_case(wl, topk)
+    assert_layout_equal(got, ref)
+    assert got["num_recv"] > 1 << 22
+    assert h.status() == 0
+
+
+@pytest.mark.parametrize("jit", ["1", "0"])
+@pytest.mark.parametrize("dtype", ["bf16", "fp8"])
+def test_largest_hidden(dtype, jit, monkeypatch):
+    # hidden 32768 (64 KB bf16 rows, the largest the library accepts), a ragged
+    # batch; the shape is outside the compiled table, so it runs the run-time
+    # specialisation or, with it switched off, the generic kernels
+    monkeypatch.setenv("EP_GB300_JIT", jit)
+    wl = synth.WORKLOADS["tiny"].with_(hidden=32768, num_tokens=96, dispatch_dtype=dtype)
+    case = synth.make_case(wl, device="cuda", mask_frac=0.1)
+    topk, w = case["topk_idx"], case["topk_weights"]
+    h = ep.EpHandle(cfg_of(wl))
+    h.layout(topk.cuda())
+    ref = oracle_layout(wl, topk.numpy())
+    R, H = wl.recv_capacity, wl.hidden
+    if dtype == "fp8":
+        recv = torch.zeros((R, H), dtype=torch.uint8, device="cuda")
+        scales = torch.zeros((R, H // 128), dtype=torch.float32, device="cuda")
+        h.dispatch(case["x"], recv, scales)
+        rq = np.zeros((R, H), np.uint8)
+        rs = np.zeros((R, H // 128), np.float32)
+        oracle.dispatch_fp8(synth.bits16(case["x"]), ref["dst_slot"], rq, rs)
+        torch.cuda.synchronize()
+        assert np.array_equal(recv.cpu().numpy(), rq)
+        assert np.array_equal(scales.cpu().numpy().view(np.uint32), rs.view(np.uint32))
+        y = synth.gen_y(wl, valid_rows=ref["meta"][:, 0] >= 0, device="cuda")
+    else:
+        y = torch.zeros((R, H), dtype=torch.bfloat16, device="cuda")
+        h.dispatch(case["x"], y)
+        rx = np.zeros((R, H), np.uint16)
+        oracle.dispatch_bf16(synth.bits16(case["x"]), ref["dst_slot"], rx)
+        torch.cuda.synchronize()
+        assert np.array_equal(synth.bits16(y), rx)
+    out = torch.empty((wl.num_tokens, H), dtype=torch.bfloat16, device="cuda")
+    h.combine(y, w.cuda(), out)
+    torch.cuda.synchronize()
+    assert np.array_equal(synth.bits16(out), oracle.combine(synth.bits16(y), ref["dst_slot"],
+                                                            w.numpy()))
+    assert h.status() == 0
+    assert ("_generic" in h.variant(1)) == (jit == "0")
