@@ -534,7 +534,8 @@ def run_all_configs(args):
                 "steps": args.steps, "peak_gbs": peak, "peak_kind": peak_kind}
         for k, b in (("layout", nb["layout"]), ("dispatch", nb[dkey]), ("combine", nb["combine"])):
             us = statistics.median(times[k])
-            line[k] = {"us_median": round(us, 2), "us_min": round(min(times[k]), 2),
+            line[k] = {"us_median": round(us, 2), "us_mean": round(statistics.mean(times[k]), 2),
+                       "us_min": round(min(times[k]), 2),
                        "us_max": round(max(times[k]), 2), "algorithmic_bytes": b,
                        "gbs": round(b / (us * 1e-6) / 1e9, 1),
                        "frac_of_peak": round(b / (us * 1e-6) / 1e9 / peak, 4),

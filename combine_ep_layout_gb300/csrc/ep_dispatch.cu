@@ -26,9 +26,14 @@
 // Optionally each destination row also receives the routing it came with
 // (its expert id and the token's weight for it), as the pages' dispatch copy
 // epilogue fills recv_topk_idx / recv_topk_weights.
+//
+// Small batches split each row over two CTAs (the geometry table below), so
+// that a batch that fills less than a wave of the GPU still keeps every SM's
+// loads and stores in flight.
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <cstdlib>
 
 #include "ep_cfg.hpp"
 #include "ep_dispatch_body.cuh"
@@ -38,14 +43,44 @@ namespace epg {
 
 namespace {
 
-template <int RB, int KC, int V>
-__global__ void __launch_bounds__(CopyThreads(RB, V)) ep_dispatch_copy_kernel(DispatchParams p) {
-  dispatch_copy_body<RB, KC, V>(p);
+template <int RB, int KC, int V, int S>
+__global__ void __launch_bounds__(CopyThreads(RB, V, S)) ep_dispatch_copy_kernel(DispatchParams p) {
+  dispatch_copy_body<RB, KC, V, S>(p);
 }
 
-template <int HC, int KC, int V>
-__global__ void __launch_bounds__(Fp8Threads(HC, V)) ep_dispatch_fp8_kernel(DispatchParams p) {
-  dispatch_fp8_body<HC, KC, V>(p);
+template <int HC, int KC, int V, int S>
+__global__ void __launch_bounds__(Fp8Threads(HC, V, S)) ep_dispatch_fp8_kernel(DispatchParams p) {
+  dispatch_fp8_body<HC, KC, V, S>(p);
+}
+
+// ---- geometry tuning table ---------------------------------------------------
+//
+// Token-count buckets -> CTAs per token row for the compiled row kernels ("MORI
+// JIT v2" §5.1: a geometry table per kernel keyed by the number of tokens).  From
+// a sweep on GB300 at hidden 7168, top-8, cold buffers: splitting each row over
+// two CTAs moved 1024 tokens in 23.4 us instead of 24.4 us and 2048 tokens in
+// 44.0 us instead of 44.9 us; from 8192 tokens on one CTA per row is as fast
+// (162 us either way; at 32768 tokens within 0.5 %).  Combine has one geometry:
+// none of the sweep's alternatives beat it.
+struct SliceBucket {
+  int max_tokens;
+  int slices;
+};
+constexpr SliceBucket kDispatchSlices[] = {{2048, 2}, {1 << 30, 1}};
+
+inline int row_slices(int num_tokens, const LaunchGeom& g) {
+  if (g.row_slices > 0) return g.row_slices;
+  for (const SliceBucket& b : kDispatchSlices)
+    if (num_tokens <= b.max_tokens) return b.slices;
+  return 1;
+}
+
+// EP_GB300_DISPATCH_SLICES=1|2 pins the table's choice (for benchmarking).
+inline int slices_override() {
+  const char* env = std::getenv("EP_GB300_DISPATCH_SLICES");
+  if (env == nullptr) return 0;
+  const int v = std::atoi(env);
+  return v == 1 || v == 2 ? v : 0;
 }
 
 // CTA size of the loop path: enough threads for `per_iter` vectors per thread
@@ -60,50 +95,68 @@ inline int loop_block(int chunks, int per_iter) {
 
 inline bool aligned32(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 31u) == 0; }
 
-template <int RB, int KC, int V>
+template <int RB, int KC, int V, int S>
 int copy_block(int row_bytes) {
-  constexpr int T = RB ? RowThreads(RB / (4 * V)) : 0;
+  constexpr int T = RB ? RowThreads(RB / (4 * V) / S) : 0;
   return T ? T : loop_block(row_bytes / (4 * V), 2);
 }
 
 template <int RB, int KC>
-cudaError_t launch_copy(const DispatchParams& p, const LaunchGeom&, cudaStream_t s) {
+cudaError_t launch_copy(const DispatchParams& p, const LaunchGeom& g, cudaStream_t s) {
   if (p.num_tokens == 0) return cudaSuccess;
   // 32-byte vectors when every row start is 32-byte aligned
-  if (p.row_bytes % 32 == 0 && aligned32(p.x) && aligned32(p.recv_x))
-    ep_dispatch_copy_kernel<RB, KC, 8><<<p.num_tokens, copy_block<RB, KC, 8>(p.row_bytes), 0, s>>>(p);
-  else
-    ep_dispatch_copy_kernel<RB, KC, 4><<<p.num_tokens, copy_block<RB, KC, 4>(p.row_bytes), 0, s>>>(p);
+  if (p.row_bytes % 32 == 0 && aligned32(p.x) && aligned32(p.recv_x)) {
+    if constexpr (RB != 0 && Splittable(RB / 32, 1, 2)) {
+      if (row_slices(p.num_tokens, g) == 2) {
+        ep_dispatch_copy_kernel<RB, KC, 8, 2>
+            <<<2 * p.num_tokens, copy_block<RB, KC, 8, 2>(p.row_bytes), 0, s>>>(p);
+        return cudaGetLastError();
+      }
+    }
+    ep_dispatch_copy_kernel<RB, KC, 8, 1><<<p.num_tokens, copy_block<RB, KC, 8, 1>(p.row_bytes), 0, s>>>(p);
+  } else {
+    ep_dispatch_copy_kernel<RB, KC, 4, 1><<<p.num_tokens, copy_block<RB, KC, 4, 1>(p.row_bytes), 0, s>>>(p);
+  }
   return cudaGetLastError();
 }
 
 template <int RB, int KC>
 cudaError_t prepare_copy(int, int, int, LaunchGeom* g) {
+  g->row_slices = slices_override();
   return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-      &g->blocks_per_sm, ep_dispatch_copy_kernel<RB, KC, 8>, kRowMaxThreads, 0);
+      &g->blocks_per_sm, ep_dispatch_copy_kernel<RB, KC, 8, 1>, kRowMaxThreads, 0);
 }
 
-template <int HC, int KC, int V>
+template <int HC, int KC, int V, int S>
 int fp8_block(int hidden) {
-  constexpr int T = HC ? RowThreads(2 * HC / (4 * V)) : 0;
+  constexpr int T = HC ? RowThreads(2 * HC / (4 * V) / S) : 0;
   return T ? T : loop_block(2 * hidden / (4 * V), 1);
 }
 
 template <int HC, int KC>
-cudaError_t launch_fp8(const DispatchParams& p, const LaunchGeom&, cudaStream_t s) {
+cudaError_t launch_fp8(const DispatchParams& p, const LaunchGeom& g, cudaStream_t s) {
   if (p.num_tokens == 0) return cudaSuccess;
   // hidden % 128 == 0 here, so 32-byte input vectors only need an aligned x
-  if (aligned32(p.x))
-    ep_dispatch_fp8_kernel<HC, KC, 8><<<p.num_tokens, fp8_block<HC, KC, 8>(p.hidden), 0, s>>>(p);
-  else
-    ep_dispatch_fp8_kernel<HC, KC, 4><<<p.num_tokens, fp8_block<HC, KC, 4>(p.hidden), 0, s>>>(p);
+  if (aligned32(p.x)) {
+    if constexpr (HC != 0 && Splittable(2 * HC / 32, 128 / 16, 2)) {
+      if (row_slices(p.num_tokens, g) == 2) {
+        ep_dispatch_fp8_kernel<HC, KC, 8, 2>
+            <<<2 * p.num_tokens, fp8_block<HC, KC, 8, 2>(p.hidden), 0, s>>>(p);
+        return cudaGetLastError();
+      }
+    }
+    ep_dispatch_fp8_kernel<HC, KC, 8, 1><<<p.num_tokens, fp8_block<HC, KC, 8, 1>(p.hidden), 0, s>>>(p);
+  } else {
+    ep_dispatch_fp8_kernel<HC, KC, 4, 1><<<p.num_tokens, fp8_block<HC, KC, 4, 1>(p.hidden), 0, s>>>(p);
+  }
   return cudaGetLastError();
 }
 
 template <int HC, int KC>
 cudaError_t prepare_fp8(int, int, int, LaunchGeom* g) {
+  g->row_slices = slices_override();
   return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-      &g->blocks_per_sm, ep_dispatch_fp8_kernel<HC, KC, 8>, kRowMaxThreads, 0);
+      &g->blocks_per_sm, ep_dispatch_fp8_kernel<HC, KC, 8, 1>, kRowMaxThreads, 0);
 }
 
 }  // namespace

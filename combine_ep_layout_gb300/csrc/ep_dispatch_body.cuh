@@ -43,14 +43,22 @@ __device__ __forceinline__ void store(void* p, const Vec<V>& r) {
 // ---- geometry ----------------------------------------------------------------
 
 // Threads per CTA of the copy kernel (RB row bytes, V words per vector) and of
-// the FP8 kernel (HC channels); 0 row bytes / channels: the runtime-shape
-// variant, kRowMaxThreads threads walking the row in a loop.
-constexpr int CopyThreads(int rb, int v) {
-  return rb ? (RowThreads(rb / (4 * v)) ? RowThreads(rb / (4 * v)) : kRowMaxThreads) : kRowMaxThreads;
-}
-constexpr int Fp8Threads(int hc, int v) {
-  return hc ? (RowThreads(2 * hc / (4 * v)) ? RowThreads(2 * hc / (4 * v)) : kRowMaxThreads)
+// the FP8 kernel (HC channels) when each row is split over S CTAs; 0 row bytes /
+// channels: the runtime-shape variant, kRowMaxThreads threads walking the row
+// in a loop.
+constexpr int CopyThreads(int rb, int v, int s = 1) {
+  return rb ? (RowThreads(rb / (4 * v) / s) ? RowThreads(rb / (4 * v) / s) : kRowMaxThreads)
             : kRowMaxThreads;
+}
+constexpr int Fp8Threads(int hc, int v, int s = 1) {
+  return hc ? (RowThreads(2 * hc / (4 * v) / s) ? RowThreads(2 * hc / (4 * v) / s) : kRowMaxThreads)
+            : kRowMaxThreads;
+}
+
+// A row of `vectors` vectors can be split over s CTAs when each slice is a
+// whole number of `unit`-vector groups held by a compile-time geometry.
+constexpr bool Splittable(int vectors, int unit, int s) {
+  return vectors > 0 && vectors % (s * unit) == 0 && RowThreads(vectors / s) != 0;
 }
 
 // Forward the routing with the rows (the dispatch copy epilogue's
@@ -86,31 +94,35 @@ __device__ __forceinline__ void forward_routing(const DispatchParams& p, int t, 
 
 // ---- copy (bf16, fp32 and packed-fp4 transports) ------------------------------
 
-template <int RB, int KC, int V>
+// S > 1 (compiled row geometries only): each row is split into S contiguous
+// slices, CTA b copying slice b % S of token b / S.
+template <int RB, int KC, int V, int S = 1>
 __device__ __forceinline__ void dispatch_copy_body(const DispatchParams& p) {
   constexpr int UNIT = 4 * V;  // bytes per vector
   constexpr int KM = KC ? KC : kMaxTopk;
   const int K = KC ? KC : p.topk;
   const int row = RB ? RB : p.row_bytes;
-  const int t = blockIdx.x;
+  const int t = S == 1 ? static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.x) / S;
   const uint8_t* xr = static_cast<const uint8_t*>(p.x) + static_cast<int64_t>(t) * row;
   uint8_t* rx = static_cast<uint8_t*>(p.recv_x);
   const int32_t* sl = p.dst_slot + static_cast<int64_t>(t) * K;
 
-  constexpr int CH = RB ? RB / UNIT : 0;
+  constexpr int CH = RB ? RB / UNIT / S : 0;  // vectors of this CTA's slice
   constexpr int T = RB ? RowThreads(CH) : 0;
+  static_assert(S == 1 || (RB != 0 && Splittable(RB / UNIT, 1, S)), "row slices need a compiled geometry");
   if constexpr (T != 0) {
     constexpr int PER = CH / T;
+    const int64_t base = S == 1 ? 0 : static_cast<int64_t>(blockIdx.x % S) * CH * UNIT;
     Vec<V> v[PER];
 #pragma unroll
     for (int u = 0; u < PER; ++u)
-      load_stream<V>(xr + static_cast<int64_t>(threadIdx.x + u * T) * UNIT, v[u]);
+      load_stream<V>(xr + base + static_cast<int64_t>(threadIdx.x + u * T) * UNIT, v[u]);
 #pragma unroll
     for (int k = 0; k < KM; ++k) {
       if (k >= K) break;
       const int32_t d = __ldg(sl + k);
       if (d < 0) continue;
-      uint8_t* dr = rx + static_cast<int64_t>(d) * row;
+      uint8_t* dr = rx + static_cast<int64_t>(d) * row + base;
 #pragma unroll
       for (int u = 0; u < PER; ++u) store<V>(dr + static_cast<int64_t>(threadIdx.x + u * T) * UNIT, v[u]);
     }
@@ -134,7 +146,7 @@ __device__ __forceinline__ void dispatch_copy_body(const DispatchParams& p) {
       }
     }
   }
-  forward_routing(p, t, K, sl);
+  if (S == 1 || blockIdx.x % S == 0) forward_routing(p, t, K, sl);
 }
 
 // ---- FP8 --------------------------------------------------------------------
@@ -195,7 +207,9 @@ __device__ __forceinline__ void store_q(void* p, const uint32_t (&q)[V / 2]) {
   }
 }
 
-template <int HC, int KC, int V>
+// S > 1 (compiled geometries only): each row is split into S slices of whole
+// 128-channel groups, CTA b quantising slice b % S of token b / S.
+template <int HC, int KC, int V, int S = 1>
 __device__ __forceinline__ void dispatch_fp8_body(const DispatchParams& p) {
   constexpr int UNIT = 4 * V;            // input bytes per vector (2V channels)
   constexpr int LANES = 128 / (2 * V);   // lanes per 128-channel group
@@ -203,21 +217,24 @@ __device__ __forceinline__ void dispatch_fp8_body(const DispatchParams& p) {
   const int H = HC ? HC : p.hidden;
   const int K = KC ? KC : p.topk;
   const int G = H / kScaleGroup;
-  const int t = blockIdx.x;
+  const int t = S == 1 ? static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.x) / S;
   const uint8_t* xr = static_cast<const uint8_t*>(p.x) + static_cast<int64_t>(t) * 2 * H;
   uint8_t* rq = static_cast<uint8_t*>(p.recv_x);
   float* rs = p.recv_scales;
   const int32_t* sl = p.dst_slot + static_cast<int64_t>(t) * K;
   const bool leader = (threadIdx.x % LANES) == 0;
 
-  constexpr int CH = HC ? 2 * HC / UNIT : 0;
+  constexpr int CH = HC ? 2 * HC / UNIT / S : 0;  // vectors of this CTA's slice
   constexpr int T = HC ? RowThreads(CH) : 0;
+  static_assert(S == 1 || (HC != 0 && Splittable(2 * HC / UNIT, LANES, S)),
+                "row slices need a compiled geometry of whole scale groups");
   if constexpr (T != 0) {
     constexpr int PER = CH / T;
+    const int c0 = S == 1 ? 0 : static_cast<int>(blockIdx.x % S) * CH;  // first vector of the slice
     Vec<V> v[PER];
 #pragma unroll
     for (int u = 0; u < PER; ++u)
-      load_stream<V>(xr + static_cast<int64_t>(threadIdx.x + u * T) * UNIT, v[u]);
+      load_stream<V>(xr + static_cast<int64_t>(c0 + threadIdx.x + u * T) * UNIT, v[u]);
     uint32_t q[PER][V / 2];
     float s[PER];
 #pragma unroll
@@ -229,7 +246,7 @@ __device__ __forceinline__ void dispatch_fp8_body(const DispatchParams& p) {
       if (d < 0) continue;
 #pragma unroll
       for (int u = 0; u < PER; ++u) {
-        const int c = threadIdx.x + u * T;
+        const int c = c0 + threadIdx.x + u * T;
         store_q<V>(rq + static_cast<int64_t>(d) * H + static_cast<int64_t>(c) * (2 * V), q[u]);
         if (leader) rs[static_cast<int64_t>(d) * G + c / LANES] = s[u];
       }
@@ -259,7 +276,7 @@ __device__ __forceinline__ void dispatch_fp8_body(const DispatchParams& p) {
       }
     }
   }
-  forward_routing(p, t, K, sl);
+  if (S == 1 || blockIdx.x % S == 0) forward_routing(p, t, K, sl);
 }
 
 }  // namespace epg

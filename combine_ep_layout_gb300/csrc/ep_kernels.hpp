@@ -52,6 +52,7 @@ struct LaunchGeom {
   int num_sms;        // SMs of the device
   int blocks_per_sm;  // resident CTAs per SM for the variant's block and shared memory
   int cluster_ok;     // layout: the single-launch cluster kernel can be scheduled
+  int row_slices;     // dispatch: CTAs per token row forced by EP_GB300_DISPATCH_SLICES (0: table)
 };
 
 using LayoutLaunch = cudaError_t (*)(const LayoutParams&, const LaunchGeom&, cudaStream_t);

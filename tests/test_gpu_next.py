@@ -226,3 +226,50 @@ def test_shared_layout_rejects_a_different_routing_shape():
                      wl.topk, wl.alignment, "bf16", False, no_expand=True)
     with pytest.raises(ep.EpError):
         ep.EpHandle(ne, layout_of=h)
+
+
+# The dispatch geometry table splits each row over two CTAs for batches of up to
+# 2048 tokens; EP_GB300_DISPATCH_SLICES (read when the handle is built) pins the
+# choice, so both geometries are checked on small and large batches.
+@pytest.mark.parametrize("slices", ["1", "2"])
+@pytest.mark.parametrize("name,dtype", [("decode", "bf16"), ("decode", "fp8"), ("skewed", "bf16"),
+                                        ("tiny", "fp32"), ("tiny", "fp8")])
+def test_dispatch_row_slices(name, dtype, slices, monkeypatch):
+    monkeypatch.setenv("EP_GB300_DISPATCH_SLICES", slices)
+    wl = synth.WORKLOADS[name]
+    case = synth.make_case(wl, device="cuda", mask_frac=0.05)
+    topk, w = case["topk_idx"], case["topk_weights"]
+    h = ep.EpHandle(cfg_of(wl, dtype))
+    h.layout(topk.cuda())
+    ref = ref_layout(wl, topk.numpy())
+    R, H = wl.recv_capacity, wl.hidden
+    rw = torch.full((R,), -3.0, device="cuda")
+    ri = torch.full((R,), -9, dtype=torch.int32, device="cuda")
+    want_w = np.full(R, -3.0, np.float32)
+    want_i = np.full(R, -9, np.int32)
+    oracle.forward_routing(topk.numpy(), w.numpy(), ref["dst_slot"], want_w, want_i)
+    if dtype == "fp8":
+        recv = torch.zeros((R, H), dtype=torch.uint8, device="cuda")
+        scales = torch.zeros((R, H // 128), dtype=torch.float32, device="cuda")
+        h.dispatch(case["x"], recv, scales, w.cuda(), rw, ri)
+        rq = np.zeros((R, H), np.uint8)
+        rs = np.zeros((R, H // 128), np.float32)
+        oracle.dispatch_fp8(synth.bits16(case["x"]), ref["dst_slot"], rq, rs)
+        torch.cuda.synchronize()
+        assert np.array_equal(recv.cpu().numpy(), rq)
+        assert np.array_equal(scales.cpu().numpy().view(np.uint32), rs.view(np.uint32))
+    else:
+        rb = 2 * H if dtype == "bf16" else 4 * H
+        x = case["x"] if dtype == "bf16" else torch.randint(
+            0, 256, (wl.num_tokens, rb), dtype=torch.uint8, device="cuda",
+            generator=torch.Generator(device="cuda").manual_seed(4)).view(torch.float32)
+        recv = torch.full((R, rb), 0x5A, dtype=torch.uint8, device="cuda")
+        h.dispatch(x, recv.view(torch.bfloat16) if dtype == "bf16" else recv.view(torch.float32),
+                   None, w.cuda(), rw, ri)
+        want = np.full((R, rb), 0x5A, np.uint8)
+        oracle.dispatch_bytes(x.contiguous().view(torch.uint8).cpu().numpy(), ref["dst_slot"], want)
+        torch.cuda.synchronize()
+        assert np.array_equal(recv.cpu().numpy(), want)
+    assert np.array_equal(rw.cpu().numpy().view(np.uint32), want_w.view(np.uint32))
+    assert np.array_equal(ri.cpu().numpy(), want_i)
+    assert h.status() == 0
