@@ -171,6 +171,49 @@ __device__ void block_exclusive_scan(const int32_t* v, int n, int A, int32_t* ou
   __syncthreads();
 }
 
+// Exclusive scan of align(v[e], A) for e in [0, n) by one warp (ceil(n/32)
+// consecutive values per lane) into out[0..n] (out[n] = total).
+__device__ __forceinline__ void warp_exclusive_scan(const int32_t* v, int n, int A, int32_t* out) {
+  const int lane = threadIdx.x & 31;
+  const int V = (n + 31) / 32;
+  const int beg = min(n, lane * V), end = min(n, beg + V);
+  int sum = 0;
+  for (int e = beg; e < end; ++e) sum += (v[e] + A - 1) / A * A;
+  int incl = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  int run = incl - sum;
+  for (int e = beg; e < end; ++e) {
+    out[e] = run;
+    run += (v[e] + A - 1) / A * A;
+  }
+  if (lane == 31) out[n] = incl;
+}
+
+// Expert counts up to this many are scanned by single warps (no block barriers
+// inside the scan); larger ones by the whole block.
+constexpr int kWarpScanMax = 512;
+
+// The two exclusive scans over the E experts: align(a[e], A) into out_a and,
+// when b is non-null, b[e] into out_b (E+1 outputs each).  All threads call;
+// the results are visible to the whole CTA on return.  For E <= kWarpScanMax
+// warps 0 and 1 scan one array each, at the same time, behind one barrier.
+__device__ void expert_scans(const int32_t* a, int A, int32_t* out_a, const int32_t* b,
+                             int32_t* out_b, int E, int32_t* warp_tot) {
+  if (E <= kWarpScanMax) {
+    const int warp = threadIdx.x >> 5;
+    if (warp == 0) warp_exclusive_scan(a, E, A, out_a);
+    else if (warp == 1 && b != nullptr) warp_exclusive_scan(b, E, 1, out_b);
+    __syncthreads();
+  } else {
+    block_exclusive_scan(a, E, A, out_a, warp_tot);
+    if (b != nullptr) block_exclusive_scan(b, E, 1, out_b, warp_tot);
+  }
+}
+
 // Exclusive scan of v[r] over r < n <= 64 by one warp (two values per lane)
 // into out[0..n] (out[n] = total).
 __device__ __forceinline__ void warp_scan64(const int32_t* v, int n, int32_t* out) {
@@ -410,7 +453,9 @@ __device__ void slots_expand_tokens(const LayoutParams& p, int t0, int ntok, con
   __syncthreads();
 
   // metadata rows of this range, in (expert, rank) order: flat words f of the
-  // concatenated rows; rows of one expert are contiguous in memory.
+  // concatenated rows; rows of one expert are contiguous in memory, so
+  // consecutive threads write consecutive words.  (One row per thread instead
+  // measured 29% slower at prefill: the stores lose their coalescing.)
   const int nvalid = cx[E];
   if ((KW & 1) == 0) {
     // even row width: word pairs (8-byte stores; rows start 8-byte aligned)
@@ -481,11 +526,11 @@ __global__ void __launch_bounds__(kSlotThreads) ep_layout_slots_kernel(LayoutPar
     }
   }
   __syncthreads();
-  // the aligned exclusive prefix over experts (every CTA; E values)
-  block_exclusive_scan(cnt_s, E, p.alignment, psum_s, warp_tot);
+  // the aligned exclusive prefix over experts (every CTA; E values) and the
+  // scan of this chunk's counts
+  expert_scans(cnt_s, p.alignment, psum_s, has_tokens ? cl : nullptr, cx, E, warp_tot);
   if (c == 0) write_outputs_expand(p, cnt_s, psum_s, p.col_total + E);
   if (has_tokens) {  // uniform per CTA
-    block_exclusive_scan(cl, E, 1, cx, warp_tot);
     const int t0 = c * kLayoutTPC;
     const int ntok = min(p.num_tokens, t0 + kLayoutTPC) - t0;
     slots_expand_tokens<KC>(p, t0, ntok, psum_s, co, cx, p.dst_slot + static_cast<int64_t>(t0) * K,
@@ -607,6 +652,7 @@ __device__ void slots_nonexpand_tokens(const LayoutParams& p, int t0, int ntok, 
 __device__ void write_outputs_nonexpand(const LayoutParams& p, const int32_t* cnt_s, int32_t* psum_s,
                                         const int32_t* prank, const int32_t* tpr, int32_t* warp_tot) {
   const int E = p.num_experts, W = p.world_size;
+  // one scan on one CTA: the whole block is faster than a single warp here
   block_exclusive_scan(cnt_s, E, p.alignment, psum_s, warp_tot);
   for (int e = threadIdx.x; e <= E; e += blockDim.x) {
     p.psum_expert[e] = psum_s[e];
@@ -733,11 +779,17 @@ __global__ void __launch_bounds__(kClusterThreads) ep_layout_cluster_kernel(Layo
   cluster_arrive();
   cluster_wait();
   for (int j = threadIdx.x; j < EW; j += kClusterThreads) {
+    int v[kClusterCtas];
+#pragma unroll
+    for (int b = 0; b < kClusterCtas; ++b)  // all remote loads in flight together
+      v[b] = b >= static_cast<int>(ncta) ? 0
+           : b == static_cast<int>(me)   ? colcnt[j]
+                                         : ld_cluster_shared(colcnt + j, static_cast<uint32_t>(b));
     int t = 0, o = 0;
-    for (uint32_t b = 0; b < ncta; ++b) {
-      const int v = b == me ? colcnt[j] : ld_cluster_shared(colcnt + j, b);
-      o += b < me ? v : 0;
-      t += v;
+#pragma unroll
+    for (int b = 0; b < kClusterCtas; ++b) {
+      o += b < static_cast<int>(me) ? v[b] : 0;
+      t += v[b];
     }
     tot[j] = t;
     off[j] = o;
@@ -746,9 +798,8 @@ __global__ void __launch_bounds__(kClusterThreads) ep_layout_cluster_kernel(Layo
   __syncthreads();
 
   if constexpr (!NE) {
-    block_exclusive_scan(tot, E, p.alignment, psum_s, warp_tot);
+    expert_scans(tot, p.alignment, psum_s, colcnt, cx, E, warp_tot);
     if (me == 0) write_outputs_expand(p, tot, psum_s, tot + E);
-    block_exclusive_scan(colcnt, E, 1, cx, warp_tot);
     slots_expand_tokens<KC>(p, t0, ntok, psum_s, off, cx, loc, ids, slots_s, sorted, src);
     fill_unreceived(p, psum_s, tot, psum_s[E], static_cast<int>(me), static_cast<int>(ncta));
   } else {
