@@ -206,6 +206,13 @@ def host_cpu():
     """Model name of the host CPU and its hardware threads (for the CPU-baseline record)."""
     model = platform.processor() or platform.machine()
     try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name:"):
+                return {"cpu_model": line.split(":", 1)[1].strip(), "host_threads": os.cpu_count()}
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
         with open("/proc/cpuinfo") as f:
             for line in f:
                 key = line.split(":")[0].strip().lower()
