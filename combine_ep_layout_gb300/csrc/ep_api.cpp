@@ -156,26 +156,6 @@ int check_device(const ep_handle* h) {
   return EP_OK;
 }
 
-}  // namespace
-
-extern "C" {
-
-int64_t ep_recv_capacity(const ep_cfg_t* cfg) noexcept {
-  try {
-    int rc = validate(cfg);
-    if (rc != EP_OK && rc != EP_EUNSUPPORTED) return rc;
-    return recv_rows(cfg);
-  } catch (const std::exception& ex) {
-    return fail(EP_EINVAL, ex.what());
-  } catch (...) {
-    return fail(EP_EINVAL, "unknown exception");
-  }
-}
-
-}  // extern "C"
-
-namespace {
-
 // ep_handle_create (src null) and ep_handle_create_shared (src: the handle
 // whose layout the new one uses; nothing of the layout is allocated).
 int create_handle(const ep_cfg_t* cfg, ep_handle* src, ep_handle_t* out) {
@@ -291,6 +271,18 @@ int create_handle(const ep_cfg_t* cfg, ep_handle* src, ep_handle_t* out) {
 }  // namespace
 
 extern "C" {
+
+int64_t ep_recv_capacity(const ep_cfg_t* cfg) noexcept {
+  try {
+    int rc = validate(cfg);
+    if (rc != EP_OK && rc != EP_EUNSUPPORTED) return rc;
+    return recv_rows(cfg);
+  } catch (const std::exception& ex) {
+    return fail(EP_EINVAL, ex.what());
+  } catch (...) {
+    return fail(EP_EINVAL, "unknown exception");
+  }
+}
 
 int ep_handle_create(const ep_cfg_t* cfg, ep_handle_t* out) noexcept {
   return create_handle(cfg, nullptr, out);
