@@ -47,6 +47,7 @@ struct DeviceSetup {
   cudaError_t err = cudaSuccess;
   int32_t* scratch = nullptr;  // device address of g_noalloc_scratch on this device
   int num_sms = 0;
+  int cluster_ok = 1;          // every layout variant can run its single-launch cluster kernel
 };
 
 DeviceSetup g_setup[kNoAllocMaxDevices];
@@ -70,6 +71,7 @@ void setup_device(DeviceSetup* s) {
       s->err = e;
       return;
     }
+    s->cluster_ok &= g.cluster_ok;
   }
   s->scratch = static_cast<int32_t*>(p);
 }
@@ -153,7 +155,7 @@ extern "C" int ep_layout_noalloc(const ep_cfg_t* cfg, const int64_t* topk_idx, i
     p.err = device_error;
     p.epr_magic = RankMagic(cfg->num_expert_per_rank);
     BindLayoutScratch(&p, s->scratch, Cs, cols);
-    const LaunchGeom g{s->num_sms, 1};
+    const LaunchGeom g{s->num_sms, 1, s->cluster_ok, 0};
     if ((e = FindLayout(K, false).launch(p, g, st)) != cudaSuccess) return err_cuda(e, "layout launch");
     return EP_OK;
   } catch (...) {

@@ -211,7 +211,8 @@ int ep_combine(ep_handle_t h, const void *y, const float *topk_weights, void *ou
  * writes the same outputs as ep_layout (same definitions, same bytes) into
  * buffers the caller passes, and keeps its scratch in a fixed 1 MiB array
  * compiled into the library (held by every GPU that loads the library until
- * the process exits).
+ * the process exits).  Batches of up to 2048 tokens run the single-launch
+ * cluster layout, which needs no scratch at all.
  *   cfg                       as for ep_handle_create (dispatch_dtype,
  *                             hidden_dim and use_weights are checked but unused;
  *                             no_expand = 1 returns EP_EUNSUPPORTED)

@@ -54,8 +54,11 @@ PAIRS = [
 
 @pytest.mark.gpu
 def test_noalloc_layout_matches_the_allocating_layout_on_two_calls_in_a_row(gpu):
-    calls = [synth.WORKLOADS["prefill_bf16"], synth.WORKLOADS["skewed"]]
-    for wl in calls:                       # call 1, then call 2 on the same static scratch
+    # small batches run the single-launch cluster kernel, large ones the three
+    # launches that use the static scratch
+    calls = [synth.WORKLOADS["decode"], synth.WORKLOADS["prefill_bf16"], synth.WORKLOADS["skewed"],
+             synth.WORKLOADS["decode"].with_(num_tokens=1000, alignment=16)]
+    for wl in calls:                       # one call after another on the same static scratch
         topk = synth.gen_topk(wl, mask_frac=0.01).cuda()
         out = noalloc_outputs(wl, wl.num_tokens)
         ep.ep_layout_noalloc(cfg_of(wl), topk, out)
