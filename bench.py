@@ -492,7 +492,9 @@ def run_all_configs(args):
     peak, peak_kind = measured_peaks()
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     s = torch.cuda.Stream(device=dev)
-    for name, wl, ne in [(n, w, ne) for ne in (False, True) for n, w in synth.WORKLOADS.items()]:
+    only = set(args.workload.split(",")) if args.workload else None
+    for name, wl, ne in [(n, w, ne) for ne in (False, True) for n, w in synth.WORKLOADS.items()
+                         if only is None or n in only]:
         N, H, K = wl.num_tokens, wl.hidden, wl.topk
         cfg = ep.make_cfg(wl.world_size, H, wl.max_tok_per_rank, wl.num_expert_per_rank, K,
                           wl.alignment, wl.dispatch_dtype, wl.use_weights and not ne, no_expand=ne)
@@ -669,6 +671,8 @@ def main(argv=None):
                     help="tokens of a smaller case of the prefill shape (profiling only)")
     ap.add_argument("--all-configs", action="store_true",
                     help="time layout / dispatch / combine on every workload (one line each)")
+    ap.add_argument("--workload", default=None,
+                    help="with --all-configs: comma-separated workload names (default: all)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

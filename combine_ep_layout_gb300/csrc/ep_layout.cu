@@ -118,6 +118,11 @@ __device__ __forceinline__ void cluster_arrive() {
 __device__ __forceinline__ void cluster_wait() {
   asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
+// Arrive without releasing anything: for a signal that publishes no writes
+// (no fence on the way).
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
 
 // Load the int32 at the same shared-memory offset as `local` in CTA `rank` of
 // the cluster (distributed shared memory).
@@ -195,7 +200,7 @@ __device__ __forceinline__ void warp_exclusive_scan(const int32_t* v, int n, int
 
 // Expert counts up to this many are scanned by single warps (no block barriers
 // inside the scan); larger ones by the whole block.
-constexpr int kWarpScanMax = 512;
+constexpr int kWarpScanMax = 128;
 
 // The two exclusive scans over the E experts: align(a[e], A) into out_a and,
 // when b is non-null, b[e] into out_b (E+1 outputs each).  All threads call;
@@ -646,14 +651,12 @@ __device__ void slots_nonexpand_tokens(const LayoutParams& p, int t0, int ntok, 
 }
 
 // CTA 0's outputs of the non-expand layout: counts and aligned expert prefix
-// (as in the expand layout), tokens per rank and their exclusive prefix, rows.
-// cnt_s [E] holds the counts; psum_s [E+1] and warp_tot [33] are scratch.
-// All threads of the CTA call.
-__device__ void write_outputs_nonexpand(const LayoutParams& p, const int32_t* cnt_s, int32_t* psum_s,
-                                        const int32_t* prank, const int32_t* tpr, int32_t* warp_tot) {
+// (as in the expand layout; psum_s already scanned), tokens per rank and their
+// exclusive prefix, rows.
+__device__ void write_outputs_nonexpand(const LayoutParams& p, const int32_t* cnt_s,
+                                        const int32_t* psum_s, const int32_t* prank,
+                                        const int32_t* tpr) {
   const int E = p.num_experts, W = p.world_size;
-  // one scan on one CTA: the whole block is faster than a single warp here
-  block_exclusive_scan(cnt_s, E, p.alignment, psum_s, warp_tot);
   for (int e = threadIdx.x; e <= E; e += blockDim.x) {
     p.psum_expert[e] = psum_s[e];
     if (e < E) p.cnt[e] = cnt_s[e];
@@ -709,7 +712,8 @@ __global__ void __launch_bounds__(kSlotThreads) ep_layout_slots_ne_kernel(Layout
   if (c == 0) {
     for (int e = tid; e < E; e += kSlotThreads) cnt_s[e] = p.col_total[e];
     __syncthreads();
-    write_outputs_nonexpand(p, cnt_s, psum_s, prank, tpr, warp_tot);
+    expert_scans(cnt_s, p.alignment, psum_s, nullptr, nullptr, E, warp_tot);
+    write_outputs_nonexpand(p, cnt_s, psum_s, prank, tpr);
   }
   if (has_tokens) {  // uniform per CTA
     __syncthreads();
@@ -732,7 +736,7 @@ __host__ __device__ constexpr int ClusterSmemWords(int E, int W, int K, int tpb,
          + tpb * K                                        // ids
          + (ne ? 0 : 3 * tpb * K + 2 * tpb)               // loc, slots_s, sorted, src (expand)
          + 2 * (E + 1) + 33                               // psum_s, cx, warp_tot
-         + (W + 1) + W + (W + 1) + W;                     // prank, rbase, rcx, tpr
+         + (W + 1) + W + (W + 1);                         // prank, rbase, rcx
 }
 
 template <int KC, bool NE>
@@ -767,7 +771,6 @@ __global__ void __launch_bounds__(kClusterThreads) ep_layout_cluster_kernel(Layo
   int32_t* prank = warp_tot + 33;                              // [W+1]
   int32_t* rbase = prank + W + 1;                              // [W]
   int32_t* rcx = rbase + W;                                    // [W+1]
-  int32_t* tpr = rcx + W + 1;                                  // [W]
 
   const uint32_t me = cluster_ctarank(), ncta = cluster_nctarank();
   const int t0 = static_cast<int>(me) * tpb;
@@ -794,7 +797,7 @@ __global__ void __launch_bounds__(kClusterThreads) ep_layout_cluster_kernel(Layo
     tot[j] = t;
     off[j] = o;
   }
-  cluster_arrive();  // this CTA is done reading remote shared memory
+  cluster_arrive_relaxed();  // this CTA is done reading remote shared memory
   __syncthreads();
 
   if constexpr (!NE) {
@@ -803,15 +806,18 @@ __global__ void __launch_bounds__(kClusterThreads) ep_layout_cluster_kernel(Layo
     slots_expand_tokens<KC>(p, t0, ntok, psum_s, off, cx, loc, ids, slots_s, sorted, src);
     fill_unreceived(p, psum_s, tot, psum_s[E], static_cast<int>(me), static_cast<int>(ncta));
   } else {
+    // rank prefix, this CTA's rank scan and (CTA 0, few experts) the expert
+    // prefix on three warps behind one barrier
     const int warp = threadIdx.x >> 5;
-    for (int r = threadIdx.x; r < W; r += kClusterThreads) tpr[r] = tot[E + r];
+    const bool warp_psum = E <= kWarpScanMax;
+    if (warp == 0) warp_scan64(tot + E, W, prank);
+    else if (warp == 1) warp_scan64(colcnt + E, W, rcx);
+    else if (warp == 2 && me == 0 && warp_psum) warp_exclusive_scan(tot, E, p.alignment, psum_s);
     __syncthreads();
-    if (warp == 0) warp_scan64(tpr, W, prank);
-    if (warp == 1) warp_scan64(colcnt + E, W, rcx);
-    __syncthreads();
+    if (me == 0 && !warp_psum) block_exclusive_scan(tot, E, p.alignment, psum_s, warp_tot);
     for (int r = threadIdx.x; r < W; r += kClusterThreads) rbase[r] = prank[r] + off[E + r];
-    if (me == 0) write_outputs_nonexpand(p, tot, psum_s, prank, tpr, warp_tot);
-    __syncthreads();
+    if (me == 0) write_outputs_nonexpand(p, tot, psum_s, prank, tot + E);
+    // rbase is read after slots_nonexpand_tokens' first barrier
     slots_nonexpand_tokens<KC>(p, t0, ntok, tpb, rbase, rcx, ids, woff, dslot, src_ne, sorted_ne);
     fill_unreceived(p, nullptr, nullptr, prank[W], static_cast<int>(me), static_cast<int>(ncta));
   }
