@@ -44,7 +44,8 @@ namespace epg {
 namespace {
 
 template <int RB, int KC, int V, int S>
-__global__ void __launch_bounds__(CopyThreads(RB, V, S)) ep_dispatch_copy_kernel(DispatchParams p) {
+__global__ void __launch_bounds__(CopyThreads(RB, V, S), CopyMinBlocks(RB, V, S))
+    ep_dispatch_copy_kernel(DispatchParams p) {
   dispatch_copy_body<RB, KC, V, S>(p);
 }
 
