@@ -380,20 +380,21 @@ def run_e2e(args, ep, torch, dev, wl, topk_cpu, w_cpu, x, handles, bufs, step_by
     x_h = x.cpu().pin_memory()
     topk_h = topk_cpu.pin_memory()
     w_h = w_cpu.pin_memory()
-    out_h = [torch.empty((N, H), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
-    x_d = [torch.empty_like(x) for _ in range(2)]
-    topk_d = [torch.empty(topk_cpu.shape, dtype=torch.int64, device=dev) for _ in range(2)]
-    w_d = [torch.empty(w_cpu.shape, dtype=torch.float32, device=dev) for _ in range(2)]
-    out_d = [torch.empty((N, H), dtype=torch.bfloat16, device=dev) for _ in range(2)]
+    nb = args.e2e_buffers
+    out_h = [torch.empty((N, H), dtype=torch.bfloat16).pin_memory() for _ in range(nb)]
+    x_d = [torch.empty_like(x) for _ in range(nb)]
+    topk_d = [torch.empty(topk_cpu.shape, dtype=torch.int64, device=dev) for _ in range(nb)]
+    w_d = [torch.empty(w_cpu.shape, dtype=torch.float32, device=dev) for _ in range(nb)]
+    out_d = [torch.empty((N, H), dtype=torch.bfloat16, device=dev) for _ in range(nb)]
     s_in, s_cmp, s_out = (torch.cuda.Stream(device=dev) for _ in range(3))
 
     def run(n):
         done = [None] * n     # compute of step i finished (its inputs may be overwritten)
         read = [None] * n     # step i's output is on the host (out_d[b] may be overwritten)
         for i in range(n):
-            b = i % 2
-            if i >= 2:
-                s_in.wait_event(done[i - 2])
+            b = i % nb
+            if i >= nb:
+                s_in.wait_event(done[i - nb])
             with torch.cuda.stream(s_in):
                 x_d[b].copy_(x_h, non_blocking=True)
                 topk_d[b].copy_(topk_h, non_blocking=True)
@@ -401,8 +402,8 @@ def run_e2e(args, ep, torch, dev, wl, topk_cpu, w_cpu, x, handles, bufs, step_by
             ready = torch.cuda.Event()
             ready.record(s_in)
             s_cmp.wait_event(ready)
-            if i >= 2:
-                s_cmp.wait_event(read[i - 2])
+            if i >= nb:
+                s_cmp.wait_event(read[i - nb])
             h16.layout(topk_d[b], stream=s_cmp)
             h16.dispatch(x_d[b], recv, stream=s_cmp)
             h16.combine(recv, w_d[b], out_d[b], stream=s_cmp)
@@ -435,8 +436,8 @@ def run_e2e(args, ep, torch, dev, wl, topk_cpu, w_cpu, x, handles, bufs, step_by
     return {"value": round(units / (ms * 1e-3) / 1e9, 1), "unit": "GB/s",
             "ms_per_step": round(ms, 4), "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "host_link": link,
-            "pipelining": "double-buffered device inputs/outputs; upload, compute and "
-                          "read-back on three streams ordered by events"}
+            "pipelining": "%d device buffers of inputs/outputs in rotation; upload, compute "
+                          "and read-back on three streams ordered by events" % nb}
 
 
 def host_link(torch, x_h, x_d, out_d, out_h, s_in, s_out, reps=5):
@@ -663,6 +664,8 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--e2e-buffers", type=int, default=2,
+                    help="device input/output buffers the end-to-end loop rotates through")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
