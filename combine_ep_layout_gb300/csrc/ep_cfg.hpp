@@ -94,6 +94,19 @@ constexpr int RowThreads(int chunks) {
   return 0;
 }
 
+// Minimum resident CTAs per SM asked of the compiler for the copy kernel of
+// rows of rb bytes (v words per vector, s CTAs per row).  When a thread holds at
+// most 16 words of the row, 32 registers suffice and the whole SM (65536
+// registers) can be filled; stating that keeps the compiler from trading a
+// register for a spill.  Larger per-thread shares, and the loop variant, are
+// left to the compiler (1).
+constexpr int CopyMinBlocks(int rb, int v, int s = 1) {
+  return rb && RowThreads(rb / (4 * v) / s) &&
+                 (rb / (4 * v) / s / RowThreads(rb / (4 * v) / s)) * v <= 16
+             ? 65536 / (32 * RowThreads(rb / (4 * v) / s))
+             : 1;
+}
+
 // Layout chunking: the count and slot kernels give each CTA kLayoutTPC tokens.
 constexpr int kLayoutTPC = 128;
 constexpr int kLayoutCountWarps = 16;

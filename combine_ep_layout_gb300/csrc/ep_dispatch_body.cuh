@@ -55,18 +55,6 @@ constexpr int Fp8Threads(int hc, int v, int s = 1) {
             : kRowMaxThreads;
 }
 
-// Minimum resident CTAs per SM asked of the compiler for the copy kernel.
-// When a thread holds at most 16 words of the row, 32 registers suffice and
-// the whole SM (2048 threads) can be resident; stating that keeps the compiler
-// from trading a register for a spill.  Larger per-thread shares are left to
-// the compiler (1).
-constexpr int CopyMinBlocks(int rb, int v, int s = 1) {
-  return rb && RowThreads(rb / (4 * v) / s) &&
-                 (rb / (4 * v) / s / RowThreads(rb / (4 * v) / s)) * v <= 16
-             ? 65536 / (32 * CopyThreads(rb, v, s))
-             : 1;
-}
-
 // A row of `vectors` vectors can be split over s CTAs when each slice is a
 // whole number of `unit`-vector groups held by a compile-time geometry.
 constexpr bool Splittable(int vectors, int unit, int s) {

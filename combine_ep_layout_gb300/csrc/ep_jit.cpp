@@ -224,6 +224,12 @@ const HeaderSet& headers() {
   return hs;
 }
 
+// Minimum resident CTAs per SM stated in the rendered launch bounds (the copy
+// kernel's, as for the compiled variants; 1 elsewhere).
+int min_blocks_of(const Request& r) {
+  return r.kind == Request::kCopy ? CopyMinBlocks(r.row_bytes, 8) : 1;
+}
+
 int block_of(const Request& r) {
   switch (r.kind) {
     case Request::kCopy: return RowThreads(r.row_bytes / 32);
@@ -373,9 +379,9 @@ std::string RenderSource(const Request& r) {
       std::snprintf(buf, sizeof buf,
                     "// ep_gb300 run-time specialisation (generated)\n"
                     "#include \"ep_dispatch_body.cuh\"\n"
-                    "extern \"C\" __global__ void __launch_bounds__(%d) %s(epg::DispatchParams p) {\n"
+                    "extern \"C\" __global__ void __launch_bounds__(%d, %d) %s(epg::DispatchParams p) {\n"
                     "  epg::dispatch_copy_body<%d, %d, 8>(p);\n}\n",
-                    block_of(r), name.c_str(), r.row_bytes, r.topk);
+                    block_of(r), min_blocks_of(r), name.c_str(), r.row_bytes, r.topk);
       break;
     case Request::kFp8:
       std::snprintf(buf, sizeof buf,
