@@ -126,6 +126,12 @@ def _stream_ptr(stream, device):
     return ctypes.c_void_p(stream.cuda_stream)
 
 
+def _require(cond, msg):
+    """Argument checks that survive python -O (unlike assert)."""
+    if not cond:
+        raise ValueError(msg)
+
+
 def _ptr(t):
     return ctypes.c_void_p(t.data_ptr()) if t is not None else None
 
@@ -165,9 +171,11 @@ class EpHandle:
         return self._h
 
     def layout(self, topk_idx, num_tokens=None, stream=None):
-        assert topk_idx.dtype == torch.int64 and topk_idx.is_cuda and topk_idx.is_contiguous()
+        _require(topk_idx.dtype == torch.int64 and topk_idx.is_cuda and topk_idx.is_contiguous(),
+                 "topk_idx must be a contiguous int64 CUDA tensor")
+        _require(topk_idx.dim() == 2 and topk_idx.shape[1] == self.cfg.num_expert_per_token,
+                 "topk_idx must be [num_tokens, num_expert_per_token]")
         n = topk_idx.shape[0] if num_tokens is None else int(num_tokens)
-        assert topk_idx.dim() == 2 and topk_idx.shape[1] == self.cfg.num_expert_per_token
         _check(load_library().ep_layout(self.ptr, _ptr(topk_idx) if n else None, n,
                                         _stream_ptr(stream, self.device)))
         self.num_tokens = n
@@ -175,9 +183,10 @@ class EpHandle:
     def dispatch(self, x, recv_x, recv_scales=None, topk_weights=None, recv_topk_weights=None,
                  recv_topk_idx=None, stream=None):
         """ep_dispatch, or ep_dispatch_fwd when recv_topk_weights / recv_topk_idx are given."""
-        assert x.is_cuda and x.is_contiguous() and recv_x.is_contiguous()
+        _require(x.is_cuda and x.is_contiguous() and recv_x.is_contiguous(),
+                 "x and recv_x must be contiguous CUDA tensors")
         for t in (recv_scales, topk_weights, recv_topk_weights, recv_topk_idx):
-            assert t is None or t.is_contiguous()
+            _require(t is None or t.is_contiguous(), "optional dispatch tensors must be contiguous")
         L = load_library()
         st = _stream_ptr(stream, self.device)
         if recv_topk_weights is None and recv_topk_idx is None:
@@ -189,10 +198,13 @@ class EpHandle:
 
     def combine(self, y, topk_weights, out, bias=None, stream=None):
         """ep_combine, or ep_combine_ex when a bias is given or out is fp32."""
-        assert y.is_cuda and y.is_contiguous() and out.is_contiguous()
-        assert topk_weights is None or topk_weights.is_contiguous()
-        assert bias is None or (bias.dtype == torch.bfloat16 and bias.is_contiguous())
-        assert out.dtype in (torch.bfloat16, torch.float32)
+        _require(y.is_cuda and y.is_contiguous() and out.is_contiguous(),
+                 "y and out must be contiguous CUDA tensors")
+        _require(topk_weights is None or topk_weights.is_contiguous(),
+                 "topk_weights must be contiguous")
+        _require(bias is None or (bias.dtype == torch.bfloat16 and bias.is_contiguous()),
+                 "bias must be a contiguous bf16 tensor")
+        _require(out.dtype in (torch.bfloat16, torch.float32), "out must be bf16 or fp32")
         L = load_library()
         st = _stream_ptr(stream, self.device)
         if bias is None and out.dtype == torch.bfloat16:
@@ -203,7 +215,8 @@ class EpHandle:
                                    odt, st))
 
     def field(self, field):
-        """A torch int32 view (no copy) of one handle field on the device."""
+        """A torch int32 view (no copy) of one handle field on the handle's device;
+        valid until the handle is freed, and overwritten by the next layout."""
         p, n = ctypes.c_void_p(), ctypes.c_int64()
         _check(load_library().ep_handle_get(self.ptr, field, ctypes.byref(p), ctypes.byref(n)))
         K = self.cfg.num_expert_per_token
@@ -214,9 +227,10 @@ class EpHandle:
             shape = (n.value // K, K)
         elif field == FIELD_RECV_SRC_METADATA:
             shape = (n.value // (K + 2), K + 2)
+        dev = torch.device("cuda", self.device)
         if n.value == 0:
-            return torch.zeros(shape, dtype=torch.int32, device="cuda")
-        return torch.as_tensor(_DevArray(p.value or 0, shape), device="cuda")
+            return torch.zeros(shape, dtype=torch.int32, device=dev)
+        return torch.as_tensor(_DevArray(p.value or 0, shape), device=dev)
 
     def status(self):
         v = ctypes.c_int32()
@@ -294,9 +308,11 @@ def ep_layout_noalloc(cfg, topk_idx, out, stream=None):
     """Layout into caller-owned int32 CUDA tensors (dict keyed by NOALLOC_OUTPUTS);
     the library allocates nothing for this call."""
     n = topk_idx.shape[0]
-    assert topk_idx.dtype == torch.int64 and topk_idx.is_cuda and topk_idx.is_contiguous()
+    _require(topk_idx.dtype == torch.int64 and topk_idx.is_cuda and topk_idx.is_contiguous(),
+             "topk_idx must be a contiguous int64 CUDA tensor")
     for k in NOALLOC_OUTPUTS:
-        assert out[k].dtype == torch.int32 and out[k].is_cuda and out[k].is_contiguous(), k
+        _require(out[k].dtype == torch.int32 and out[k].is_cuda and out[k].is_contiguous(),
+                 "%s must be a contiguous int32 CUDA tensor" % k)
     _check(load_library().ep_layout_noalloc(
         ctypes.byref(cfg), _ptr(topk_idx) if n else None, n,
         *[_ptr(out[k]) for k in NOALLOC_OUTPUTS], _stream_ptr(stream, topk_idx.device)))
