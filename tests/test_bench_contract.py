@@ -1,0 +1,67 @@
+"""bench.py's JSON line: the keys and the consistency the benchmark contract asks
+for, on the reference arm (the CPU oracle, no GPU) and on a small batch of the
+library's arm (GPU)."""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+BASE_KEYS = {"metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+             "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config"}
+
+
+def run_bench(*args, timeout=900):
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), *args], cwd=ROOT,
+                       capture_output=True, text=True, timeout=timeout)
+    assert r.returncode == 0, r.stdout[-2000:] + r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    return json.loads(lines[0])
+
+
+def test_reference_arm_line():
+    d = run_bench("--impl", "reference", "--steps", "1", "--warmup", "3", "--ref-block", "256")
+    assert BASE_KEYS <= set(d) and d["impl"] == "reference"
+    assert d["unit"] == "GB/s" and d["higher_is_better"] is True and d["value"] > 0
+    assert d["steps"] == 1 and d["warmup"] == 3 and d["n_gpus"] == 1
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] == 1 and cb["sample"]
+    assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}
+    assert d["config"]["workload"] and d["config"]["tokens"] == 32768
+
+
+def test_warmup_below_three_is_refused():
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--warmup", "2"],
+                       cwd=ROOT, capture_output=True, text=True, timeout=120)
+    assert r.returncode != 0 and "warmup" in r.stderr
+
+
+@pytest.mark.gpu
+def test_library_arm_line():
+    import __graft_entry__
+    __graft_entry__.build()
+    d = run_bench("--tokens", "2048", "--steps", "20", "--warmup", "3", "--cpu-seconds", "0.5")
+    assert BASE_KEYS <= set(d) and "impl" not in d
+    assert d["unit"] == "GB/s" and d["scaling"] == "weak" and d["vs_baseline"] is None
+    assert d["steps"] == 20 and d["ms_per_step"] > 0 and d["value"] > 0
+    roof = d["roofline"]
+    assert roof["bound"] == "hbm" and roof["unit"] == "GB/s"
+    assert abs(roof["frac"] - roof["achieved"] / roof["peak"]) < 1e-3
+    assert "traffic" in roof
+    assert roof["kernel"] in d["kernels"] and d["kernels"][roof["kernel"]]["gbs"] == roof["achieved"]
+    e = d["e2e"]
+    assert e["unit"] == "GB/s" and e["value"] > 0
+    assert e["h2d_bytes_per_step"] > 0 and e["d2h_bytes_per_step"] > 0
+    assert e["host_link"]["floor_ms_per_step"] > 0
+    assert e["ms_per_step"] >= 0.5 * e["host_link"]["floor_ms_per_step"]
+    clk = d["clocks"]
+    assert {"sm_mhz", "sm_max_mhz", "reasons"} <= set(clk)
+    # 2048 tokens: the single-launch cluster layout, then three data kernels per step
+    assert d["gpu_launches"] == 4 * d["steps"]
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] == 1 and cb["value"] > 0 and cb["sample"]
+    assert d["config"]["tokens"] == 2048
