@@ -1,6 +1,7 @@
 """Build libep_gb300.so in-tree: every .cu / .cpp under csrc/ compiled by nvcc
 for sm_103a (one -gencode), in parallel, then linked into a shared library
 beside this file.  No cmake, no torch extension machinery."""
+import fcntl
 import glob
 import hashlib
 import os
@@ -41,15 +42,35 @@ def _digest():
     return h.hexdigest()
 
 
+def _up_to_date(stamp, dig):
+    if not (os.path.exists(LIB) and os.path.exists(stamp)):
+        return False
+    with open(stamp) as f:
+        return f.read() == dig
+
+
 def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    """Compile and link; skipped when the library is newer build of the same sources."""
+    """Compile and link; skipped when the library is a build of the same sources.
+    Processes that build at the same time (one per rank under torchrun) take
+    turns on a lock file, and each re-checks the stamp once it holds the lock,
+    so the sources are compiled once and no process links or loads a half-written
+    object or library."""
     stamp = os.path.join(BUILD, "stamp")
     dig = _digest() + "|" + " ".join(extra_flags)
-    if not force and os.path.exists(LIB) and os.path.exists(stamp):
-        with open(stamp) as f:
-            if f.read() == dig:
-                return LIB
+    if not force and _up_to_date(stamp, dig):
+        return LIB
     os.makedirs(BUILD, exist_ok=True)
+    with open(os.path.join(BUILD, ".lock"), "w") as lock:
+        fcntl.flock(lock, fcntl.LOCK_EX)
+        try:
+            if not force and _up_to_date(stamp, dig):
+                return LIB
+            return _compile_and_link(stamp, dig, verbose, extra_flags)
+        finally:
+            fcntl.flock(lock, fcntl.LOCK_UN)
+
+
+def _compile_and_link(stamp, dig, verbose, extra_flags):
     cc = nvcc()
 
     def compile_one(src):
