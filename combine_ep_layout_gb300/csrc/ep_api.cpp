@@ -100,7 +100,11 @@ struct ep_handle {
   int64_t max_tokens = 0, rcap = 0;
   int max_chunks = 0;
   int num_tokens = 0;
-  cudaStream_t last_stream = nullptr;
+  cudaStream_t last_stream = nullptr;  // stream of the last call that enqueued work
+  bool launched = false;               // some call enqueued work on last_stream
+  // private non-blocking stream on which the metadata block is allocated,
+  // cleared and freed (stream-ordered allocator: no device-wide synchronisation)
+  cudaStream_t own_stream = nullptr;
   void* block = nullptr;
   bool no_expand = false;
   // non-null: this handle uses the routing of that handle's ep_layout (its own
@@ -191,7 +195,11 @@ int create_handle(const ep_cfg_t* cfg, ep_handle* src, ep_handle_t* out) {
     h->max_chunks = NumLayoutChunks(static_cast<int>(h->max_tokens));
 
     auto bail = [&](int code) {
-      if (h->block) cudaFree(h->block);
+      if (h->block) {
+        cudaFreeAsync(h->block, h->own_stream);
+        cudaStreamSynchronize(h->own_stream);
+      }
+      if (h->own_stream) cudaStreamDestroy(h->own_stream);
       delete h;
       return code;
     };
@@ -236,10 +244,17 @@ int create_handle(const ep_cfg_t* cfg, ep_handle* src, ep_handle_t* out) {
     const size_t n_scr = al(sizeof(int32_t) * static_cast<size_t>(LayoutScratchInts(h->max_chunks, cols)));
     const size_t n_send = h->no_expand ? n_slot : 0;
     const size_t total = n_small + 2 * n_slot + n_meta + n_scr + n_send;
-    e = cudaMalloc(&h->block, total);
+    // Stream-ordered allocation on a private non-blocking stream: creating a
+    // handle waits for nothing but its own clearing memset, never for work on
+    // the caller's other streams (cudaMalloc and cudaDeviceSynchronize may wait
+    // for the whole device).
+    if ((e = cudaStreamCreateWithFlags(&h->own_stream, cudaStreamNonBlocking)) != cudaSuccess)
+      return bail(fail_cuda(e, "cudaStreamCreateWithFlags"));
+    e = cudaMallocAsync(&h->block, total, h->own_stream);
     if (e != cudaSuccess) {
       cudaGetLastError();
-      return bail(fail(EP_ENOMEM, std::string("cudaMalloc of the handle's metadata failed: ") +
+      h->block = nullptr;
+      return bail(fail(EP_ENOMEM, std::string("cudaMallocAsync of the handle's metadata failed: ") +
                                       cudaGetErrorString(e)));
     }
     char* b = static_cast<char*>(h->block);
@@ -256,9 +271,11 @@ int create_handle(const ep_cfg_t* cfg, ep_handle* src, ep_handle_t* out) {
     h->scratch = reinterpret_cast<int32_t*>(b + n_small + 2 * n_slot + n_meta);
     h->send_slot = h->no_expand ? reinterpret_cast<int32_t*>(b + n_small + 2 * n_slot + n_meta + n_scr)
                                 : h->dst_slot;
-    if ((e = cudaMemset(h->block, 0, total)) != cudaSuccess)
-      return bail(fail_cuda(e, "cudaMemset"));
-    if ((e = cudaDeviceSynchronize()) != cudaSuccess) return bail(fail_cuda(e, "cudaDeviceSynchronize"));
+    if ((e = cudaMemsetAsync(h->block, 0, total, h->own_stream)) != cudaSuccess)
+      return bail(fail_cuda(e, "cudaMemsetAsync"));
+    // the block is ready for any stream once this returns
+    if ((e = cudaStreamSynchronize(h->own_stream)) != cudaSuccess)
+      return bail(fail_cuda(e, "cudaStreamSynchronize"));
     *out = h;
     return EP_OK;
   } catch (const std::exception& ex) {
@@ -338,6 +355,7 @@ int ep_layout(ep_handle_t h, const int64_t* topk_idx, int32_t num_tokens, ep_str
     if (cluster) h->layout_ran.insert(h->layout_ran.rfind('_'), "_cluster");  // ..._cluster_k8
     h->num_tokens = num_tokens;
     h->last_stream = s;
+    h->launched = true;
     return EP_OK;
   } catch (const std::exception& ex) {
     return fail(EP_EINVAL, ex.what());
@@ -394,6 +412,7 @@ int ep_dispatch_fwd(ep_handle_t h, const void* x, void* recv_x, float* recv_scal
                            : h->dispatch.launch(p, h->g_dispatch, s);
     if (e != cudaSuccess) return fail_cuda(e, "dispatch launch");
     h->last_stream = s;
+    h->launched = true;
     return EP_OK;
   } catch (const std::exception& ex) {
     return fail(EP_EINVAL, ex.what());
@@ -442,6 +461,7 @@ int ep_combine_ex(ep_handle_t h, const void* y, const float* topk_weights, const
                            : h->combine.launch(p, h->g_combine, s);
     if (e != cudaSuccess) return fail_cuda(e, "combine launch");
     h->last_stream = s;
+    h->launched = true;
     return EP_OK;
   } catch (const std::exception& ex) {
     return fail(EP_EINVAL, ex.what());
@@ -453,7 +473,13 @@ int ep_combine_ex(ep_handle_t h, const void* y, const float* topk_weights, const
 void ep_handle_free(ep_handle_t h) noexcept {
   try {
     if (!h) return;
-    if (h->block) cudaFree(h->block);
+    // the handle's work on its last stream finishes before its memory goes
+    if (h->launched) cudaStreamSynchronize(h->last_stream);
+    if (h->block) {
+      cudaFreeAsync(h->block, h->own_stream);
+      cudaStreamSynchronize(h->own_stream);
+    }
+    if (h->own_stream) cudaStreamDestroy(h->own_stream);
     delete h;
   } catch (...) {
   }
@@ -496,14 +522,15 @@ int ep_handle_status(ep_handle_t h, int32_t* device_error) noexcept {
     if (!h || !device_error) return fail(EP_EINVAL, "NULL argument");
     int rc = check_device(h);
     if (rc != EP_OK) return rc;
-    cudaError_t e = cudaStreamSynchronize(h->last_stream);
-    if (e != cudaSuccess) return fail_cuda(e, "cudaStreamSynchronize");
+    // read and clear the error word in order on the handle's last stream and
+    // wait for that stream only (other streams of the process keep running)
+    const cudaStream_t s = h->last_stream;
     int32_t v = 0;
     int32_t* err = owner(h)->err;
-    if ((e = cudaMemcpy(&v, err, sizeof v, cudaMemcpyDeviceToHost)) != cudaSuccess)
-      return fail_cuda(e, "cudaMemcpy");
-    if ((e = cudaMemset(err, 0, sizeof v)) != cudaSuccess) return fail_cuda(e, "cudaMemset");
-    if ((e = cudaDeviceSynchronize()) != cudaSuccess) return fail_cuda(e, "cudaDeviceSynchronize");
+    cudaError_t e = cudaMemcpyAsync(&v, err, sizeof v, cudaMemcpyDeviceToHost, s);
+    if (e != cudaSuccess) return fail_cuda(e, "cudaMemcpyAsync");
+    if ((e = cudaMemsetAsync(err, 0, sizeof v, s)) != cudaSuccess) return fail_cuda(e, "cudaMemsetAsync");
+    if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return fail_cuda(e, "cudaStreamSynchronize");
     *device_error = v;
     return EP_OK;
   } catch (...) {

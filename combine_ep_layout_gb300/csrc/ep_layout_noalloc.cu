@@ -1,7 +1,7 @@
 // ep_layout_noalloc.cu -- the layout for callers that cannot allocate device
 // memory.
 //
-// ep_handle_create allocates, with cudaMalloc, the handle's outputs and the
+// ep_handle_create allocates (cudaMallocAsync) the handle's outputs and the
 // layout's scratch: per-chunk expert/rank histograms and their prefix sums
 // over chunks.  Some callers cannot make that call.  A framework that hands
 // all device memory to its own caching pool may not allow an extra cudaMalloc
@@ -14,16 +14,21 @@
 // that allocates.
 //
 // The array costs every GPU that loads the library kNoAllocScratchInts * 4
-// bytes (1 MiB) until the process exits.  Its device address is looked up once
-// per device (cudaGetSymbolAddress, with that device current) on the first
-// call made while that device is current.  That call also sets the layout
-// kernels' shared-memory limit, so it should come before any stream capture.
+// bytes (1 MiB) until the process exits.  Its device address is looked up per
+// device (cudaGetSymbolAddress, with that device current) by the first call
+// made while that device is current; the same set-up also sets the layout
+// kernels' shared-memory limit, so that first call should come before any
+// stream capture.  The set-up is recorded only when it succeeds (a failed one
+// is retried by the next call) and is tied to the device's current CUDA
+// context: after cudaDeviceReset, or under another context, it runs again,
+// so no call launches with an address or a limit of a context that is gone.
 //
 // All calls share the one array and it keeps whatever the last call left
 // there.  The layout kernels write every scratch entry they later read, so no
 // part of it has to start at zero.  Two calls that can run at the same time on
 // the GPU (different streams, no ordering between them) overwrite each
 // other's scratch and give wrong results: order them, e.g. on one stream.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -43,37 +48,65 @@ constexpr int kNoAllocMaxDevices = 64;
 static __device__ __align__(256) int32_t g_noalloc_scratch[kNoAllocScratchInts];
 
 struct DeviceSetup {
-  std::once_flag once;
-  cudaError_t err = cudaSuccess;
-  int32_t* scratch = nullptr;  // device address of g_noalloc_scratch on this device
+  bool done = false;
+  unsigned long long ctx_id = 0;  // CUDA context the set-up was made in
+  int32_t* scratch = nullptr;     // device address of g_noalloc_scratch in that context
   int num_sms = 0;
-  int cluster_ok = 1;          // every layout variant can run its single-launch cluster kernel
+  int cluster_ok = 1;             // every layout variant can run its single-launch cluster kernel
 };
 
+std::mutex g_setup_mutex;
 DeviceSetup g_setup[kNoAllocMaxDevices];
 
-// Runs once per device, with that device current.
-void setup_device(DeviceSetup* s) {
+// Unique id of the calling thread's current CUDA context (cuCtxGetCurrent +
+// cuCtxGetId, reached through the runtime so that nothing links the driver
+// library directly).  A new context -- after cudaDeviceReset, say -- has a new id.
+cudaError_t current_context_id(unsigned long long* id) {
+  using GetCurrent = CUresult (*)(CUcontext*);
+  using GetId = CUresult (*)(CUcontext, unsigned long long*);
+  static GetCurrent get_current = nullptr;
+  static GetId get_id = nullptr;
+  if (get_current == nullptr || get_id == nullptr) {
+    void* f1 = nullptr;
+    void* f2 = nullptr;
+    cudaDriverEntryPointQueryResult q1, q2;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f1, 12000, cudaEnableDefault, &q1);
+    if (e != cudaSuccess) return e;
+    e = cudaGetDriverEntryPointByVersion("cuCtxGetId", &f2, 12000, cudaEnableDefault, &q2);
+    if (e != cudaSuccess) return e;
+    if (q1 != cudaDriverEntryPointSuccess || q2 != cudaDriverEntryPointSuccess)
+      return cudaErrorNotSupported;
+    get_current = reinterpret_cast<GetCurrent>(f1);
+    get_id = reinterpret_cast<GetId>(f2);
+  }
+  CUcontext ctx = nullptr;
+  if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return cudaErrorDeviceUninitialized;
+  if (get_id(ctx, id) != CUDA_SUCCESS) return cudaErrorDeviceUninitialized;
+  return cudaSuccess;
+}
+
+// Per-device set-up, with that device current: the scratch address and the
+// layout kernels' shared-memory opt-in.  Fills *s only when every step succeeds.
+cudaError_t setup_device(int dev, unsigned long long ctx_id, DeviceSetup* s) {
   void* p = nullptr;
   cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-  if (e != cudaSuccess) { s->err = e; return; }
-  int dev = 0;
-  if ((e = cudaGetDevice(&dev)) != cudaSuccess) { s->err = e; return; }
-  if ((e = cudaDeviceGetAttribute(&s->num_sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) {
-    s->err = e;
-    return;
-  }
+  if (e != cudaSuccess) return e;
+  int sms = 0;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
   // shared-memory opt-in of every layout variant, sized for the largest E+W
+  int cluster_ok = 1;
   const int topks[] = {4, 6, 8, 0};
   for (int k : topks) {
-    LaunchGeom g{s->num_sms, 1};
-    if ((e = FindLayout(k, false).prepare(0, k, kMaxExperts + kMaxWorld, &g)) != cudaSuccess) {
-      s->err = e;
-      return;
-    }
-    s->cluster_ok &= g.cluster_ok;
+    LaunchGeom g{sms, 1};
+    if ((e = FindLayout(k, false).prepare(0, k, kMaxExperts + kMaxWorld, &g)) != cudaSuccess) return e;
+    cluster_ok &= g.cluster_ok;
   }
   s->scratch = static_cast<int32_t*>(p);
+  s->num_sms = sms;
+  s->cluster_ok = cluster_ok;
+  s->ctx_id = ctx_id;
+  s->done = true;
+  return cudaSuccess;
 }
 
 int err_cuda(cudaError_t e, const char* what) {
@@ -126,9 +159,22 @@ extern "C" int ep_layout_noalloc(const ep_cfg_t* cfg, const int64_t* topk_idx, i
     if (e != cudaSuccess) return err_cuda(e, "cudaGetDevice");
     if (dev < 0 || dev >= kNoAllocMaxDevices)
       return RecordError(EP_EUNSUPPORTED, "ep_layout_noalloc: device ordinal above 63");
-    DeviceSetup* s = &g_setup[dev];
-    std::call_once(s->once, setup_device, s);
-    if (s->err != cudaSuccess) return err_cuda(s->err, "ep_layout_noalloc set-up");
+    unsigned long long ctx_id = 0;
+    if ((e = current_context_id(&ctx_id)) != cudaSuccess) return err_cuda(e, "current CUDA context");
+    DeviceSetup setup;
+    {
+      std::lock_guard<std::mutex> lock(g_setup_mutex);
+      DeviceSetup* s = &g_setup[dev];
+      if (!s->done || s->ctx_id != ctx_id) {
+        DeviceSetup fresh;
+        if ((e = setup_device(dev, ctx_id, &fresh)) != cudaSuccess) {
+          cudaGetLastError();
+          return err_cuda(e, "ep_layout_noalloc set-up");
+        }
+        *s = fresh;
+      }
+      setup = *s;
+    }
 
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if ((e = cudaMemsetAsync(device_error, 0, sizeof(int32_t), st)) != cudaSuccess)
@@ -154,8 +200,8 @@ extern "C" int ep_layout_noalloc(const ep_cfg_t* cfg, const int64_t* topk_idx, i
     p.meta = recv_src_metadata;
     p.err = device_error;
     p.epr_magic = RankMagic(cfg->num_expert_per_rank);
-    BindLayoutScratch(&p, s->scratch, Cs, cols);
-    const LaunchGeom g{s->num_sms, 1, s->cluster_ok, 0};
+    BindLayoutScratch(&p, setup.scratch, Cs, cols);
+    const LaunchGeom g{setup.num_sms, 1, setup.cluster_ok, 0};
     if ((e = FindLayout(K, false).launch(p, g, st)) != cudaSuccess) return err_cuda(e, "layout launch");
     return EP_OK;
   } catch (...) {

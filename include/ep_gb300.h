@@ -22,8 +22,10 @@
  *   - The caller owns every buffer it passes (inputs and outputs).  The
  *     handle owns its routing metadata (allocated by ep_handle_create, freed
  *     by ep_handle_free).
- *   - Work is enqueued on `stream` (NULL = the legacy default stream); no
- *     entry point synchronises except ep_handle_status.  The layout,
+ *   - Work is enqueued on `stream` (NULL = the legacy default stream).  No
+ *     entry point synchronises the device: ep_handle_create waits for its
+ *     own clearing memset only, ep_handle_status and ep_handle_free for the
+ *     handle's last stream only.  The layout,
  *     dispatch and combine calls allocate nothing and can be enqueued while a
  *     stream is being captured into a CUDA graph.
  *   - Return value 0 on success, else one of the negative EP_E* codes, with
@@ -104,8 +106,11 @@ typedef struct ep_handle *ep_handle_t;
 int64_t ep_recv_capacity(const ep_cfg_t *cfg) EP_NOEXCEPT;
 
 /* Validate cfg, pick the compiled kernel variants for it and allocate the
- * handle's device metadata on the current device (cudaMalloc; sized for W*T
- * tokens).  *out receives the handle.  Errors: EP_EINVAL (bad cfg or NULL;
+ * handle's device metadata on the current device (sized for W*T tokens), with
+ * the stream-ordered allocator (cudaMallocAsync) on a private non-blocking
+ * stream, then clear it on that stream and wait for that stream alone: work
+ * running on the caller's streams is neither waited for nor disturbed.
+ * *out receives the handle.  Errors: EP_EINVAL (bad cfg or NULL;
  * no_expand = 1 with use_weights = 1), EP_EUNSUPPORTED, EP_ENOMEM, EP_ECUDA. */
 int ep_handle_create(const ep_cfg_t *cfg, ep_handle_t *out) EP_NOEXCEPT;
 
@@ -127,8 +132,8 @@ int ep_handle_create_shared(const ep_cfg_t *cfg, ep_handle_t layout_src, ep_hand
 
 /* Layout.  topk_idx: device int64 [num_tokens, K] row-major, token t of
  * logical rank t / T.  Entries equal to -1 are masked (no receive row); any
- * other value outside [0, E) is skipped and sets bit 0 of the device error
- * word (see ep_handle_status).  Computes on the device, into the handle:
+ * other value outside [0, E) is skipped and sets the value 1 (bit 0) in the
+ * device error word (see ep_handle_status).  Computes on the device, into the handle:
  *   num_unaligned_recv_tokens_per_expert [E]   entries routed to each expert
  *   num_tokens_per_rank [W]                    tokens with >= 1 expert on rank r
  *   psum_num_recv_tokens_per_expert [E+1]      exclusive prefix sum of the
@@ -225,13 +230,16 @@ int ep_combine(ep_handle_t h, const void *y, const float *topk_weights, void *ou
  *   dst_slot                  device int32 [num_tokens, K]
  *   recv_src_metadata         device int32 [Rcap, K+2] (8-byte aligned when K is even)
  *   device_error              device int32 [1]; cleared, then error bits as in
- *                             ep_handle_status (bit 0: an id outside [-1, E) was skipped)
+ *                             ep_handle_status (value 1 (bit 0): an id outside [-1, E) was skipped)
  * Size limit: 2*(E+W)*ceil(num_tokens/128) + (E+W) int32 of scratch must fit
  * in 262144 (for example 32768 tokens over 256 experts and 8 ranks need
  * 135432); larger requests return EP_EINVAL with the sizes in the message.
  * The first call on a device, with that device current, looks up the
  * scratch array's address and sets the layout kernels' shared-memory limit
- * on that device; make that first call before any stream capture.  Every
+ * on that device; make that first call before any stream capture.  That
+ * set-up is kept only when it succeeds (a failed one is tried again by the
+ * next call) and belongs to the device's current CUDA context: after
+ * cudaDeviceReset the next call repeats it.  Every
  * call shares the scratch array: calls that may run at the same time on the
  * GPU (unordered streams) overwrite each other's scratch and give wrong
  * results, so order them (one stream, or events).  Allocates nothing. */
@@ -250,8 +258,11 @@ int ep_layout_noalloc(const ep_cfg_t *cfg, const int64_t *topk_idx, int32_t num_
 int ep_combine_ex(ep_handle_t h, const void *y, const float *topk_weights, const void *bias,
                   void *out, int32_t out_dtype, ep_stream_t stream) EP_NOEXCEPT;
 
-/* Release the handle and its device memory (cudaFree, which waits for work
- * using it to finish).  NULL is ignored. */
+/* Release the handle and its device memory.  Waits for the stream of the
+ * handle's last layout / dispatch / combine call (which must still exist),
+ * then frees the metadata in stream order on the handle's private stream.
+ * Work on other streams that uses the handle must be complete, or ordered
+ * before that last call, when this is called.  NULL is ignored. */
 void ep_handle_free(ep_handle_t h) EP_NOEXCEPT;
 
 /* Fields of the handle, for ep_handle_get. */
@@ -272,10 +283,11 @@ enum {
  * ownership; valid until ep_handle_free).  EP_EINVAL for an unknown field. */
 int ep_handle_get(ep_handle_t h, int32_t field, void **dev_ptr, int64_t *numel) EP_NOEXCEPT;
 
-/* Synchronise the handle's last stream, read and clear the sticky device
- * error word.  Bits: 1 = a topk id outside [-1, E) was skipped; 2 is reserved
- * for a kernel that gave up a bounded wait (no kernel of this version waits).
- * Returns EP_ECUDA if the synchronisation fails. */
+/* Read and clear the sticky device error word, in order on the stream of
+ * the handle's last layout / dispatch / combine call, and wait for that
+ * stream only.  Values: 1 (bit 0) = a topk id outside [-1, E) was skipped;
+ * 2 (bit 1) is reserved for a kernel that gives up a bounded wait.  Returns EP_ECUDA if the
+ * copy or the synchronisation fails. */
 int ep_handle_status(ep_handle_t h, int32_t *device_error) EP_NOEXCEPT;
 
 /* Name of the kernel variant chosen for a step (0 = layout, 1 = dispatch,
