@@ -38,32 +38,32 @@ __global__ void __launch_bounds__(kCombineThreads) ep_combine_kernel(CombinePara
 inline bool aligned32(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 31u) == 0; }
 
 template <int HC, int KC, bool WEIGHTED, int V>
-cudaError_t launch_flags(const CombineParams& p, cudaStream_t s) {
+cudaError_t launch_flags(const CombineParams& p, cudaStream_t s, int pdl) {
   const bool bias = p.bias != nullptr, f32 = p.out_f32 != 0;
+  const int n = p.num_tokens;
   if (bias && f32)
-    ep_combine_kernel<HC, KC, WEIGHTED, V, true, true><<<p.num_tokens, kCombineThreads, 0, s>>>(p);
-  else if (bias)
-    ep_combine_kernel<HC, KC, WEIGHTED, V, true, false><<<p.num_tokens, kCombineThreads, 0, s>>>(p);
-  else if (f32)
-    ep_combine_kernel<HC, KC, WEIGHTED, V, false, true><<<p.num_tokens, kCombineThreads, 0, s>>>(p);
-  else
-    ep_combine_kernel<HC, KC, WEIGHTED, V, false, false><<<p.num_tokens, kCombineThreads, 0, s>>>(p);
-  return cudaGetLastError();
+    return LaunchData(ep_combine_kernel<HC, KC, WEIGHTED, V, true, true>, n, kCombineThreads, s, p, pdl);
+  if (bias)
+    return LaunchData(ep_combine_kernel<HC, KC, WEIGHTED, V, true, false>, n, kCombineThreads, s, p, pdl);
+  if (f32)
+    return LaunchData(ep_combine_kernel<HC, KC, WEIGHTED, V, false, true>, n, kCombineThreads, s, p, pdl);
+  return LaunchData(ep_combine_kernel<HC, KC, WEIGHTED, V, false, false>, n, kCombineThreads, s, p, pdl);
 }
 
 template <int HC, int KC, bool WEIGHTED>
-cudaError_t launch_combine(const CombineParams& p, const LaunchGeom&, cudaStream_t s) {
+cudaError_t launch_combine(const CombineParams& p, const LaunchGeom& g, cudaStream_t s) {
   if (p.num_tokens == 0) return cudaSuccess;
   // 32-byte chunks when every row start is 32-byte aligned; otherwise the
   // generic variant with 16-byte chunks
   const bool v8 = p.hidden % 16 == 0 && aligned32(p.y) && aligned32(p.out) &&
                   (p.bias == nullptr || aligned32(p.bias));
-  if (v8) return launch_flags<HC, KC, WEIGHTED, 8>(p, s);
-  return launch_flags<0, 0, WEIGHTED, 4>(p, s);
+  if (v8) return launch_flags<HC, KC, WEIGHTED, 8>(p, s, g.pdl);
+  return launch_flags<0, 0, WEIGHTED, 4>(p, s, g.pdl);
 }
 
 template <int HC, int KC, bool WEIGHTED>
 cudaError_t prepare_combine(int, int, int, LaunchGeom* g) {
+  g->pdl = PdlEnabled() ? 1 : 0;
   return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
       &g->blocks_per_sm, ep_combine_kernel<HC, KC, WEIGHTED, 8, false, false>, kCombineThreads, 0);
 }

@@ -15,12 +15,12 @@ constexpr int kCombineThreads = 128;
 template <int V>
 __device__ __forceinline__ void ld_stream(const void* p, Vec<V>& r) {
   if constexpr (V == 8) {
-    asm volatile("ld.global.nc.L1::no_allocate.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+    asm volatile("ld.global.cg.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
                  : "=r"(r.w[0]), "=r"(r.w[1]), "=r"(r.w[2]), "=r"(r.w[3]), "=r"(r.w[4]),
                    "=r"(r.w[5]), "=r"(r.w[6]), "=r"(r.w[7])
                  : "l"(p));
   } else {
-    asm volatile("ld.global.nc.L1::no_allocate.v4.b32 {%0,%1,%2,%3}, [%4];"
+    asm volatile("ld.global.cg.v4.b32 {%0,%1,%2,%3}, [%4];"
                  : "=r"(r.w[0]), "=r"(r.w[1]), "=r"(r.w[2]), "=r"(r.w[3])
                  : "l"(p));
   }
@@ -85,6 +85,10 @@ __device__ __forceinline__ void combine_body(const CombineParams& p) {
   const int row = 2 * H;
   const int chunks = row / UNIT;
   const int t = blockIdx.x;
+  // every input here may be an output of the preceding grid (dst_slot of the
+  // layout, y of the expert step): nothing is read before it has completed
+  allow_dependent_grids();
+  grid_dependency_wait();
 
   int32_t slot[KM];
   float w[KM];
@@ -93,8 +97,8 @@ __device__ __forceinline__ void combine_body(const CombineParams& p) {
     slot[k] = -1;
     w[k] = 1.0f;
     if (k < K) {
-      slot[k] = __ldg(p.dst_slot + static_cast<int64_t>(t) * K + k);
-      if (WEIGHTED) w[k] = __ldg(p.weights + static_cast<int64_t>(t) * K + k);
+      slot[k] = ld_coherent(p.dst_slot + static_cast<int64_t>(t) * K + k);
+      if (WEIGHTED) w[k] = ld_coherent(p.weights + static_cast<int64_t>(t) * K + k);
     }
   }
   const uint8_t* y = static_cast<const uint8_t*>(p.y);

@@ -49,8 +49,12 @@ __global__ void __launch_bounds__(CopyThreads(RB, V, S), CopyMinBlocks(RB, V, S)
   dispatch_copy_body<RB, KC, V, S>(p);
 }
 
+// The explicit minimum of one resident CTA leaves the register budget to the
+// kernel's needs (39-47 registers): with the thread bound alone ptxas held some
+// variants to 32 registers and moved values to local memory (a 4-byte spill and
+// 8-24 byte stack frames).
 template <int HC, int KC, int V, int S>
-__global__ void __launch_bounds__(Fp8Threads(HC, V, S)) ep_dispatch_fp8_kernel(DispatchParams p) {
+__global__ void __launch_bounds__(Fp8Threads(HC, V, S), 1) ep_dispatch_fp8_kernel(DispatchParams p) {
   dispatch_fp8_body<HC, KC, V, S>(p);
 }
 
@@ -108,22 +112,21 @@ cudaError_t launch_copy(const DispatchParams& p, const LaunchGeom& g, cudaStream
   // 32-byte vectors when every row start is 32-byte aligned
   if (p.row_bytes % 32 == 0 && aligned32(p.x) && aligned32(p.recv_x)) {
     if constexpr (RB != 0 && Splittable(RB / 32, 1, 2)) {
-      if (row_slices(p.num_tokens, g) == 2) {
-        ep_dispatch_copy_kernel<RB, KC, 8, 2>
-            <<<2 * p.num_tokens, copy_block<RB, KC, 8, 2>(p.row_bytes), 0, s>>>(p);
-        return cudaGetLastError();
-      }
+      if (row_slices(p.num_tokens, g) == 2)
+        return LaunchData(ep_dispatch_copy_kernel<RB, KC, 8, 2>, 2 * p.num_tokens,
+                          copy_block<RB, KC, 8, 2>(p.row_bytes), s, p, g.pdl);
     }
-    ep_dispatch_copy_kernel<RB, KC, 8, 1><<<p.num_tokens, copy_block<RB, KC, 8, 1>(p.row_bytes), 0, s>>>(p);
-  } else {
-    ep_dispatch_copy_kernel<RB, KC, 4, 1><<<p.num_tokens, copy_block<RB, KC, 4, 1>(p.row_bytes), 0, s>>>(p);
+    return LaunchData(ep_dispatch_copy_kernel<RB, KC, 8, 1>, p.num_tokens,
+                      copy_block<RB, KC, 8, 1>(p.row_bytes), s, p, g.pdl);
   }
-  return cudaGetLastError();
+  return LaunchData(ep_dispatch_copy_kernel<RB, KC, 4, 1>, p.num_tokens,
+                    copy_block<RB, KC, 4, 1>(p.row_bytes), s, p, g.pdl);
 }
 
 template <int RB, int KC>
 cudaError_t prepare_copy(int, int, int, LaunchGeom* g) {
   g->row_slices = slices_override();
+  g->pdl = PdlEnabled() ? 1 : 0;
   return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
       &g->blocks_per_sm, ep_dispatch_copy_kernel<RB, KC, 8, 1>, kRowMaxThreads, 0);
 }
@@ -140,27 +143,31 @@ cudaError_t launch_fp8(const DispatchParams& p, const LaunchGeom& g, cudaStream_
   // hidden % 128 == 0 here, so 32-byte input vectors only need an aligned x
   if (aligned32(p.x)) {
     if constexpr (HC != 0 && Splittable(2 * HC / 32, 128 / 16, 2)) {
-      if (row_slices(p.num_tokens, g) == 2) {
-        ep_dispatch_fp8_kernel<HC, KC, 8, 2>
-            <<<2 * p.num_tokens, fp8_block<HC, KC, 8, 2>(p.hidden), 0, s>>>(p);
-        return cudaGetLastError();
-      }
+      if (row_slices(p.num_tokens, g) == 2)
+        return LaunchData(ep_dispatch_fp8_kernel<HC, KC, 8, 2>, 2 * p.num_tokens,
+                          fp8_block<HC, KC, 8, 2>(p.hidden), s, p, g.pdl);
     }
-    ep_dispatch_fp8_kernel<HC, KC, 8, 1><<<p.num_tokens, fp8_block<HC, KC, 8, 1>(p.hidden), 0, s>>>(p);
-  } else {
-    ep_dispatch_fp8_kernel<HC, KC, 4, 1><<<p.num_tokens, fp8_block<HC, KC, 4, 1>(p.hidden), 0, s>>>(p);
+    return LaunchData(ep_dispatch_fp8_kernel<HC, KC, 8, 1>, p.num_tokens,
+                      fp8_block<HC, KC, 8, 1>(p.hidden), s, p, g.pdl);
   }
-  return cudaGetLastError();
+  return LaunchData(ep_dispatch_fp8_kernel<HC, KC, 4, 1>, p.num_tokens,
+                    fp8_block<HC, KC, 4, 1>(p.hidden), s, p, g.pdl);
 }
 
 template <int HC, int KC>
 cudaError_t prepare_fp8(int, int, int, LaunchGeom* g) {
   g->row_slices = slices_override();
+  g->pdl = PdlEnabled() ? 1 : 0;
   return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
       &g->blocks_per_sm, ep_dispatch_fp8_kernel<HC, KC, 8, 1>, kRowMaxThreads, 0);
 }
 
 }  // namespace
+
+bool PdlEnabled() {
+  const char* env = std::getenv("EP_GB300_PDL");
+  return env == nullptr || env[0] != '0';
+}
 
 Variant<DispatchLaunch> FindDispatch(int hidden, int topk, EpDType dtype) {
   switch (dtype) {

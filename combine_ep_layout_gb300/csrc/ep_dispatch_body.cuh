@@ -15,12 +15,12 @@ namespace epg {
 template <int V>
 __device__ __forceinline__ void load_stream(const void* p, Vec<V>& r) {
   if constexpr (V == 8) {
-    asm volatile("ld.global.nc.L1::no_allocate.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+    asm volatile("ld.global.cg.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
                  : "=r"(r.w[0]), "=r"(r.w[1]), "=r"(r.w[2]), "=r"(r.w[3]), "=r"(r.w[4]),
                    "=r"(r.w[5]), "=r"(r.w[6]), "=r"(r.w[7])
                  : "l"(p));
   } else {
-    asm volatile("ld.global.nc.L1::no_allocate.v4.b32 {%0,%1,%2,%3}, [%4];"
+    asm volatile("ld.global.cg.v4.b32 {%0,%1,%2,%3}, [%4];"
                  : "=r"(r.w[0]), "=r"(r.w[1]), "=r"(r.w[2]), "=r"(r.w[3])
                  : "l"(p));
   }
@@ -110,9 +110,14 @@ __device__ __forceinline__ void dispatch_copy_body(const DispatchParams& p) {
   constexpr int CH = RB ? RB / UNIT / S : 0;  // vectors of this CTA's slice
   constexpr int T = RB ? RowThreads(CH) : 0;
   static_assert(S == 1 || (RB != 0 && Splittable(RB / UNIT, 1, S)), "row slices need a compiled geometry");
+  const int64_t base = (S == 1 || RB == 0) ? 0 : static_cast<int64_t>(blockIdx.x % S) * CH * UNIT;
+  // x is not an output of the layout: warm L2 with this CTA's part of the row
+  // while the preceding grid drains, then wait for that grid (dst_slot)
+  if (threadIdx.x == 0) prefetch_l2(xr + base, RB ? CH * UNIT : row);
+  allow_dependent_grids();
+  grid_dependency_wait();
   if constexpr (T != 0) {
     constexpr int PER = CH / T;
-    const int64_t base = S == 1 ? 0 : static_cast<int64_t>(blockIdx.x % S) * CH * UNIT;
     Vec<V> v[PER];
 #pragma unroll
     for (int u = 0; u < PER; ++u)
@@ -120,7 +125,7 @@ __device__ __forceinline__ void dispatch_copy_body(const DispatchParams& p) {
 #pragma unroll
     for (int k = 0; k < KM; ++k) {
       if (k >= K) break;
-      const int32_t d = __ldg(sl + k);
+      const int32_t d = ld_coherent(sl + k);
       if (d < 0) continue;
       uint8_t* dr = rx + static_cast<int64_t>(d) * row + base;
 #pragma unroll
@@ -131,7 +136,7 @@ __device__ __forceinline__ void dispatch_copy_body(const DispatchParams& p) {
     const int nt = blockDim.x;
     int32_t d[KM];
 #pragma unroll
-    for (int k = 0; k < KM; ++k) d[k] = k < K ? __ldg(sl + k) : -1;
+    for (int k = 0; k < KM; ++k) d[k] = k < K ? ld_coherent(sl + k) : -1;
     for (int c0 = threadIdx.x; c0 < chunks; c0 += 2 * nt) {
       const int c1 = c0 + nt;
       Vec<V> a, b;
@@ -228,13 +233,19 @@ __device__ __forceinline__ void dispatch_fp8_body(const DispatchParams& p) {
   constexpr int T = HC ? RowThreads(CH) : 0;
   static_assert(S == 1 || (HC != 0 && Splittable(2 * HC / UNIT, LANES, S)),
                 "row slices need a compiled geometry of whole scale groups");
+  const int cs = (S == 1 || HC == 0) ? 0 : static_cast<int>(blockIdx.x % S) * CH;  // first vector of the slice
+  // x is not an output of the layout: warm L2 with this CTA's part of the row
+  // while the preceding grid drains, then wait for that grid (dst_slot)
+  if (threadIdx.x == 0)
+    prefetch_l2(xr + static_cast<int64_t>(cs) * UNIT, HC ? CH * UNIT : 2 * H);
+  allow_dependent_grids();
+  grid_dependency_wait();
   if constexpr (T != 0) {
     constexpr int PER = CH / T;
-    const int c0 = S == 1 ? 0 : static_cast<int>(blockIdx.x % S) * CH;  // first vector of the slice
     Vec<V> v[PER];
 #pragma unroll
     for (int u = 0; u < PER; ++u)
-      load_stream<V>(xr + static_cast<int64_t>(c0 + threadIdx.x + u * T) * UNIT, v[u]);
+      load_stream<V>(xr + static_cast<int64_t>(cs + threadIdx.x + u * T) * UNIT, v[u]);
     uint32_t q[PER][V / 2];
     float s[PER];
 #pragma unroll
@@ -242,11 +253,11 @@ __device__ __forceinline__ void dispatch_fp8_body(const DispatchParams& p) {
 #pragma unroll
     for (int k = 0; k < KM; ++k) {
       if (k >= K) break;
-      const int32_t d = __ldg(sl + k);
+      const int32_t d = ld_coherent(sl + k);
       if (d < 0) continue;
 #pragma unroll
       for (int u = 0; u < PER; ++u) {
-        const int c = c0 + threadIdx.x + u * T;
+        const int c = cs + threadIdx.x + u * T;
         store_q<V>(rq + static_cast<int64_t>(d) * H + static_cast<int64_t>(c) * (2 * V), q[u]);
         if (leader) rs[static_cast<int64_t>(d) * G + c / LANES] = s[u];
       }
@@ -255,7 +266,7 @@ __device__ __forceinline__ void dispatch_fp8_body(const DispatchParams& p) {
     const int chunks = 2 * H / UNIT;
     int32_t d[KM];
 #pragma unroll
-    for (int k = 0; k < KM; ++k) d[k] = k < K ? __ldg(sl + k) : -1;
+    for (int k = 0; k < KM; ++k) d[k] = k < K ? ld_coherent(sl + k) : -1;
     // uniform trip count (blockDim is a multiple of 32): the shuffles see every lane
     for (int c0 = 0; c0 < chunks; c0 += blockDim.x) {
       const int c = c0 + threadIdx.x;

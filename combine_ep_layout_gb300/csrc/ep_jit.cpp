@@ -20,6 +20,7 @@
 #include <utility>
 
 #include "ep_cfg.hpp"
+#include "ep_kernels.hpp"
 
 namespace epg {
 namespace jit {
@@ -146,6 +147,7 @@ struct Driver {
   decltype(&cuModuleLoadData) load = nullptr;
   decltype(&cuModuleGetFunction) get_function = nullptr;
   decltype(&cuLaunchKernel) launch = nullptr;
+  decltype(&cuLaunchKernelEx) launch_ex = nullptr;  // for programmatic dependent launch
   bool ok = false;
 };
 
@@ -157,6 +159,7 @@ const Driver& driver() {
     r.load = reinterpret_cast<decltype(r.load)>(dlsym(h, "cuModuleLoadData"));
     r.get_function = reinterpret_cast<decltype(r.get_function)>(dlsym(h, "cuModuleGetFunction"));
     r.launch = reinterpret_cast<decltype(r.launch)>(dlsym(h, "cuLaunchKernel"));
+    r.launch_ex = reinterpret_cast<decltype(r.launch_ex)>(dlsym(h, "cuLaunchKernelEx"));
     r.ok = r.load && r.get_function && r.launch;
     return r;
   }();
@@ -387,7 +390,7 @@ std::string RenderSource(const Request& r) {
       std::snprintf(buf, sizeof buf,
                     "// ep_gb300 run-time specialisation (generated)\n"
                     "#include \"ep_dispatch_body.cuh\"\n"
-                    "extern \"C\" __global__ void __launch_bounds__(%d) %s(epg::DispatchParams p) {\n"
+                    "extern \"C\" __global__ void __launch_bounds__(%d, 1) %s(epg::DispatchParams p) {\n"
                     "  epg::dispatch_fp8_body<%d, %d, 8>(p);\n}\n",
                     block_of(r), name.c_str(), r.hidden, r.topk);
       break;
@@ -511,8 +514,28 @@ bool Load(const Request& r, Kernel* out, std::string* err) {
 cudaError_t Launch(const Kernel& k, int grid, const void* params, cudaStream_t stream) {
   if (grid <= 0) return cudaSuccess;
   void* args[1] = {const_cast<void*>(params)};
-  const CUresult r = driver().launch(reinterpret_cast<CUfunction>(k.function), grid, 1, 1, k.block,
-                                     1, 1, 0, reinterpret_cast<CUstream>(stream), args, nullptr);
+  const Driver& d = driver();
+  CUresult r;
+  if (d.launch_ex && epg::PdlEnabled()) {
+    // programmatic stream serialisation, as for the compiled variants: the
+    // kernel bodies wait for the preceding grid before touching memory
+    CUlaunchAttribute attr[1];
+    attr[0].id = CU_LAUNCH_ATTRIBUTE_PROGRAMMATIC_STREAM_SERIALIZATION;
+    attr[0].value.programmaticStreamSerializationAllowed = 1;
+    CUlaunchConfig cfg = {};
+    cfg.gridDimX = static_cast<unsigned>(grid);
+    cfg.gridDimY = cfg.gridDimZ = 1;
+    cfg.blockDimX = static_cast<unsigned>(k.block);
+    cfg.blockDimY = cfg.blockDimZ = 1;
+    cfg.sharedMemBytes = 0;
+    cfg.hStream = reinterpret_cast<CUstream>(stream);
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    r = d.launch_ex(&cfg, reinterpret_cast<CUfunction>(k.function), args, nullptr);
+  } else {
+    r = d.launch(reinterpret_cast<CUfunction>(k.function), grid, 1, 1, k.block, 1, 1, 0,
+                 reinterpret_cast<CUstream>(stream), args, nullptr);
+  }
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorLaunchFailure;
 }
 

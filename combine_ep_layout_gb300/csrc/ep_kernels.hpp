@@ -53,7 +53,31 @@ struct LaunchGeom {
   int blocks_per_sm;  // resident CTAs per SM for the variant's block and shared memory
   int cluster_ok;     // layout: the single-launch cluster kernel can be scheduled
   int row_slices;     // dispatch: CTAs per token row forced by EP_GB300_DISPATCH_SLICES (0: table)
+  int pdl;            // dispatch / combine: launched with programmatic stream serialisation
 };
+
+// Programmatic dependent launch of the data kernels, unless EP_GB300_PDL=0
+// (read when a handle is built; for A/B measurements).
+bool PdlEnabled();
+
+// Launch `kernel(p)` on `s`, with programmatic stream serialisation when `pdl`:
+// the kernel may then be scheduled while the preceding kernel of the stream
+// drains; it waits for that kernel's completion (grid_dependency_wait) before
+// it touches memory.
+template <class P>
+cudaError_t LaunchData(void (*kernel)(P), int grid, int block, cudaStream_t s, const P& p, int pdl) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(static_cast<unsigned>(block));
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, p);
+}
 
 using LayoutLaunch = cudaError_t (*)(const LayoutParams&, const LaunchGeom&, cudaStream_t);
 using DispatchLaunch = cudaError_t (*)(const DispatchParams&, const LaunchGeom&, cudaStream_t);

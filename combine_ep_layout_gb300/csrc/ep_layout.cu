@@ -11,7 +11,9 @@
 // writes its slots and metadata (slots_*_tokens).  Two ways to run that:
 //
 // Large batches, three launches (the last two with programmatic dependent
-// launch so that each is scheduled while its predecessor drains):
+// launch so that each is scheduled while its predecessor drains; the last
+// one, like the cluster kernel, lets the dispatch that follows be scheduled
+// early too):
 //   count  one CTA per chunk of kLayoutTPC tokens.  The chunk's ids are staged
 //          in shared memory with one coalesced load and every pass runs from
 //          there.  Per-warp histograms over contiguous runs of entries use
@@ -82,17 +84,6 @@ __device__ __forceinline__ int expert_of(int64_t v, int E) {
 // RankMagic (0 when Epr == 1).
 __device__ __forceinline__ int rank_of(int e, uint32_t magic) {
   return magic ? static_cast<int>(__umulhi(static_cast<uint32_t>(e), magic)) : e;
-}
-
-// Let the next kernel of the stream (launched with programmatic stream
-// serialisation) be scheduled; it waits for this grid's completion itself.
-__device__ __forceinline__ void allow_dependents() {
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-
-// Wait until the preceding grid of the stream has completed and its writes are visible.
-__device__ __forceinline__ void wait_for_preceding_grid() {
-  asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 // ---- thread-block cluster primitives (sm_90 and later) ----------------------
@@ -335,7 +326,7 @@ __global__ void __launch_bounds__(kCountThreads) ep_layout_count_kernel(LayoutPa
   const int c = blockIdx.x;
   const int t0 = c * kLayoutTPC;
   const int ntok = min(p.num_tokens, t0 + kLayoutTPC) - t0;
-  allow_dependents();
+  allow_dependent_grids();
   count_tokens<KC>(p, t0, ntok, whist, ids, colcnt,
                    p.no_expand ? nullptr : p.dst_slot + static_cast<int64_t>(t0) * K);
   for (int j = threadIdx.x; j < EW; j += kCountThreads)
@@ -351,8 +342,8 @@ __global__ void __launch_bounds__(kSpineWarps * 32) ep_layout_spine_kernel(Layou
   const int C = p.num_chunks;
   const int j = blockIdx.x * kSpineWarps + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
-  allow_dependents();
-  wait_for_preceding_grid();
+  allow_dependent_grids();
+  grid_dependency_wait();
   if (j >= EW) return;
   const int32_t* in = p.chunk_hist + static_cast<int64_t>(j) * C;
   int32_t* out = p.chunk_off + static_cast<int64_t>(j) * C;
@@ -522,7 +513,8 @@ __global__ void __launch_bounds__(kSlotThreads) ep_layout_slots_kernel(LayoutPar
 
   const int c = blockIdx.x;
   const bool has_tokens = c < C;
-  wait_for_preceding_grid();
+  allow_dependent_grids();   // the dispatch that follows may be scheduled now
+  grid_dependency_wait();
   for (int e = threadIdx.x; e < E; e += kSlotThreads) {
     cnt_s[e] = p.col_total[e];
     if (has_tokens) {
@@ -695,7 +687,8 @@ __global__ void __launch_bounds__(kSlotThreads) ep_layout_slots_ne_kernel(Layout
   const int c = blockIdx.x;
   const bool has_tokens = c < C;
   const int tid = threadIdx.x, warp = tid >> 5;
-  wait_for_preceding_grid();
+  allow_dependent_grids();   // the dispatch that follows may be scheduled now
+  grid_dependency_wait();
   for (int r = tid; r < W; r += kSlotThreads) {
     tpr[r] = p.col_total[E + r];
     if (has_tokens) {
@@ -773,6 +766,7 @@ __global__ void __launch_bounds__(kClusterThreads) ep_layout_cluster_kernel(Layo
   int32_t* rcx = rbase + W;                                    // [W+1]
 
   const uint32_t me = cluster_ctarank(), ncta = cluster_nctarank();
+  allow_dependent_grids();   // the dispatch that follows may be scheduled now
   const int t0 = static_cast<int>(me) * tpb;
   const int ntok = max(0, min(p.num_tokens, t0 + tpb) - t0);
   count_tokens<KC>(p, t0, ntok, whist, ids, colcnt, NE ? nullptr : loc);
