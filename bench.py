@@ -124,6 +124,83 @@ def ncu_traffic(kernel):
     return k.get("dram_bytes_per_launch")
 
 
+# NVML clock-event reason bits (nvml.h, nvmlClocksEventReason*) reported by name
+NVML_REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+                0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+
+class NvmlClockSampler:
+    """SM clock, its maximum, power and clock-event reasons read in-process
+    through NVML (read-only queries of libnvidia-ml, loaded with ctypes) every
+    `period_s` on a background thread, so that a timed region of a few tens of
+    milliseconds still holds tens of samples.  `ok` is False when NVML or the
+    device cannot be found; the caller then falls back to nvidia-smi."""
+
+    def __init__(self, device_index, period_s=0.001):
+        import ctypes
+        self.period = period_s
+        self.samples = []          # (sm_mhz, power_w, reasons bitmask)
+        self.max_mhz = None
+        self.ok = False
+        self._stop = threading.Event()
+        try:
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                return
+            h = ctypes.c_void_p()
+            import torch
+            props = torch.cuda.get_device_properties(device_index)
+            bus = "%08X:%02X:%02X.0" % (props.pci_domain_id, props.pci_bus_id, props.pci_device_id)
+            if nv.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), ctypes.byref(h)) != 0:
+                return
+            self.nv, self.h, self.ct = nv, h, ctypes
+            mx = ctypes.c_uint()
+            if nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:   # NVML_CLOCK_SM
+                self.max_mhz = float(mx.value)
+            self._reasons = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                nv.nvmlDeviceGetCurrentClocksThrottleReasons
+            self.ok = self._sample() is not None
+        except (OSError, AttributeError, RuntimeError, AssertionError):
+            self.ok = False
+
+    def _sample(self):
+        ct, nv, h = self.ct, self.nv, self.h
+        mhz, mw, rs = ct.c_uint(), ct.c_uint(), ct.c_ulonglong()
+        if nv.nvmlDeviceGetClockInfo(h, 1, ct.byref(mhz)) != 0:
+            return None
+        nv.nvmlDeviceGetPowerUsage(h, ct.byref(mw))
+        self._reasons(h, ct.byref(rs))
+        return (float(mhz.value), mw.value / 1000.0, int(rs.value))
+
+    def _run(self):
+        while not self._stop.is_set():
+            v = self._sample()
+            if v is not None:
+                self.samples.append(v)
+            time.sleep(self.period)
+
+    def __enter__(self):
+        self.samples = []
+        self.t = threading.Thread(target=self._run, daemon=True)
+        self.t.start()
+        return self
+
+    def __exit__(self, *a):
+        self._stop.set()
+        self.t.join(timeout=5)
+
+    def summary(self):
+        sm = [v[0] for v in self.samples]
+        bits = 0
+        for v in self.samples:
+            bits |= v[2]
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": self.max_mhz,
+                "reasons": sorted(n for b, n in NVML_REASONS.items() if bits & b),
+                "samples": len(sm), "sm_mhz_min": min(sm) if sm else None,
+                "power_w_max": round(max(v[1] for v in self.samples), 1) if sm else None,
+                "source": "NVML in-process, every %.0f ms" % (self.period * 1e3)}
+
+
 class ClockSampler:
     """nvidia-smi clocks and throttle reasons sampled every 20 ms; entering the
     context waits (up to 5 s) for the first sample so that the sampler is
@@ -182,7 +259,8 @@ class ClockSampler:
                 if v.lower().startswith("active"):
                     reasons.add(n)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(sm),
+                "source": "nvidia-smi every 20 ms"}
 
 
 # ------------------------------------------------------------- GPU arm
@@ -303,7 +381,8 @@ def run_ours(args, rank, local_rank, world):
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
-    with ClockSampler(local_rank) as clk:
+    nvml = NvmlClockSampler(local_rank)
+    with (nvml if nvml.ok else ClockSampler(local_rank)) as clk:
         start.record(stream)
         for i in range(args.steps):
             step(events[i])
@@ -349,6 +428,7 @@ def run_ours(args, rank, local_rank, world):
 
     if rank != 0:
         return None
+    clocks = clk.summary()
     gbs = units / (ms * 1e-3) / 1e9
     line = {
         "metric": METRIC, "value": round(gbs, 1), "unit": "GB/s", "n_gpus": world,
@@ -360,7 +440,9 @@ def run_ours(args, rank, local_rank, world):
         "kernels": kernels,
         "roofline": roof,
         "gpu_launches": launches_per_step * args.steps,
-        "clocks": clk.summary(),
+        "clocks": clocks,
+        # step time x median SM clock: thousands of SM cycles per step
+        "ms_per_step_x_sm_mhz": round(ms * clocks["sm_mhz"], 1) if clocks.get("sm_mhz") else None,
         "e2e": e2e,
         "cpu_baseline": cpu,
     }
@@ -475,14 +557,25 @@ def host_link(torch, x_h, x_d, out_d, out_h, s_in, s_out, reps=5):
 
 def run_all_configs(args):
     """Per workload (tiny, decode, prefill bf16, prefill FP8, skewed) and layout
-    (expand, then non-expand: one row per (token, rank), unweighted combine):
-    layout, dispatch and combine timed separately with CUDA events, L2 flushed
-    (a 256 MB write) before every step and outside the timed events; medians
-    over args.steps steps.  One JSON line per workload and layout.  Each step
-    starts behind a ~100 us device-side sleep, so that the host has enqueued
-    the whole step before the GPU reaches it: the events then time device work
-    (and the gaps between back-to-back kernels), not Python's launch latency,
-    which is longer than a small workload's kernels."""
+    (expand, then non-expand: one row per (token, rank), unweighted combine),
+    one JSON line each with four timed regions per step, each after its own L2
+    flush and GPU sleep (below):
+      layout    the layout alone;
+      dispatch  the dispatch alone (on the layout just computed);
+      combine   the combine alone (on the rows just dispatched, or y);
+      step      layout -> dispatch -> combine back to back, events only at its
+                two ends, so that the kernels' programmatic dependent launch
+                (each scheduled while its predecessor drains) is counted.
+    Medians (and means) over args.steps steps.  The flush writes a 256 MB
+    buffer (twice L2) and then reads another 256 MB buffer: the write alone
+    leaves L2 full of the flush's own dirty lines, which the next write-heavy
+    kernel would then have to write back to DRAM on top of its own traffic
+    (decode dispatch measured 24.8 us after a write-only flush and 20.8 us
+    after write + read); flushing before each kernel likewise keeps a kernel
+    from paying for the write-back of its predecessor's output.  Each region
+    starts behind a ~100 us device-side sleep, so that the host has enqueued it
+    before the GPU reaches it: the events then time device work, not Python's
+    launch latency, which is longer than a small workload's kernels."""
     import torch
 
     import combine_ep_layout_gb300 as ep
@@ -492,8 +585,16 @@ def run_all_configs(args):
     dev = torch.device("cuda", 0)
     peak, peak_kind = measured_peaks()
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    flush_read = torch.ones(256 << 20, dtype=torch.uint8, device=dev)
     s = torch.cuda.Stream(device=dev)
     only = set(args.workload.split(",")) if args.workload else None
+
+    def cold(i):
+        with torch.cuda.stream(s):
+            flush.fill_(i & 0xFF)
+            flush_read.sum(dtype=torch.int32)
+            torch.cuda._sleep(SLEEP_CYCLES)
+
     for name, wl, ne in [(n, w, ne) for ne in (False, True) for n, w in synth.WORKLOADS.items()
                          if only is None or n in only]:
         N, H, K = wl.num_tokens, wl.hidden, wl.topk
@@ -511,23 +612,28 @@ def run_all_configs(args):
         # for the FP8 workload an independent bf16 N(0,1) [Rcap, H]
         y = synth.gen_y(wl, device=dev) if fp8 else recv
         out = torch.empty((N, H), dtype=torch.bfloat16, device=dev)
-        times = {"layout": [], "dispatch": [], "combine": []}
+        wc = None if ne else w
+        regions = {
+            "layout": lambda: h.layout(topk, stream=s),
+            "dispatch": lambda: h.dispatch(x, recv, scales, stream=s),
+            "combine": lambda: h.combine(y, wc, out, stream=s),
+            "step": lambda: (h.layout(topk, stream=s), h.dispatch(x, recv, scales, stream=s),
+                             h.combine(y, wc, out, stream=s)),
+        }
+        times = {k: [] for k in regions}
         for i in range(args.warmup + args.steps):
-            with torch.cuda.stream(s):
-                flush.fill_(i & 0xFF)
-                torch.cuda._sleep(SLEEP_CYCLES)
-            ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
-            ev[0].record(s)
-            h.layout(topk, stream=s)
-            ev[1].record(s)
-            h.dispatch(x, recv, scales, stream=s)
-            ev[2].record(s)
-            h.combine(y, None if ne else w, out, stream=s)
-            ev[3].record(s)
+            ev = []
+            for k, fn in regions.items():
+                cold(i)
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(s)
+                fn()
+                b.record(s)
+                ev.append((k, a, b))
             s.synchronize()
             if i >= args.warmup:
-                for j, k in enumerate(times):
-                    times[k].append(ev[j].elapsed_time(ev[j + 1]) * 1e3)
+                for k, a, b in ev:
+                    times[k].append(a.elapsed_time(b) * 1e3)
         assert h.status() == 0
         if ne:
             rows = int(h.field(ep.FIELD_NUM_RECV).cpu()[0])
@@ -539,10 +645,13 @@ def run_all_configs(args):
         line = {"workload": name, "layout_kind": "non-expand" if ne else "expand",
                 "tokens": N, "hidden": H, "experts": wl.num_experts, "topk": K,
                 "alignment": wl.alignment, "dispatch_dtype": wl.dispatch_dtype,
-                "routing": wl.routing, "l2": "flushed before every step (256 MB write)",
-                "timing": "device: step enqueued behind a 100 us GPU sleep",
+                "routing": wl.routing,
+                "l2": "flushed before every timed region (256 MB write, then 256 MB read)",
+                "timing": "device: each region enqueued behind a 100 us GPU sleep",
                 "steps": args.steps, "peak_gbs": peak, "peak_kind": peak_kind}
-        for k, b in (("layout", nb["layout"]), ("dispatch", nb[dkey]), ("combine", nb["combine"])):
+        step_bytes = nb["layout"] + nb[dkey] + nb["combine"]
+        for k, b in (("layout", nb["layout"]), ("dispatch", nb[dkey]), ("combine", nb["combine"]),
+                     ("step", step_bytes)):
             us = statistics.median(times[k])
             line[k] = {"us_median": round(us, 2), "us_mean": round(statistics.mean(times[k]), 2),
                        "us_min": round(min(times[k]), 2),
@@ -550,8 +659,9 @@ def run_all_configs(args):
                        "gbs": round(b / (us * 1e-6) / 1e9, 1),
                        "frac_of_peak": round(b / (us * 1e-6) / 1e9 / peak, 4),
                        "frac_of_8tbs": round(b / (us * 1e-6) / 1e9 / 8000.0, 4),
-                       "tokens_per_s": round(N / (us * 1e-6), 1),
-                       "variant": h.variant({"layout": 0, "dispatch": 1, "combine": 2}[k])}
+                       "tokens_per_s": round(N / (us * 1e-6), 1)}
+            if k != "step":
+                line[k]["variant"] = h.variant({"layout": 0, "dispatch": 1, "combine": 2}[k])
         print(json.dumps(line), flush=True)
         h.free()
         del recv, scales, y, out, x

@@ -59,7 +59,10 @@ def test_library_arm_line():
     assert e["host_link"]["floor_ms_per_step"] > 0
     assert e["ms_per_step"] >= 0.5 * e["host_link"]["floor_ms_per_step"]
     clk = d["clocks"]
-    assert {"sm_mhz", "sm_max_mhz", "reasons"} <= set(clk)
+    assert {"sm_mhz", "sm_max_mhz", "reasons", "samples", "source"} <= set(clk)
+    # clocks are read in-process through NVML every millisecond during the timed region
+    assert clk["source"].startswith("NVML") and clk["samples"] >= 1
+    assert abs(d["ms_per_step_x_sm_mhz"] - d["ms_per_step"] * clk["sm_mhz"]) < 1
     # 2048 tokens: the single-launch cluster layout, then three data kernels per step
     assert d["gpu_launches"] == 4 * d["steps"]
     cb = d["cpu_baseline"]
