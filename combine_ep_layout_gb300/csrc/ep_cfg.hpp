@@ -98,12 +98,16 @@ constexpr int RowThreads(int chunks) {
 // rows of rb bytes (v words per vector, s CTAs per row).  When a thread holds at
 // most 16 words of the row, 32 registers suffice and the whole SM (65536
 // registers) can be filled; stating that keeps the compiler from trading a
-// register for a spill.  Larger per-thread shares, and the loop variant, are
-// left to the compiler (1).
+// register for a spill.  The count is capped at the SM's 32 resident CTAs
+// (small rows take small CTAs).  Larger per-thread shares, and the loop
+// variant, are left to the compiler (1).
+constexpr int kMaxCtasPerSm = 32;
 constexpr int CopyMinBlocks(int rb, int v, int s = 1) {
   return rb && RowThreads(rb / (4 * v) / s) &&
                  (rb / (4 * v) / s / RowThreads(rb / (4 * v) / s)) * v <= 16
-             ? 65536 / (32 * RowThreads(rb / (4 * v) / s))
+             ? (65536 / (32 * RowThreads(rb / (4 * v) / s)) < kMaxCtasPerSm
+                    ? 65536 / (32 * RowThreads(rb / (4 * v) / s))
+                    : kMaxCtasPerSm)
              : 1;
 }
 

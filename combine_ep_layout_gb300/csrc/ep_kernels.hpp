@@ -40,9 +40,13 @@ struct LayoutParams {
   int32_t* err;              // [1]
   int32_t* topk_i32;         // [N, K] clone of the ids (-1 where skipped), or nullptr
   uint32_t epr_magic;        // RankMagic(num_expert_per_rank)
-  // scratch (BindLayoutScratch): per-chunk column histograms, column-major [E+W][C]
+  // scratch (BindLayoutScratch): per-chunk column histograms, row-major [C][E+W]
+  // (a chunk's row is contiguous: written by count, read by slots), the same
+  // counts column-major [E+W][C] (a column is contiguous: read by the spine),
+  // and the exclusive prefix over chunks, row-major [C][E+W]
   int32_t* chunk_hist;
-  int32_t* chunk_off;        // exclusive prefix over chunks, [E+W][C]
+  int32_t* chunk_hist_cols;
+  int32_t* chunk_off;
   int32_t* col_total;        // [E+W]
 };
 
@@ -98,10 +102,18 @@ Variant<LayoutLaunch> FindLayout(int topk, bool no_expand);
 // cluster kernel (small batches) rather than count / spine / slots.
 bool LayoutUsesCluster(const LayoutParams& p, const LaunchGeom& g);
 Variant<DispatchLaunch> FindDispatch(int hidden, int topk, EpDType dtype);
+// The dispatch that stages rows through shared memory with TMA bulk copies
+// (byte-copy transports; null launch when the dtype or the row size is not
+// served), requested by EP_GB300_DISPATCH_TMA=1.
+Variant<DispatchLaunch> FindDispatchTma(EpDType dtype, int row_bytes);
+bool DispatchTmaRequested();
+// Bound of a device-side wait in ns: EP_GB300_WAIT_NS, else kDefaultWaitNs.
+uint64_t WaitLimitNs();
 Variant<CombineLaunch> FindCombine(int hidden, int topk, bool use_weights);
 
 // int32 words of layout scratch for up to max_chunks chunks and `columns` = E+W
-// columns: [chunk_hist] [chunk_off], each [columns][max_chunks], then [columns] totals.
+// columns: [chunk_hist] [chunk_hist_cols] [chunk_off], each columns x max_chunks,
+// then [columns] totals.
 int64_t LayoutScratchInts(int max_chunks, int columns);
 // Point p's scratch fields into `base` (LayoutScratchInts(max_chunks, columns) words).
 void BindLayoutScratch(LayoutParams* p, int32_t* base, int max_chunks, int columns);

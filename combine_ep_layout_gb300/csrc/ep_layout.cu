@@ -23,7 +23,7 @@
 //          each entry its stable rank in the chunk.  Tokens per rank: each
 //          entry ORs its rank bit into its token's mask, then warp ballots
 //          count the set bits.  The chunk's column totals (E experts + W ranks)
-//          go to a column-major [E+W][C] table.
+//          go to one contiguous row of a row-major [C][E+W] table.
 //   spine  a warp per column scans the C chunk totals (chunk offsets and
 //          column totals).
 //   slots  every CTA rebuilds the aligned exclusive prefix over the experts
@@ -66,8 +66,12 @@ namespace epg {
 namespace {
 
 constexpr int kCountThreads = kLayoutCountWarps * 32;
+// Resident count CTAs per SM asked of the compiler (at most 42 registers): the
+// 256 chunks of a 32768-token batch then run in one wave.  (The runtime-top-k
+// variant carries up to 16 ids per thread and asks for 2.)
+constexpr int kCountMinBlocks = 3;
 constexpr int kSpineWarps = 8;
-constexpr int kSlotThreads = 256;
+constexpr int kSlotThreads = 512;
 constexpr int kClusterThreads = kCountThreads;   // the cluster kernel counts like count
 constexpr int kClusterCtas = 8;                  // portable cluster size
 constexpr int kClusterMaxTPB = 2 * kLayoutTPC;   // tokens per CTA of the cluster kernel
@@ -128,6 +132,11 @@ __device__ __forceinline__ int32_t ld_cluster_shared(const int32_t* local, uint3
 
 // ---- scans --------------------------------------------------------------------
 
+// v rounded up to a multiple of A (a mask when A is a power of two).
+__device__ __forceinline__ int align_up(int v, int A) {
+  return (A & (A - 1)) == 0 ? (v + A - 1) & -A : (v + A - 1) / A * A;
+}
+
 // Block-wide exclusive scan of align(v[e], A) for e in [0, n) into out[0..n]
 // (out[n] = total).  warp_tot needs 33 words.  All threads must call it.
 __device__ void block_exclusive_scan(const int32_t* v, int n, int A, int32_t* out,
@@ -137,7 +146,7 @@ __device__ void block_exclusive_scan(const int32_t* v, int n, int A, int32_t* ou
   const int V = (n + nthr - 1) / nthr;
   const int beg = min(n, tid * V), end = min(n, beg + V);
   int sum = 0;
-  for (int e = beg; e < end; ++e) sum += (v[e] + A - 1) / A * A;
+  for (int e = beg; e < end; ++e) sum += align_up(v[e], A);
   int incl = sum;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -161,7 +170,7 @@ __device__ void block_exclusive_scan(const int32_t* v, int n, int A, int32_t* ou
   int run = warp_tot[warp] + incl - sum;
   for (int e = beg; e < end; ++e) {
     out[e] = run;
-    run += (v[e] + A - 1) / A * A;
+    run += align_up(v[e], A);
   }
   if (tid == 0) out[n] = warp_tot[32];
   __syncthreads();
@@ -174,7 +183,7 @@ __device__ __forceinline__ void warp_exclusive_scan(const int32_t* v, int n, int
   const int V = (n + 31) / 32;
   const int beg = min(n, lane * V), end = min(n, beg + V);
   int sum = 0;
-  for (int e = beg; e < end; ++e) sum += (v[e] + A - 1) / A * A;
+  for (int e = beg; e < end; ++e) sum += align_up(v[e], A);
   int incl = sum;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -184,14 +193,14 @@ __device__ __forceinline__ void warp_exclusive_scan(const int32_t* v, int n, int
   int run = incl - sum;
   for (int e = beg; e < end; ++e) {
     out[e] = run;
-    run += (v[e] + A - 1) / A * A;
+    run += align_up(v[e], A);
   }
   if (lane == 31) out[n] = incl;
 }
 
 // Expert counts up to this many are scanned by single warps (no block barriers
-// inside the scan); larger ones by the whole block.
-constexpr int kWarpScanMax = 128;
+// inside the scan; at most 16 values per lane); larger ones by the whole block.
+constexpr int kWarpScanMax = 512;
 
 // The two exclusive scans over the E experts: align(a[e], A) into out_a and,
 // when b is non-null, b[e] into out_b (E+1 outputs each).  All threads call;
@@ -230,112 +239,197 @@ __device__ __forceinline__ void warp_scan64(const int32_t* v, int n, int32_t* ou
 
 // ---------------------------------------------------------------- count
 
-// Count the tokens [t0, t0 + ntok) of this CTA (kCountThreads threads, all of
-// which call this).  ids [ntok*K] receives the staged expert ids (-1 = skip);
-// whist [NW][E+W] ends as each warp's exclusive start per column; colcnt[E+W]
-// receives the range's column totals (entries per expert, tokens per rank);
-// loc, when non-null, receives each entry's stable rank among the range's
-// entries of its expert (shared or global memory).
+// Batches of 32 entries a warp of a counting CTA walks at most: ranges of up to
+// kClusterMaxTPB tokens, kLayoutCountWarps warps.
 template <int KC>
-__device__ void count_tokens(const LayoutParams& p, int t0, int ntok, int32_t* whist, int32_t* ids,
-                             int32_t* colcnt, int32_t* loc) {
+constexpr int CountBatches() {
+  return ((kClusterMaxTPB * (KC ? KC : kMaxTopk) + kLayoutCountWarps - 1) / kLayoutCountWarps + 31) / 32;
+}
+
+// What a counting thread keeps in registers for the slot pass of the same CTA:
+// the expert of its entry in each batch (-1: none) and the entry's rank among
+// the earlier entries of that expert in its warp's run.
+template <int KC>
+struct CountRegs {
+  int e[CountBatches<KC>()];
+  int loc[CountBatches<KC>()];
+};
+
+// Token rank masks are OR-reduced over each token's lanes with shuffles when
+// K is a power of two that divides 32 (then a 32-entry batch holds whole
+// tokens); otherwise each entry sets its bit with a shared-memory atomic.
+template <int KC>
+constexpr bool ShuffleMasks() { return KC != 0 && 32 % KC == 0; }
+
+// Count the tokens [t0, t0 + ntok) of this CTA (kCountThreads threads, all of
+// which call this).  The range's entries, flat index i = (t - t0)*K + k, are cut
+// into one contiguous run of whole 32-entry batches per warp.  For each batch
+// the lanes that carry the same expert find each other with __match_any_sync:
+// an entry's rank among its run's earlier entries of its expert is the warp's
+// running count of that expert (the warp's own row of whist, which only that
+// warp touches until the barrier) plus the lanes of its group below it.  One
+// pass therefore gives the warp's histogram and every entry's stable rank in
+// the run.  Tokens per rank: each token's rank mask (bit r: an expert on rank
+// r) goes to tmask[t - t0], and after the barrier ballots count each rank's
+// bit.  On return (after one block barrier; the caller barriers again before
+// reading them):
+//   whist [NW][E+W]  each warp's exclusive start per expert (a scan over the warps)
+//   colcnt [E+W]     the range's entries per expert, then tokens per rank
+//   ids [ntok*K]     the staged expert ids (-1: skipped), when non-null
+//   regs             per batch: expert and rank within the warp's run
+// A range entry's rank among all the range's entries of expert e is
+// whist[warp][e] + regs.loc[b].
+template <int KC>
+__device__ void count_tokens(const LayoutParams& p, int t0, int ntok, int32_t* whist,
+                             unsigned long long* tmask, int32_t* colcnt, int32_t* ids,
+                             CountRegs<KC>& regs) {
   constexpr int NW = kLayoutCountWarps;
+  constexpr int NB = CountBatches<KC>();
+  static_assert(NW == 16, "the column scan gives each expert column a half warp");
   const int K = KC ? KC : p.topk;
   const int E = p.num_experts, W = p.world_size;
   const int EW = E + W;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nent = ntok * K;
-  const int64_t* topk = p.topk_idx + static_cast<int64_t>(t0) * K;
-
-  bool bad = false;
-  int32_t* clone = p.topk_i32 ? p.topk_i32 + static_cast<int64_t>(t0) * K : nullptr;
-  for (int i = tid; i < nent; i += kCountThreads) {
-    const int64_t v = topk[i];
-    const int e = expert_of(v, E);
-    bad |= (e < 0 && v != -1);
-    ids[i] = e;
-    if (clone) clone[i] = e;
-  }
-  for (int i = tid; i < NW * EW; i += kCountThreads) whist[i] = 0;
-  __syncthreads();
-
-  // per-warp histogram over a contiguous run of entries (whole 32-entry batches)
   const int per_warp = (((nent + NW - 1) / NW) + 31) & ~31;
   const int wbeg = warp * per_warp;
   const int wend = min(nent, wbeg + per_warp);
-  int32_t* wh = whist + warp * EW;
-  for (int i = wbeg + lane; i < wend; i += 32) {
-    const int e = ids[i];
-    if (e >= 0) atomicAdd(&wh[e], 1);
-  }
-  // tokens per rank: each thread builds its token's rank mask in registers
-  // (no atomics: all K entries of a token would hit one word), warp ballots count
-  for (int tl0 = warp * 32; tl0 < ntok; tl0 += kCountThreads) {
-    const int tl = tl0 + lane;
-    unsigned long long mask = 0ull;
-    if (tl < ntok)
-      for (int k = 0; k < K; ++k) {
-        const int e = ids[tl * K + k];
-        if (e >= 0) mask |= 1ull << rank_of(e, p.epr_magic);
-      }
-    for (int r = 0; r < W; ++r) {
-      const int n = __popc(__ballot_sync(0xffffffffu, (mask >> r) & 1ull));
-      if (lane == 0 && n) atomicAdd(&whist[E + r], n);
-    }
-  }
-  __syncthreads();
+  const int64_t* topk = p.topk_idx + static_cast<int64_t>(t0) * K;
+  int32_t* clone = p.topk_i32 ? p.topk_i32 + static_cast<int64_t>(t0) * K : nullptr;
 
-  // exclusive scan across warps per column; the column total is the range's count
-  for (int j = tid; j < EW; j += kCountThreads) {
-    int run = 0;
+  // all of the warp's ids in flight at once
+  int64_t raw[NB];
 #pragma unroll
-    for (int w = 0; w < NW; ++w) {
-      const int v = whist[w * EW + j];
-      whist[w * EW + j] = run;
-      run += v;
-    }
-    colcnt[j] = run;
+  for (int b = 0; b < NB; ++b) {
+    const int i = wbeg + b * 32 + lane;
+    raw[b] = (b * 32 < per_warp && i < wend) ? topk[i] : -1;
   }
+  int32_t* wh = whist + warp * EW;
+  for (int j = lane; j < EW; j += 32) wh[j] = 0;
+  if constexpr (!ShuffleMasks<KC>()) {
+    for (int t = tid; t < ntok; t += kCountThreads) tmask[t] = 0ull;
+    __syncthreads();
+  }
+  __syncwarp();
+
+  bool bad = false;
+#pragma unroll
+  for (int b = 0; b < NB; ++b) {
+    if (b * 32 >= per_warp) break;  // warp-uniform: the run's batches are done
+    const int i = wbeg + b * 32 + lane;
+    const bool in = i < wend;
+    const int e = in ? expert_of(raw[b], E) : -1;
+    bad |= in && e < 0 && raw[b] != -1;
+    if (in) {
+      if (ids) ids[i] = e;
+      if (clone) clone[i] = e;
+    }
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    const int base = e >= 0 ? wh[e] : 0;
+    __syncwarp();
+    if (e >= 0 && lane == __ffs(peers) - 1) wh[e] = base + __popc(peers);
+    __syncwarp();
+    regs.e[b] = e;
+    regs.loc[b] = base + __popc(peers & lanemask_lt());
+    unsigned long long m = e >= 0 ? 1ull << rank_of(e, p.epr_magic) : 0ull;
+    if constexpr (ShuffleMasks<KC>()) {
+#pragma unroll
+      for (int o = 1; o < KC; o <<= 1) m |= __shfl_xor_sync(0xffffffffu, m, o);
+      if (in && i % KC == 0) tmask[i / KC] = m;
+    } else {
+      if (m) atomicOr(&tmask[i / K], m);
+    }
+  }
+  if (bad) atomicOr(p.err, kErrBadExpert);
   __syncthreads();
 
-  // stable rank of each entry within the range (the expand layout's slots)
-  if (loc != nullptr)
-    for (int i = wbeg; i < wend; i += 32) {
-      const int idx = i + lane;
-      const int e = idx < wend ? ids[idx] : -1;
-      const unsigned peers = __match_any_sync(0xffffffffu, e);
-      const int base = e >= 0 ? wh[e] : 0;
-      const int rank = base + __popc(peers & lanemask_lt());
-      __syncwarp();
-      if (e >= 0 && lane == __ffs(peers) - 1) wh[e] = base + __popc(peers);
-      __syncwarp();
-      if (idx < wend) loc[idx] = e >= 0 ? rank : -1;
+  // per expert, a half warp scans the 16 warps' counts: each warp's start and
+  // the range's total
+  for (int j0 = 2 * warp; j0 < E; j0 += 2 * NW) {
+    const int j = j0 + (lane >> 4), w = lane & 15;
+    const bool ok = j < E;
+    const int v = ok ? whist[w * EW + j] : 0;
+    int incl = v;
+#pragma unroll
+    for (int o = 1; o < 16; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o, 16);
+      if (w >= o) incl += y;
     }
-  if (bad) atomicOr(p.err, kErrBadExpert);
+    if (ok) {
+      whist[w * EW + j] = incl - v;
+      if (w == 15) colcnt[j] = incl;
+    }
+  }
+  // tokens per rank: count each rank's bit over the token masks
+  for (int r = warp; r < W; r += NW) {
+    int c = 0;
+    for (int t = lane; t - lane < ntok; t += 32) {
+      const unsigned long long m = t < ntok ? tmask[t] : 0ull;
+      c += __popc(__ballot_sync(0xffffffffu, (m >> r) & 1ull));
+    }
+    if (lane == 0) colcnt[E + r] = c;
+  }
+}
+
+// Each counted entry's rank among all of its range's entries of its expert
+// (the slots' offset inside the range), written to loc[i] (-1 when skipped).
+// After a barrier that follows count_tokens.
+template <int KC>
+__device__ __forceinline__ void write_range_ranks(int ntok, int K, const int32_t* whist, int EW,
+                                                  const CountRegs<KC>& regs, int32_t* loc) {
+  constexpr int NW = kLayoutCountWarps;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nent = ntok * K;
+  const int per_warp = (((nent + NW - 1) / NW) + 31) & ~31;
+  const int wbeg = warp * per_warp;
+  const int wend = min(nent, wbeg + per_warp);
+#pragma unroll
+  for (int b = 0; b < CountBatches<KC>(); ++b) {
+    if (b * 32 >= per_warp) break;
+    const int i = wbeg + b * 32 + lane;
+    if (i < wend) {
+      const int e = regs.e[b];
+      loc[i] = e >= 0 ? whist[warp * EW + e] + regs.loc[b] : -1;
+    }
+  }
+}
+
+// Shared-memory words of the counting scratch (whist, tmask as 64-bit words,
+// colcnt) for E+W columns and up to tpb tokens.
+__host__ __device__ constexpr int CountSmemWords(int EW, int tpb) {
+  return kLayoutCountWarps * EW + 2 * tpb + EW;
 }
 
 template <int KC>
-__global__ void __launch_bounds__(kCountThreads) ep_layout_count_kernel(LayoutParams p) {
+__global__ void __launch_bounds__(kCountThreads, KC ? kCountMinBlocks : 2) ep_layout_count_kernel(LayoutParams p) {
   const int K = KC ? KC : p.topk;
   const int EW = p.num_experts + p.world_size;
-  const int C = p.num_chunks;
-  extern __shared__ int32_t sm[];
-  int32_t* whist = sm;                                      // [NW][EW]
-  int32_t* colcnt = whist + kLayoutCountWarps * EW;         // [EW]
-  int32_t* ids = colcnt + EW;                               // [TPC*K]
+  extern __shared__ __align__(16) int32_t sm[];
+  auto* tmask = reinterpret_cast<unsigned long long*>(sm);   // [TPC]
+  int32_t* whist = sm + 2 * kLayoutTPC;                      // [NW][EW]
+  int32_t* colcnt = whist + kLayoutCountWarps * EW;          // [EW]
   const int c = blockIdx.x;
   const int t0 = c * kLayoutTPC;
   const int ntok = min(p.num_tokens, t0 + kLayoutTPC) - t0;
   allow_dependent_grids();
-  count_tokens<KC>(p, t0, ntok, whist, ids, colcnt,
-                   p.no_expand ? nullptr : p.dst_slot + static_cast<int64_t>(t0) * K);
-  for (int j = threadIdx.x; j < EW; j += kCountThreads)
-    p.chunk_hist[static_cast<int64_t>(j) * C + c] = colcnt[j];
+  CountRegs<KC> regs;
+  count_tokens<KC>(p, t0, ntok, whist, tmask, colcnt, nullptr, regs);
+  __syncthreads();
+  // the range ranks go to dst_slot, which the slots kernel turns into slots
+  if (!p.no_expand)
+    write_range_ranks<KC>(ntok, K, whist, EW, regs, p.dst_slot + static_cast<int64_t>(t0) * K);
+  // the range's column totals: a contiguous row of the [C][E+W] table (read
+  // by the slots kernel) and a column entry of the [E+W][C] copy (read by the
+  // spine, one column per warp)
+  for (int j = threadIdx.x; j < EW; j += kCountThreads) {
+    p.chunk_hist[static_cast<int64_t>(c) * EW + j] = colcnt[j];
+    p.chunk_hist_cols[static_cast<int64_t>(j) * p.num_chunks + c] = colcnt[j];
+  }
 }
 
 // ---------------------------------------------------------------- spine
 
-// A warp per column j of the [E+W][C] table: exclusive scan over the C chunks
+// A warp per column j of the [C][E+W] table: exclusive scan over the C chunks
 // (each lane a contiguous run of chunks, kept in registers when short).
 __global__ void __launch_bounds__(kSpineWarps * 32) ep_layout_spine_kernel(LayoutParams p) {
   const int EW = p.num_experts + p.world_size;
@@ -345,8 +439,11 @@ __global__ void __launch_bounds__(kSpineWarps * 32) ep_layout_spine_kernel(Layou
   allow_dependent_grids();
   grid_dependency_wait();
   if (j >= EW) return;
-  const int32_t* in = p.chunk_hist + static_cast<int64_t>(j) * C;
-  int32_t* out = p.chunk_off + static_cast<int64_t>(j) * C;
+  // column j: read contiguously from the [E+W][C] copy, written into the
+  // row-major [C][E+W] offsets table that the slots kernel reads by rows
+  const int32_t* in = p.chunk_hist_cols + static_cast<int64_t>(j) * C;
+  int32_t* out = p.chunk_off + j;
+  const int64_t ld = EW;
   constexpr int kRegRun = 8;
   const int V = (C + 31) / 32;
   const int cbeg = min(C, lane * V), cend = min(C, cbeg + V);
@@ -372,13 +469,13 @@ __global__ void __launch_bounds__(kSpineWarps * 32) ep_layout_spine_kernel(Layou
 #pragma unroll
     for (int u = 0; u < kRegRun; ++u)
       if (cbeg + u < cend) {
-        out[cbeg + u] = run;
+        out[(cbeg + u) * ld] = run;
         run += reg[u];
       }
   } else {
     for (int c = cbeg; c < cend; ++c) {
       const int v = in[c];
-      out[c] = run;
+      out[c * ld] = run;
       run += v;
     }
   }
@@ -405,44 +502,35 @@ __device__ void write_outputs_expand(const LayoutParams& p, const int32_t* cnt_s
 }
 
 // Slots and metadata of the tokens [t0, t0 + ntok) of this CTA (expand
-// layout; all threads call, token t0 + i is owned by thread i).  psum_s [E+1]
-// is the aligned expert prefix, co[E] the range's offset inside each expert's
-// rows, cx[E+1] the exclusive scan over experts of the range's counts, loc the
-// stable rank of each entry within the range (count_tokens; may alias
-// p.dst_slot, which is overwritten with the slots), ids the staged expert ids
-// or nullptr (then read from topk_idx).  Scratch: slots_s and sorted [ntok*K],
-// src [2*ntok].
+// layout; all threads call, entry i = (t - t0)*K + k spread over all of them).
+// psum_s [E+1] is the aligned expert prefix, co[E] the range's offset inside
+// each expert's rows, cx[E+1] the exclusive scan over experts of the range's
+// counts, loc[i] the entry's rank among the range's entries of its expert
+// (may alias p.dst_slot of the range, which is overwritten with the slots),
+// ids[i] the staged expert ids or nullptr (then read from topk_idx).
+// Scratch: slots_s and sorted [ntok*K], src [2*ntok].
 template <int KC>
 __device__ void slots_expand_tokens(const LayoutParams& p, int t0, int ntok, const int32_t* psum_s,
                                     const int32_t* co, const int32_t* cx, const int32_t* loc,
                                     const int32_t* ids, int32_t* slots_s, int32_t* sorted,
                                     int32_t* src) {
-  constexpr int KM = KC ? KC : kMaxTopk;
   const int K = KC ? KC : p.topk;
   const int KW = K + 2;  // metadata row width
   const int E = p.num_experts, T = p.max_tok_per_rank;
   const int nthr = blockDim.x;
-  if (threadIdx.x < ntok) {
-    const int tl = threadIdx.x, t = t0 + tl;
-    const int64_t* row = p.topk_idx + static_cast<int64_t>(t) * K;
-    int32_t* ds = p.dst_slot + static_cast<int64_t>(t) * K;
-    int32_t slot[KM];
-#pragma unroll
-    for (int k = 0; k < KM; ++k) {
-      if (k < K) {
-        const int e = ids ? ids[tl * K + k] : expert_of(row[k], E);
-        const int l = loc[tl * K + k];
-        slot[k] = e >= 0 ? psum_s[e] + co[e] + l : -1;
-        if (e >= 0) sorted[cx[e] + l] = tl * K + k;
-      }
-    }
-#pragma unroll
-    for (int k = 0; k < KM; ++k)
-      if (k < K) {
-        ds[k] = slot[k];
-        slots_s[tl * K + k] = slot[k];
-      }
-    const int r = t / T;
+  const int nent = ntok * K;
+  int32_t* ds = p.dst_slot + static_cast<int64_t>(t0) * K;
+  const int64_t* topk = p.topk_idx + static_cast<int64_t>(t0) * K;
+  for (int i = threadIdx.x; i < nent; i += nthr) {
+    const int e = ids ? ids[i] : expert_of(topk[i], E);
+    const int l = loc[i];  // read before ds[i] (possibly the same word) is overwritten
+    const int slot = e >= 0 ? psum_s[e] + co[e] + l : -1;
+    if (e >= 0) sorted[cx[e] + l] = i;
+    ds[i] = slot;
+    slots_s[i] = slot;
+  }
+  for (int tl = threadIdx.x; tl < ntok; tl += nthr) {
+    const int t = t0 + tl, r = t / T;
     src[2 * tl] = r;
     src[2 * tl + 1] = t - r * T;
   }
@@ -476,18 +564,20 @@ __device__ void slots_expand_tokens(const LayoutParams& p, int t0, int ntok, con
 }
 
 // -1 into the rows that receive nothing, share `part` of `parts`: the padding
-// of experts e = part, part + parts, ... (cnt_s non-null: expand layout) and a
-// slice of [R, capacity).
+// rows of the experts (cnt_s non-null: expand layout; a warp per expert, none
+// when A == 1) and a slice of [R, capacity).
 __device__ void fill_unreceived(const LayoutParams& p, const int32_t* psum_s, const int32_t* cnt_s,
                                 int R, int part, int parts) {
   const int KW = p.topk + 2;
   const int nthr = blockDim.x;
-  if (cnt_s != nullptr)
-    for (int e = part; e < p.num_experts; e += parts) {
+  if (cnt_s != nullptr && p.alignment > 1) {
+    const int lane = threadIdx.x & 31, nwarp = nthr >> 5;
+    for (int e = part * nwarp + (threadIdx.x >> 5); e < p.num_experts; e += parts * nwarp) {
       const int64_t beg = static_cast<int64_t>(psum_s[e] + cnt_s[e]) * KW;
       const int64_t end = static_cast<int64_t>(psum_s[e + 1]) * KW;
-      for (int64_t f = beg + threadIdx.x; f < end; f += nthr) p.meta[f] = -1;
+      for (int64_t f = beg + lane; f < end; f += 32) p.meta[f] = -1;
     }
+  }
   const int64_t tail_beg = static_cast<int64_t>(R) * KW;
   const int64_t tail_words = p.rcap * KW - tail_beg;
   const int64_t per = (tail_words + parts - 1) / parts;
@@ -497,10 +587,10 @@ __device__ void fill_unreceived(const LayoutParams& p, const int32_t* psum_s, co
 }
 
 template <int KC>
-__global__ void __launch_bounds__(kSlotThreads) ep_layout_slots_kernel(LayoutParams p) {
+__global__ void __launch_bounds__(kSlotThreads, 1) ep_layout_slots_kernel(LayoutParams p) {
   const int K = KC ? KC : p.topk;
   const int E = p.num_experts, C = p.num_chunks;
-  extern __shared__ int32_t sm[];
+  extern __shared__ __align__(16) int32_t sm[];
   int32_t* psum_s = sm;                   // [E+1]
   int32_t* cnt_s = psum_s + E + 1;        // [E]
   int32_t* cl = cnt_s + E;                // [E]   this chunk's count per expert
@@ -515,11 +605,12 @@ __global__ void __launch_bounds__(kSlotThreads) ep_layout_slots_kernel(LayoutPar
   const bool has_tokens = c < C;
   allow_dependent_grids();   // the dispatch that follows may be scheduled now
   grid_dependency_wait();
+  const int64_t row = static_cast<int64_t>(c) * (E + p.world_size);  // this chunk's table row
   for (int e = threadIdx.x; e < E; e += kSlotThreads) {
     cnt_s[e] = p.col_total[e];
     if (has_tokens) {
-      cl[e] = p.chunk_hist[static_cast<int64_t>(e) * C + c];
-      co[e] = p.chunk_off[static_cast<int64_t>(e) * C + c];
+      cl[e] = p.chunk_hist[row + e];
+      co[e] = p.chunk_off[row + e];
     }
   }
   __syncthreads();
@@ -666,11 +757,11 @@ __host__ __device__ constexpr int NonExpandScratchWords(int tpb, int K, int W) {
 }
 
 template <int KC>
-__global__ void __launch_bounds__(kSlotThreads) ep_layout_slots_ne_kernel(LayoutParams p) {
+__global__ void __launch_bounds__(kSlotThreads, 1) ep_layout_slots_ne_kernel(LayoutParams p) {
   const int K = KC ? KC : p.topk;
   const int E = p.num_experts, W = p.world_size, C = p.num_chunks;
   const int RM = K < W ? K : W;
-  extern __shared__ int32_t sm[];
+  extern __shared__ __align__(16) int32_t sm[];
   int2* sorted = reinterpret_cast<int2*>(sm);          // [TPC*RM]
   int32_t* woff = sm + 2 * kLayoutTPC * RM;            // [TPC/32][W]
   int32_t* dslot = woff + (kLayoutTPC / 32) * W;       // [TPC*K]
@@ -689,11 +780,12 @@ __global__ void __launch_bounds__(kSlotThreads) ep_layout_slots_ne_kernel(Layout
   const int tid = threadIdx.x, warp = tid >> 5;
   allow_dependent_grids();   // the dispatch that follows may be scheduled now
   grid_dependency_wait();
+  const int64_t row = static_cast<int64_t>(c) * (E + W);  // this chunk's table row
   for (int r = tid; r < W; r += kSlotThreads) {
     tpr[r] = p.col_total[E + r];
     if (has_tokens) {
-      rcl[r] = p.chunk_hist[static_cast<int64_t>(E + r) * C + c];
-      rbase[r] = p.chunk_off[static_cast<int64_t>(E + r) * C + c];
+      rcl[r] = p.chunk_hist[row + E + r];
+      rbase[r] = p.chunk_off[row + E + r];
     }
   }
   __syncthreads();
@@ -725,6 +817,7 @@ __global__ void __launch_bounds__(kSlotThreads) ep_layout_slots_ne_kernel(Layout
 __host__ __device__ constexpr int ClusterSmemWords(int E, int W, int K, int tpb, bool ne) {
   const int EW = E + W;
   return (ne ? NonExpandScratchWords(tpb, K, W) : 0)      // non-expand scratch (first: int2)
+         + 2 * tpb                                        // tmask (64-bit words)
          + kLayoutCountWarps * EW + 3 * EW                // whist, colcnt, tot, off
          + tpb * K                                        // ids
          + (ne ? 0 : 3 * tpb * K + 2 * tpb)               // loc, slots_s, sorted, src (expand)
@@ -733,10 +826,10 @@ __host__ __device__ constexpr int ClusterSmemWords(int E, int W, int K, int tpb,
 }
 
 template <int KC, bool NE>
-__global__ void __launch_bounds__(kClusterThreads) ep_layout_cluster_kernel(LayoutParams p, int tpb) {
+__global__ void __launch_bounds__(kClusterThreads, 1) ep_layout_cluster_kernel(LayoutParams p, int tpb) {
   const int K = KC ? KC : p.topk;
   const int E = p.num_experts, W = p.world_size, EW = E + W;
-  extern __shared__ int32_t sm[];
+  extern __shared__ __align__(16) int32_t sm[];
   int32_t* base = sm;
   int2* sorted_ne = reinterpret_cast<int2*>(sm);               // NE: [tpb*RM]
   int32_t* woff = nullptr;
@@ -749,6 +842,8 @@ __global__ void __launch_bounds__(kClusterThreads) ep_layout_cluster_kernel(Layo
     src_ne = dslot + tpb * K;                                  // [2*tpb]
     base = src_ne + 2 * tpb;
   }
+  auto* tmask = reinterpret_cast<unsigned long long*>(base);   // [tpb] (8-byte aligned: even offset)
+  base += 2 * tpb;
   int32_t* whist = base;                                       // [NW][EW]
   int32_t* colcnt = whist + kLayoutCountWarps * EW;            // [EW] this CTA's totals (read remotely)
   int32_t* tot = colcnt + EW;                                  // [EW] totals over the cluster
@@ -769,12 +864,14 @@ __global__ void __launch_bounds__(kClusterThreads) ep_layout_cluster_kernel(Layo
   allow_dependent_grids();   // the dispatch that follows may be scheduled now
   const int t0 = static_cast<int>(me) * tpb;
   const int ntok = max(0, min(p.num_tokens, t0 + tpb) - t0);
-  count_tokens<KC>(p, t0, ntok, whist, ids, colcnt, NE ? nullptr : loc);
+  CountRegs<KC> regs;
+  count_tokens<KC>(p, t0, ntok, whist, tmask, colcnt, ids, regs);
 
   // every CTA's column totals are complete: gather the cluster's totals and
   // this CTA's offsets from the other CTAs' shared memory
   cluster_arrive();
   cluster_wait();
+  if constexpr (!NE) write_range_ranks<KC>(ntok, K, whist, EW, regs, loc);
   for (int j = threadIdx.x; j < EW; j += kClusterThreads) {
     int v[kClusterCtas];
 #pragma unroll
@@ -837,9 +934,8 @@ cudaError_t launch_dependent(Kern kernel, int grid, int block, size_t smem, cuda
   return cudaLaunchKernelEx(&cfg, kernel, p);
 }
 
-size_t count_smem(int topk, int cols) {
-  return sizeof(int32_t) * (static_cast<size_t>(kLayoutCountWarps) * cols + cols +
-                            static_cast<size_t>(kLayoutTPC) * topk);
+size_t count_smem(int, int cols) {
+  return sizeof(int32_t) * static_cast<size_t>(CountSmemWords(cols, kLayoutTPC));
 }
 
 size_t slots_smem(int E, int topk) {
@@ -961,13 +1057,14 @@ cudaError_t prepare_layout(int, int, int, LaunchGeom* g) {
 bool LayoutUsesCluster(const LayoutParams& p, const LaunchGeom& g) { return cluster_tpb(p, g) > 0; }
 
 int64_t LayoutScratchInts(int max_chunks, int columns) {
-  return 2LL * columns * (max_chunks > 0 ? max_chunks : 1) + columns;
+  return 3LL * columns * (max_chunks > 0 ? max_chunks : 1) + columns;
 }
 
 void BindLayoutScratch(LayoutParams* p, int32_t* base, int max_chunks, int columns) {
   const int64_t cap = max_chunks > 0 ? max_chunks : 1;
   p->chunk_hist = base;
-  p->chunk_off = base + static_cast<int64_t>(columns) * cap;
+  p->chunk_hist_cols = base + static_cast<int64_t>(columns) * cap;
+  p->chunk_off = p->chunk_hist_cols + static_cast<int64_t>(columns) * cap;
   p->col_total = p->chunk_off + static_cast<int64_t>(columns) * cap;
 }
 

@@ -141,7 +141,7 @@ extern "C" int ep_layout_noalloc(const ep_cfg_t* cfg, const int64_t* topk_idx, i
       char buf[320];
       std::snprintf(buf, sizeof buf,
                     "ep_layout_noalloc: %d tokens over %d experts + %d ranks need %lld int32 of "
-                    "scratch (2*(E+W)*ceil(N/%d) + (E+W)); the static scratch holds %lld",
+                    "scratch (3*(E+W)*ceil(N/%d) + (E+W)); the static scratch holds %lld",
                     num_tokens, E, W, static_cast<long long>(need), kLayoutTPC,
                     static_cast<long long>(kNoAllocScratchInts));
       return RecordError(EP_EINVAL, buf);

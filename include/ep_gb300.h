@@ -231,9 +231,9 @@ int ep_combine(ep_handle_t h, const void *y, const float *topk_weights, void *ou
  *   recv_src_metadata         device int32 [Rcap, K+2] (8-byte aligned when K is even)
  *   device_error              device int32 [1]; cleared, then error bits as in
  *                             ep_handle_status (value 1 (bit 0): an id outside [-1, E) was skipped)
- * Size limit: 2*(E+W)*ceil(num_tokens/128) + (E+W) int32 of scratch must fit
+ * Size limit: 3*(E+W)*ceil(num_tokens/128) + (E+W) int32 of scratch must fit
  * in 262144 (for example 32768 tokens over 256 experts and 8 ranks need
- * 135432); larger requests return EP_EINVAL with the sizes in the message.
+ * 203016); larger requests return EP_EINVAL with the sizes in the message.
  * The first call on a device, with that device current, looks up the
  * scratch array's address and sets the layout kernels' shared-memory limit
  * on that device; make that first call before any stream capture.  That

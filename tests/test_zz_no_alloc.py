@@ -109,11 +109,11 @@ def test_noalloc_empty_batch_and_small_large_small(gpu):
 @pytest.mark.gpu
 def test_noalloc_at_the_scratch_limit_matches_the_oracle(gpu):
     """The largest batch the static scratch admits for 256 experts over 8 ranks:
-    2*(E+W)*ceil(N/128) + (E+W) <= 262144 gives ceil(N/128) <= 495, N = 63360.
+    3*(E+W)*ceil(N/128) + (E+W) <= 262144 gives ceil(N/128) <= 330, N = 42240.
     Compared with the CPU oracle directly; one token more is rejected."""
-    wl = synth.WORKLOADS["prefill_bf16"].with_(max_tok_per_rank=7936, num_tokens=63360)
+    wl = synth.WORKLOADS["prefill_bf16"].with_(max_tok_per_rank=5288, num_tokens=42240)
     E, W = wl.num_experts, wl.world_size
-    assert 2 * (E + W) * 495 + (E + W) <= 262144 < 2 * (E + W) * 496 + (E + W)
+    assert 3 * (E + W) * 330 + (E + W) <= 262144 < 3 * (E + W) * 331 + (E + W)
     topk = synth.gen_topk(wl, mask_frac=0.01)
     out = noalloc_outputs(wl, wl.num_tokens)
     ep.ep_layout_noalloc(cfg_of(wl), topk.cuda(), out)
@@ -127,8 +127,8 @@ def test_noalloc_at_the_scratch_limit_matches_the_oracle(gpu):
     for k, v in want.items():
         assert np.array_equal(out[k].cpu().numpy(), np.asarray(v)), k
     assert int(out["device_error"].cpu()[0]) == 0
-    # one token past the limit: 496 chunks
-    over = wl.with_(num_tokens=63361)
+    # one token past the limit: 331 chunks
+    over = wl.with_(num_tokens=42241)
     big = noalloc_outputs(over, over.num_tokens)
     with pytest.raises(ep.EpError) as e:
         ep.ep_layout_noalloc(cfg_of(over), synth.gen_topk(over).cuda(), big)
@@ -148,7 +148,7 @@ def test_noalloc_reports_bad_expert_ids(gpu):
 
 
 def test_noalloc_rejects_requests_beyond_the_static_scratch():
-    # 64 ranks x 32 experts and 16384 tokens: 2*(2048+64)*128 + 2112 int32 > 262144
+    # 64 ranks x 32 experts and 16384 tokens: 3*(2048+64)*128 + 2112 int32 > 262144
     cfg = ep.make_cfg(64, 1024, 256, 32, 8, 1, "bf16", True)
     L = ep.load_library()
     dummy = ctypes.c_void_p(256)          # never dereferenced: the size check comes first
