@@ -76,6 +76,20 @@ __device__ __forceinline__ void st_f32(void* p, const float (&acc)[2 * V]) {
   st_stream<V>(static_cast<uint8_t*>(p) + 4 * V, b);
 }
 
+// a[k] for a runtime k of a small register array (a compile-time unrolled
+// select, so the array stays in registers)
+template <int N, class T>
+__device__ __forceinline__ T pick(const T (&a)[N], int k) {
+  T r = a[0];
+#pragma unroll
+  for (int i = 1; i < N; ++i) r = k == i ? a[i] : r;
+  return r;
+}
+template <int N>
+__device__ __forceinline__ int32_t slot_at(const int32_t (&a)[N], int k) { return pick<N>(a, k); }
+template <int N>
+__device__ __forceinline__ float w_at(const float (&a)[N], int k) { return pick<N>(a, k); }
+
 template <int HC, int KC, bool WEIGHTED, int V, bool BIAS, bool F32>
 __device__ __forceinline__ void combine_body(const CombineParams& p) {
   constexpr int KM = KC ? KC : kMaxTopk;
@@ -92,6 +106,7 @@ __device__ __forceinline__ void combine_body(const CombineParams& p) {
 
   int32_t slot[KM];
   float w[KM];
+  bool all = true;  // every entry of the token is routed
 #pragma unroll
   for (int k = 0; k < KM; ++k) {
     slot[k] = -1;
@@ -99,27 +114,20 @@ __device__ __forceinline__ void combine_body(const CombineParams& p) {
     if (k < K) {
       slot[k] = ld_coherent(p.dst_slot + static_cast<int64_t>(t) * K + k);
       if (WEIGHTED) w[k] = ld_coherent(p.weights + static_cast<int64_t>(t) * K + k);
+      all &= slot[k] >= 0;
     }
   }
   const uint8_t* y = static_cast<const uint8_t*>(p.y);
   const uint8_t* bias = BIAS ? static_cast<const uint8_t*>(p.bias) + static_cast<int64_t>(t) * row
                              : nullptr;
   uint8_t* out = static_cast<uint8_t*>(p.out) + static_cast<int64_t>(t) * (F32 ? 2 * row : row);
-  for (int c = threadIdx.x; c < chunks; c += kCombineThreads) {
-    Vec<V> v[KM];
-#pragma unroll
-    for (int k = 0; k < KM; ++k)
-      if (slot[k] >= 0)
-        ld_stream<V>(y + static_cast<int64_t>(slot[k]) * row + static_cast<int64_t>(c) * UNIT, v[k]);
-    Vec<V> bv;
-    if (BIAS) ld_stream<V>(bias + static_cast<int64_t>(c) * UNIT, bv);
-    float acc[2 * V];
-#pragma unroll
-    for (int i = 0; i < 2 * V; ++i) acc[i] = 0.0f;
-#pragma unroll
-    for (int k = 0; k < KM; ++k)
-      if (slot[k] >= 0) fold<V>(acc, v[k], w[k], WEIGHTED);
-    if (BIAS) fold<V>(acc, bv, 1.0f, false);  // one fp32 addition after the fold
+  // bias (one fp32 addition after the fold) and the store of one chunk
+  auto finish = [&](int c, float (&acc)[2 * V]) {
+    if (BIAS) {
+      Vec<V> bv;
+      ld_stream<V>(bias + static_cast<int64_t>(c) * UNIT, bv);
+      fold<V>(acc, bv, 1.0f, false);
+    }
     if (F32) {
       st_f32<V>(out + static_cast<int64_t>(c) * 2 * UNIT, acc);
     } else {
@@ -127,6 +135,49 @@ __device__ __forceinline__ void combine_body(const CombineParams& p) {
 #pragma unroll
       for (int i = 0; i < V; ++i) o.w[i] = pack_bf16x2(acc[2 * i], acc[2 * i + 1]);
       st_stream<V>(out + static_cast<int64_t>(c) * UNIT, o);
+    }
+  };
+  if (KC != 0 && all) {
+    // the common case, a token with all K entries routed: every row load of a
+    // chunk in flight and no per-entry branch.  (Branches around the loads make
+    // the compiler keep all K loaded vectors live at once: 96-128 registers
+    // instead of ~56, hence fewer resident CTAs; a decode batch of 1024 tokens
+    // then needs a second, latency-bound wave.)
+    for (int c = threadIdx.x; c < chunks; c += kCombineThreads) {
+      Vec<V> v[KM];
+#pragma unroll
+      for (int k = 0; k < KM; ++k)
+        ld_stream<V>(y + static_cast<int64_t>(slot[k]) * row + static_cast<int64_t>(c) * UNIT, v[k]);
+      float acc[2 * V];
+#pragma unroll
+      for (int i = 0; i < 2 * V; ++i) acc[i] = 0.0f;
+#pragma unroll
+      for (int k = 0; k < KM; ++k) fold<V>(acc, v[k], w[k], WEIGHTED);
+      finish(c, acc);
+    }
+  } else {
+    // tokens with a masked entry, and the runtime-top-k variant: the routed
+    // rows in k order, four loads in flight at a time
+    for (int c = threadIdx.x; c < chunks; c += kCombineThreads) {
+      float acc[2 * V];
+#pragma unroll
+      for (int i = 0; i < 2 * V; ++i) acc[i] = 0.0f;
+#pragma unroll 1
+      for (int k0 = 0; k0 < K; k0 += 4) {
+        Vec<V> v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int k = k0 + u;
+          const int32_t sk = k < K ? slot_at(slot, k) : -1;
+          if (sk >= 0) ld_stream<V>(y + static_cast<int64_t>(sk) * row + static_cast<int64_t>(c) * UNIT, v[u]);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int k = k0 + u;
+          if (k < K && slot_at(slot, k) >= 0) fold<V>(acc, v[u], w_at(w, k), WEIGHTED);
+        }
+      }
+      finish(c, acc);
     }
   }
 }
