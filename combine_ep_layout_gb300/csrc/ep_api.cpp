@@ -121,6 +121,7 @@ struct ep_handle {
   Variant<DispatchLaunch> dispatch{};
   Variant<CombineLaunch> combine{};
   LaunchGeom g_layout{}, g_dispatch{}, g_combine{};
+  uint64_t wait_ns = kDefaultWaitNs;  // bound of a device-side wait (EP_GB300_WAIT_NS)
   // run-time specialisations for shapes outside the compiled table (function
   // null when not used); they serve 32-byte-aligned buffers, the compiled
   // generic variant everything else
@@ -209,15 +210,22 @@ int create_handle(const ep_cfg_t* cfg, ep_handle* src, ep_handle_t* out) {
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, h->device);
     if (e != cudaSuccess) return bail(fail_cuda(e, "cudaDeviceGetAttribute"));
 
+    const EpDType dt = static_cast<EpDType>(cfg->dispatch_dtype);
+    const int row_bytes = static_cast<int>(RowBytes(h->H, dt));
     h->layout = FindLayout(h->K, h->no_expand);
-    h->dispatch = FindDispatch(h->H, h->K, static_cast<EpDType>(cfg->dispatch_dtype));
+    h->dispatch = FindDispatch(h->H, h->K, dt);
+    if (DispatchTmaRequested()) {  // rows staged through shared memory by TMA bulk copies
+      const Variant<DispatchLaunch> tma = FindDispatchTma(dt, row_bytes);
+      if (tma.launch) h->dispatch = tma;
+    }
+    h->wait_ns = WaitLimitNs();
     h->combine = FindCombine(h->H, h->K, cfg->use_weights != 0);
     if (!h->dispatch.launch) return bail(fail(EP_EUNSUPPORTED, "no dispatch kernel for this dtype"));
     h->g_layout.num_sms = h->g_dispatch.num_sms = h->g_combine.num_sms = sms;
     const int cols = h->E + h->W;
     if ((e = h->layout.prepare(h->H, h->K, cols, &h->g_layout)) != cudaSuccess)
       return bail(fail_cuda(e, "layout kernel set-up"));
-    if ((e = h->dispatch.prepare(h->H, h->K, 0, &h->g_dispatch)) != cudaSuccess)
+    if ((e = h->dispatch.prepare(h->H, h->K, row_bytes, &h->g_dispatch)) != cudaSuccess)
       return bail(fail_cuda(e, "dispatch kernel set-up"));
     if (h->g_dispatch.blocks_per_sm < 1)
       return bail(fail(EP_EUNSUPPORTED, "dispatch kernel does not fit on an SM for this hidden_dim"));
@@ -406,6 +414,7 @@ int ep_dispatch_fwd(ep_handle_t h, const void* x, void* recv_x, float* recv_scal
     p.topk_i32 = o->topk_i32;
     p.recv_topk_weights = recv_topk_weights;
     p.recv_topk_idx = recv_topk_idx;
+    p.wait_ns = h->wait_ns;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const bool jit_ok = h->jit_dispatch.function && aligned32(x) && aligned32(recv_x);
     cudaError_t e = jit_ok ? jit::Launch(h->jit_dispatch, p.num_tokens, &p, s)

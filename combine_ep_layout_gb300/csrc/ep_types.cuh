@@ -83,7 +83,13 @@ struct DispatchParams {
   // non-expand layout: dst_slot above holds the token's distinct rows and this
   // the row of each (t, k); nullptr for the expand layout
   const int32_t* entry_slot;   // [N, K]
+  // bound of one wait on the TMA dispatch's mbarriers (ns; 0: give up at the
+  // first test that finds the copy still in flight)
+  uint64_t wait_ns;
 };
+
+// Default bound of a bounded device-side wait: one second.
+constexpr uint64_t kDefaultWaitNs = 1000000000ull;
 
 struct CombineParams {
   const void* y;             // bf16 [Rcap, H]
