@@ -43,7 +43,8 @@ KERNEL_FILES = {"ep_dispatch_copy_kernel": ["ep_dispatch_body.cuh", "ep_dispatch
                 "ep_combine_kernel": ["ep_combine_body.cuh", "ep_combine.cu"],
                 "ep_layout_count_kernel": ["ep_layout.cu"],
                 "ep_layout_spine_kernel": ["ep_layout.cu"],
-                "ep_layout_slots_kernel": ["ep_layout.cu"]}
+                "ep_layout_slots_kernel": ["ep_layout.cu"],
+                "ep_layout_fused_kernel": ["ep_layout.cu"]}
 
 
 # GPU cycles of the pre-roll sleep before each --all-configs step (~100 us at 2 GHz)
@@ -375,7 +376,9 @@ def run_ours(args, rank, local_rank, world):
     stream.synchronize()
     assert h16.status() == 0 and h8.status() == 0
     # kernels per step: the layout is one cluster launch for small batches, else three
-    launches_per_step = (1 if "_cluster_" in h16.variant(0) else 3) + 3   # timed steps only
+    # the layout is one launch (cluster or fused kernel) or three
+    single = "_cluster_" in h16.variant(0) or "_fused_" in h16.variant(0)
+    launches_per_step = (1 if single else 3) + 3   # timed steps only
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     # the timed region: exactly K steps, events only at its two ends, so that
     # each kernel's programmatic dependent launch overlaps its predecessor's tail

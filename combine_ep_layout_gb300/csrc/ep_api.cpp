@@ -112,12 +112,12 @@ struct ep_handle {
   ep_handle* src = nullptr;
   int32_t *cnt = nullptr, *tok_per_rank = nullptr, *psum_expert = nullptr, *psum_rank = nullptr,
           *num_recv = nullptr, *err = nullptr, *dst_slot = nullptr, *meta = nullptr,
-          *topk_i32 = nullptr, *scratch = nullptr;
+          *topk_i32 = nullptr, *scratch = nullptr, *fused = nullptr;
   // rows each token is written to / read from: dst_slot for the expand layout,
   // the token's distinct rank rows for the non-expand one
   int32_t* send_slot = nullptr;
   Variant<LayoutLaunch> layout{};
-  std::string layout_ran;  // kernel name of the last ep_layout (cluster or three launches)
+  std::string layout_ran;  // kernel name of the last ep_layout (cluster, fused or three launches)
   Variant<DispatchLaunch> dispatch{};
   Variant<CombineLaunch> combine{};
   LaunchGeom g_layout{}, g_dispatch{}, g_combine{};
@@ -223,6 +223,8 @@ int create_handle(const ep_cfg_t* cfg, ep_handle* src, ep_handle_t* out) {
     if (!h->dispatch.launch) return bail(fail(EP_EUNSUPPORTED, "no dispatch kernel for this dtype"));
     h->g_layout.num_sms = h->g_dispatch.num_sms = h->g_combine.num_sms = sms;
     const int cols = h->E + h->W;
+    h->g_layout.layout_experts = h->E;
+    h->g_layout.layout_world = h->W;
     if ((e = h->layout.prepare(h->H, h->K, cols, &h->g_layout)) != cudaSuccess)
       return bail(fail_cuda(e, "layout kernel set-up"));
     if ((e = h->dispatch.prepare(h->H, h->K, row_bytes, &h->g_dispatch)) != cudaSuccess)
@@ -251,7 +253,8 @@ int create_handle(const ep_cfg_t* cfg, ep_handle* src, ep_handle_t* out) {
     const size_t n_meta = al(4 * static_cast<size_t>(h->rcap) * (h->K + 2));
     const size_t n_scr = al(sizeof(int32_t) * static_cast<size_t>(LayoutScratchInts(h->max_chunks, cols)));
     const size_t n_send = h->no_expand ? n_slot : 0;
-    const size_t total = n_small + 2 * n_slot + n_meta + n_scr + n_send;
+    const size_t n_fused = al(sizeof(int32_t) * static_cast<size_t>(LayoutFusedStateInts(h->max_chunks, cols)));
+    const size_t total = n_small + 2 * n_slot + n_meta + n_scr + n_send + n_fused;
     // Stream-ordered allocation on a private non-blocking stream: creating a
     // handle waits for nothing but its own clearing memset, never for work on
     // the caller's other streams (cudaMalloc and cudaDeviceSynchronize may wait
@@ -279,6 +282,7 @@ int create_handle(const ep_cfg_t* cfg, ep_handle* src, ep_handle_t* out) {
     h->scratch = reinterpret_cast<int32_t*>(b + n_small + 2 * n_slot + n_meta);
     h->send_slot = h->no_expand ? reinterpret_cast<int32_t*>(b + n_small + 2 * n_slot + n_meta + n_scr)
                                 : h->dst_slot;
+    h->fused = reinterpret_cast<int32_t*>(b + n_small + 2 * n_slot + n_meta + n_scr + n_send);
     if ((e = cudaMemsetAsync(h->block, 0, total, h->own_stream)) != cudaSuccess)
       return bail(fail_cuda(e, "cudaMemsetAsync"));
     // the block is ready for any stream once this returns
@@ -355,12 +359,17 @@ int ep_layout(ep_handle_t h, const int64_t* topk_idx, int32_t num_tokens, ep_str
     p.topk_i32 = h->topk_i32;
     p.epr_magic = RankMagic(h->Epr);
     BindLayoutScratch(&p, h->scratch, h->max_chunks, h->E + h->W);
+    BindLayoutFusedState(&p, h->fused, h->max_chunks, h->E + h->W);
+    p.wait_ns = h->wait_ns;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    const bool cluster = LayoutUsesCluster(p, h->g_layout);
+    const LayoutPath path = LayoutPathOf(p, h->g_layout);
     cudaError_t e = h->layout.launch(p, h->g_layout, s);
     if (e != cudaSuccess) return fail_cuda(e, "layout launch");
     h->layout_ran = h->layout.name;
-    if (cluster) h->layout_ran.insert(h->layout_ran.rfind('_'), "_cluster");  // ..._cluster_k8
+    if (path == LayoutPath::kCluster)
+      h->layout_ran.insert(h->layout_ran.rfind('_'), "_cluster");  // ..._cluster_k8
+    else if (path == LayoutPath::kFused)
+      h->layout_ran.insert(h->layout_ran.rfind('_'), "_fused");    // ..._fused_k8
     h->num_tokens = num_tokens;
     h->last_stream = s;
     h->launched = true;

@@ -48,6 +48,15 @@ struct LayoutParams {
   int32_t* chunk_hist_cols;
   int32_t* chunk_off;
   int32_t* col_total;        // [E+W]
+  // state of the single-launch fused layout (BindLayoutFusedState; all nullptr:
+  // that path is not used).  EW8 = E+W rounded up to a multiple of 8.
+  uint32_t* fused_bar;       // [3] grid-barrier arrivals, their count when the launch began, launches so far
+  int32_t* fused_super;      // [2][fused_super_rows][EW8] superchunk sums, by launch parity
+  uint16_t* fused_rows;      // [max chunks][EW8] per-range column counts
+  int fused_super_rows;      // superchunk rows of one parity
+  int fused_max_ranges;      // ranges (CTAs) the state holds
+  int fused_tpb;             // tokens per CTA of the fused kernel (set by the launcher)
+  uint64_t wait_ns;          // bound of the fused kernel's grid-barrier wait
 };
 
 // Launch geometry of a variant on the current device, filled by its prepare
@@ -58,6 +67,14 @@ struct LaunchGeom {
   int cluster_ok;     // layout: the single-launch cluster kernel can be scheduled
   int row_slices;     // dispatch: CTAs per token row forced by EP_GB300_DISPATCH_SLICES (0: table)
   int pdl;            // dispatch / combine: launched with programmatic stream serialisation
+  // layout only: experts and ranks of the handle (set before prepare; 0 when
+  // unknown) and the fused kernel's resident CTAs per SM for them (0: that path
+  // is off, by EP_GB300_LAYOUT_FUSED=0 or because it does not fit)
+  int layout_experts;
+  int layout_world;
+  int fused_blocks_per_sm;
+  int fused_tpb;      // tokens per CTA of the fused kernel (0: chosen per launch)
+  int fused_max_super;  // superchunk rows the fused kernel's staging is sized for
 };
 
 // Programmatic dependent launch of the data kernels, unless EP_GB300_PDL=0
@@ -98,9 +115,11 @@ struct Variant {
 };
 
 Variant<LayoutLaunch> FindLayout(int topk, bool no_expand);
-// True when a layout launch with these parameters runs the single-launch
-// cluster kernel (small batches) rather than count / spine / slots.
-bool LayoutUsesCluster(const LayoutParams& p, const LaunchGeom& g);
+// Which kernels a layout launch with these parameters runs: the single-launch
+// cluster kernel (small batches), the single-launch fused kernel (a
+// cooperative grid, mid-size batches) or count / spine / slots.
+enum class LayoutPath { kLaunches = 0, kCluster = 1, kFused = 2 };
+LayoutPath LayoutPathOf(const LayoutParams& p, const LaunchGeom& g);
 Variant<DispatchLaunch> FindDispatch(int hidden, int topk, EpDType dtype);
 // The dispatch that stages rows through shared memory with TMA bulk copies
 // (byte-copy transports; null launch when the dtype or the row size is not
@@ -117,6 +136,13 @@ Variant<CombineLaunch> FindCombine(int hidden, int topk, bool use_weights);
 int64_t LayoutScratchInts(int max_chunks, int columns);
 // Point p's scratch fields into `base` (LayoutScratchInts(max_chunks, columns) words).
 void BindLayoutScratch(LayoutParams* p, int32_t* base, int max_chunks, int columns);
+// int32 words of the fused layout's state for up to max_chunks ranges of
+// kLayoutTPC tokens and `columns` = E+W columns (0 when max_chunks exceeds
+// what a cooperative grid can hold: that path is then never taken).
+int64_t LayoutFusedStateInts(int max_chunks, int columns);
+// Point p's fused-state fields into `base` (LayoutFusedStateInts words, zeroed
+// once when allocated; the kernel keeps it consistent from launch to launch).
+void BindLayoutFusedState(LayoutParams* p, int32_t* base, int max_chunks, int columns);
 // Magic multiplier for dividing an expert id by num_expert_per_rank on the device.
 uint32_t RankMagic(int num_expert_per_rank);
 

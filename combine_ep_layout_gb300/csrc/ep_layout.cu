@@ -44,14 +44,24 @@
 // and metadata of its range without another launch.  A second cluster barrier
 // keeps every CTA's shared memory alive until the others have read it.
 //
+// Mid-size batches (as many ranges as a cooperative grid keeps resident), one
+// launch: the fused kernel counts each range like the cluster kernel, but
+// exchanges the column totals through L2 -- a row per range and atomic sums
+// per superchunk of 16 ranges -- around one grid barrier, then finishes its
+// range with the same device code.  This is the single-pass form of the
+// counting the pages give the "notify warps" of the Dispatch data flow
+// figure: no count / scan / slots kernel boundaries, ranks kept on chip.
+//
 // Non-expand layout (EPHandle do_expand = false): one row per (token,
 // destination rank).  The counting is shared (the rank columns already count
 // each range's tokens per rank); the slots step places rank r's tokens in
 // ascending order from psum_rank[r] on, using warp ballots over the tokens'
 // rank masks for the position inside the range.
 //
-// No kernel waits on a flag: the only waits are the cluster barriers, which
-// every thread of every CTA of the cluster reaches unconditionally.
+// Waits: the cluster barriers, which every thread of every CTA of the cluster
+// reaches unconditionally, and the fused kernel's grid barrier, whose wait is
+// bounded by %globaltimer (LayoutParams::wait_ns): a CTA that gives up records
+// device error value 2 (bit 1) and returns.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -132,21 +142,24 @@ __device__ __forceinline__ int32_t ld_cluster_shared(const int32_t* local, uint3
 
 // ---- scans --------------------------------------------------------------------
 
-// v rounded up to a multiple of A (a mask when A is a power of two).
-__device__ __forceinline__ int align_up(int v, int A) {
-  return (A & (A - 1)) == 0 ? (v + A - 1) & -A : (v + A - 1) / A * A;
+// v rounded up to a multiple of A.  P2: A is a power of two (a mask); the
+// callers test that once per scan, so no element pays for a division it does
+// not need.
+template <bool P2>
+__device__ __forceinline__ int align_to(int v, int A) {
+  return P2 ? (v + A - 1) & -A : (v + A - 1) / A * A;
 }
 
 // Block-wide exclusive scan of align(v[e], A) for e in [0, n) into out[0..n]
 // (out[n] = total).  warp_tot needs 33 words.  All threads must call it.
-__device__ void block_exclusive_scan(const int32_t* v, int n, int A, int32_t* out,
-                                     int32_t* warp_tot) {
+template <bool P2>
+__device__ void block_exclusive_scan_a(const int32_t* v, int n, int A, int32_t* out, int32_t* warp_tot) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nthr = blockDim.x, nwarp = nthr >> 5;
   const int V = (n + nthr - 1) / nthr;
   const int beg = min(n, tid * V), end = min(n, beg + V);
   int sum = 0;
-  for (int e = beg; e < end; ++e) sum += align_up(v[e], A);
+  for (int e = beg; e < end; ++e) sum += align_to<P2>(v[e], A);
   int incl = sum;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -170,32 +183,66 @@ __device__ void block_exclusive_scan(const int32_t* v, int n, int A, int32_t* ou
   int run = warp_tot[warp] + incl - sum;
   for (int e = beg; e < end; ++e) {
     out[e] = run;
-    run += align_up(v[e], A);
+    run += align_to<P2>(v[e], A);
   }
   if (tid == 0) out[n] = warp_tot[32];
   __syncthreads();
 }
 
+__device__ void block_exclusive_scan(const int32_t* v, int n, int A, int32_t* out, int32_t* warp_tot) {
+  if ((A & (A - 1)) == 0) block_exclusive_scan_a<true>(v, n, A, out, warp_tot);
+  else block_exclusive_scan_a<false>(v, n, A, out, warp_tot);
+}
+
 // Exclusive scan of align(v[e], A) for e in [0, n) by one warp (ceil(n/32)
 // consecutive values per lane) into out[0..n] (out[n] = total).
-__device__ __forceinline__ void warp_exclusive_scan(const int32_t* v, int n, int A, int32_t* out) {
+template <bool P2>
+__device__ __forceinline__ void warp_exclusive_scan_a(const int32_t* v, int n, int A, int32_t* out) {
   const int lane = threadIdx.x & 31;
   const int V = (n + 31) / 32;
   const int beg = min(n, lane * V), end = min(n, beg + V);
   int sum = 0;
-  for (int e = beg; e < end; ++e) sum += align_up(v[e], A);
-  int incl = sum;
+  int incl;
+  if (V <= 16) {  // the lane's values in registers, all loads in flight at once
+    int x[16];
 #pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += y;
-  }
-  int run = incl - sum;
-  for (int e = beg; e < end; ++e) {
-    out[e] = run;
-    run += align_up(v[e], A);
+    for (int u = 0; u < 16; ++u) {
+      x[u] = beg + u < end ? align_to<P2>(v[beg + u], A) : 0;
+      sum += x[u];
+    }
+    incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    int run = incl - sum;
+#pragma unroll
+    for (int u = 0; u < 16; ++u)
+      if (beg + u < end) {
+        out[beg + u] = run;
+        run += x[u];
+      }
+  } else {
+    for (int e = beg; e < end; ++e) sum += align_to<P2>(v[e], A);
+    incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    int run = incl - sum;
+    for (int e = beg; e < end; ++e) {
+      out[e] = run;
+      run += align_to<P2>(v[e], A);
+    }
   }
   if (lane == 31) out[n] = incl;
+}
+
+__device__ __forceinline__ void warp_exclusive_scan(const int32_t* v, int n, int A, int32_t* out) {
+  if ((A & (A - 1)) == 0) warp_exclusive_scan_a<true>(v, n, A, out);
+  else warp_exclusive_scan_a<false>(v, n, A, out);
 }
 
 // Expert counts up to this many are scanned by single warps (no block barriers
@@ -285,7 +332,6 @@ __device__ void count_tokens(const LayoutParams& p, int t0, int ntok, int32_t* w
                              CountRegs<KC>& regs) {
   constexpr int NW = kLayoutCountWarps;
   constexpr int NB = CountBatches<KC>();
-  static_assert(NW == 16, "the column scan gives each expert column a half warp");
   const int K = KC ? KC : p.topk;
   const int E = p.num_experts, W = p.world_size;
   const int EW = E + W;
@@ -343,22 +389,23 @@ __device__ void count_tokens(const LayoutParams& p, int t0, int ntok, int32_t* w
   if (bad) atomicOr(p.err, kErrBadExpert);
   __syncthreads();
 
-  // per expert, a half warp scans the 16 warps' counts: each warp's start and
-  // the range's total
-  for (int j0 = 2 * warp; j0 < E; j0 += 2 * NW) {
-    const int j = j0 + (lane >> 4), w = lane & 15;
-    const bool ok = j < E;
-    const int v = ok ? whist[w * EW + j] : 0;
-    int incl = v;
+  // per expert, a thread scans its column of the 16 warps' counts: each warp's
+  // start and the range's total (consecutive threads touch consecutive words:
+  // no bank conflicts; eight loads in flight before the first add)
+  for (int j = tid; j < E; j += kCountThreads) {
+    int run = 0;
 #pragma unroll
-    for (int o = 1; o < 16; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, incl, o, 16);
-      if (w >= o) incl += y;
+    for (int w0 = 0; w0 < NW; w0 += 8) {
+      int v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) v[u] = whist[(w0 + u) * EW + j];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        whist[(w0 + u) * EW + j] = run;
+        run += v[u];
+      }
     }
-    if (ok) {
-      whist[w * EW + j] = incl - v;
-      if (w == 15) colcnt[j] = incl;
-    }
+    colcnt[j] = run;
   }
   // tokens per rank: count each rank's bit over the token masks
   for (int r = warp; r < W; r += NW) {
@@ -753,7 +800,7 @@ __device__ void write_outputs_nonexpand(const LayoutParams& p, const int32_t* cn
 
 // Shared-memory words of slots_nonexpand_tokens' scratch for tpb tokens.
 __host__ __device__ constexpr int NonExpandScratchWords(int tpb, int K, int W) {
-  return 2 * tpb * (K < W ? K : W) + (tpb / 32) * W + tpb * K + 2 * tpb;
+  return 2 * tpb * (K < W ? K : W) + (((tpb / 32) * W + 1) & ~1) + tpb * K + 2 * tpb;
 }
 
 template <int KC>
@@ -822,7 +869,101 @@ __host__ __device__ constexpr int ClusterSmemWords(int E, int W, int K, int tpb,
          + tpb * K                                        // ids
          + (ne ? 0 : 3 * tpb * K + 2 * tpb)               // loc, slots_s, sorted, src (expand)
          + 2 * (E + 1) + 33                               // psum_s, cx, warp_tot
-         + (W + 1) + W + (W + 1);                         // prank, rbase, rcx
+         + (W + 1) + W + (W + 1)                          // prank, rbase, rcx
+         + 4;                                             // misc
+}
+
+// Shared memory of one token range of the single-launch kernels (cluster and
+// fused), carved out of `sm` for tpb tokens (ClusterSmemWords words).
+struct RangeSmem {
+  int2* sorted_ne;               // NE: [tpb*RM] (rank, token) rows in (rank, token) order
+  int32_t* woff;                 // NE: [tpb/32][W]
+  int32_t* dslot;                // NE: [tpb*K]
+  int32_t* src_ne;               // NE: [2*tpb]
+  unsigned long long* tmask;     // [tpb] (8-byte aligned: even offset)
+  int32_t* whist;                // [NW][EW]
+  int32_t* colcnt;               // [EW] this range's totals (read remotely by the cluster kernel)
+  int32_t* tot;                  // [EW] totals over all ranges
+  int32_t* off;                  // [EW] sum over the ranges before this one
+  int32_t* ids;                  // [tpb*K]
+  int32_t* loc;                  // expand: [tpb*K]
+  int32_t* slots_s;              // expand: [tpb*K]
+  int32_t* sorted;               // expand: [tpb*K]
+  int32_t* src;                  // expand: [2*tpb]
+  int32_t* psum_s;               // [E+1]
+  int32_t* cx;                   // [E+1]
+  int32_t* warp_tot;             // [33]
+  int32_t* prank;                // [W+1]
+  int32_t* rbase;                // [W]
+  int32_t* rcx;                  // [W+1]
+  int32_t* misc;                 // [4]
+};
+
+template <bool NE>
+__device__ __forceinline__ RangeSmem carve_range_smem(int32_t* sm, int E, int W, int K, int tpb) {
+  const int EW = E + W;
+  RangeSmem r{};
+  int32_t* base = sm;
+  r.sorted_ne = reinterpret_cast<int2*>(sm);
+  if constexpr (NE) {
+    const int RM = K < W ? K : W;
+    r.woff = sm + 2 * tpb * RM;
+    r.dslot = r.woff + (((tpb / 32) * W + 1) & ~1);   // even: tmask below stays 8-byte aligned
+    r.src_ne = r.dslot + tpb * K;
+    base = r.src_ne + 2 * tpb;
+  }
+  r.tmask = reinterpret_cast<unsigned long long*>(base);
+  base += 2 * tpb;
+  r.whist = base;
+  r.colcnt = r.whist + kLayoutCountWarps * EW;
+  r.tot = r.colcnt + EW;
+  r.off = r.tot + EW;
+  r.ids = r.off + EW;
+  r.loc = r.ids + tpb * K;
+  r.slots_s = r.loc + (NE ? 0 : tpb * K);
+  r.sorted = r.slots_s + (NE ? 0 : tpb * K);
+  r.src = r.sorted + (NE ? 0 : tpb * K);
+  r.psum_s = r.src + (NE ? 0 : 2 * tpb);
+  r.cx = r.psum_s + E + 1;
+  r.warp_tot = r.cx + E + 1;
+  r.prank = r.warp_tot + 33;
+  r.rbase = r.prank + W + 1;
+  r.rcx = r.rbase + W;
+  r.misc = r.rcx + W + 1;
+  return r;
+}
+
+// The rest of a range once r.tot (totals over all ranges) and r.off (the sum
+// over the ranges before this one) are known, for range `me` of `nranges`:
+// prefix sums, CTA 0's outputs, slots, metadata and this range's share of the
+// rows that receive nothing.  All threads call, after a barrier that makes
+// tot and off visible.
+template <int KC, bool NE>
+__device__ void finish_range(const LayoutParams& p, const RangeSmem& r, int me, int nranges, int t0,
+                             int ntok, int tpb) {
+  const int E = p.num_experts, W = p.world_size;
+  if constexpr (!NE) {
+    expert_scans(r.tot, p.alignment, r.psum_s, r.colcnt, r.cx, E, r.warp_tot);
+    if (me == 0) write_outputs_expand(p, r.tot, r.psum_s, r.tot + E);
+    slots_expand_tokens<KC>(p, t0, ntok, r.psum_s, r.off, r.cx, r.loc, r.ids, r.slots_s, r.sorted, r.src);
+    fill_unreceived(p, r.psum_s, r.tot, r.psum_s[E], me, nranges);
+  } else {
+    // rank prefix, this range's rank scan and (range 0, few experts) the expert
+    // prefix on three warps behind one barrier
+    const int warp = threadIdx.x >> 5;
+    const bool warp_psum = E <= kWarpScanMax;
+    if (warp == 0) warp_scan64(r.tot + E, W, r.prank);
+    else if (warp == 1) warp_scan64(r.colcnt + E, W, r.rcx);
+    else if (warp == 2 && me == 0 && warp_psum) warp_exclusive_scan(r.tot, E, p.alignment, r.psum_s);
+    __syncthreads();
+    if (me == 0 && !warp_psum) block_exclusive_scan(r.tot, E, p.alignment, r.psum_s, r.warp_tot);
+    for (int q = threadIdx.x; q < W; q += blockDim.x) r.rbase[q] = r.prank[q] + r.off[E + q];
+    if (me == 0) write_outputs_nonexpand(p, r.tot, r.psum_s, r.prank, r.tot + E);
+    // rbase is read after slots_nonexpand_tokens' first barrier
+    slots_nonexpand_tokens<KC>(p, t0, ntok, tpb, r.rbase, r.rcx, r.ids, r.woff, r.dslot, r.src_ne,
+                               r.sorted_ne);
+    fill_unreceived(p, nullptr, nullptr, r.prank[W], me, nranges);
+  }
 }
 
 template <int KC, bool NE>
@@ -830,90 +971,227 @@ __global__ void __launch_bounds__(kClusterThreads, 1) ep_layout_cluster_kernel(L
   const int K = KC ? KC : p.topk;
   const int E = p.num_experts, W = p.world_size, EW = E + W;
   extern __shared__ __align__(16) int32_t sm[];
-  int32_t* base = sm;
-  int2* sorted_ne = reinterpret_cast<int2*>(sm);               // NE: [tpb*RM]
-  int32_t* woff = nullptr;
-  int32_t* dslot = nullptr;
-  int32_t* src_ne = nullptr;
-  if constexpr (NE) {
-    const int RM = K < W ? K : W;
-    woff = sm + 2 * tpb * RM;                                  // [tpb/32][W]
-    dslot = woff + (tpb / 32) * W;                             // [tpb*K]
-    src_ne = dslot + tpb * K;                                  // [2*tpb]
-    base = src_ne + 2 * tpb;
-  }
-  auto* tmask = reinterpret_cast<unsigned long long*>(base);   // [tpb] (8-byte aligned: even offset)
-  base += 2 * tpb;
-  int32_t* whist = base;                                       // [NW][EW]
-  int32_t* colcnt = whist + kLayoutCountWarps * EW;            // [EW] this CTA's totals (read remotely)
-  int32_t* tot = colcnt + EW;                                  // [EW] totals over the cluster
-  int32_t* off = tot + EW;                                     // [EW] sum over the CTAs before this one
-  int32_t* ids = off + EW;                                     // [tpb*K]
-  int32_t* loc = ids + tpb * K;                                // expand: [tpb*K]
-  int32_t* slots_s = loc + (NE ? 0 : tpb * K);                 // expand: [tpb*K]
-  int32_t* sorted = slots_s + (NE ? 0 : tpb * K);              // expand: [tpb*K]
-  int32_t* src = sorted + (NE ? 0 : tpb * K);                  // expand: [2*tpb]
-  int32_t* psum_s = src + (NE ? 0 : 2 * tpb);                  // [E+1]
-  int32_t* cx = psum_s + E + 1;                                // [E+1]
-  int32_t* warp_tot = cx + E + 1;                              // [33]
-  int32_t* prank = warp_tot + 33;                              // [W+1]
-  int32_t* rbase = prank + W + 1;                              // [W]
-  int32_t* rcx = rbase + W;                                    // [W+1]
+  const RangeSmem r = carve_range_smem<NE>(sm, E, W, K, tpb);
 
   const uint32_t me = cluster_ctarank(), ncta = cluster_nctarank();
   allow_dependent_grids();   // the dispatch that follows may be scheduled now
   const int t0 = static_cast<int>(me) * tpb;
   const int ntok = max(0, min(p.num_tokens, t0 + tpb) - t0);
   CountRegs<KC> regs;
-  count_tokens<KC>(p, t0, ntok, whist, tmask, colcnt, ids, regs);
+  count_tokens<KC>(p, t0, ntok, r.whist, r.tmask, r.colcnt, r.ids, regs);
 
   // every CTA's column totals are complete: gather the cluster's totals and
   // this CTA's offsets from the other CTAs' shared memory
   cluster_arrive();
   cluster_wait();
-  if constexpr (!NE) write_range_ranks<KC>(ntok, K, whist, EW, regs, loc);
+  if constexpr (!NE) write_range_ranks<KC>(ntok, K, r.whist, EW, regs, r.loc);
   for (int j = threadIdx.x; j < EW; j += kClusterThreads) {
     int v[kClusterCtas];
 #pragma unroll
     for (int b = 0; b < kClusterCtas; ++b)  // all remote loads in flight together
       v[b] = b >= static_cast<int>(ncta) ? 0
-           : b == static_cast<int>(me)   ? colcnt[j]
-                                         : ld_cluster_shared(colcnt + j, static_cast<uint32_t>(b));
+           : b == static_cast<int>(me)   ? r.colcnt[j]
+                                         : ld_cluster_shared(r.colcnt + j, static_cast<uint32_t>(b));
     int t = 0, o = 0;
 #pragma unroll
     for (int b = 0; b < kClusterCtas; ++b) {
       o += b < static_cast<int>(me) ? v[b] : 0;
       t += v[b];
     }
-    tot[j] = t;
-    off[j] = o;
+    r.tot[j] = t;
+    r.off[j] = o;
   }
   cluster_arrive_relaxed();  // this CTA is done reading remote shared memory
   __syncthreads();
-
-  if constexpr (!NE) {
-    expert_scans(tot, p.alignment, psum_s, colcnt, cx, E, warp_tot);
-    if (me == 0) write_outputs_expand(p, tot, psum_s, tot + E);
-    slots_expand_tokens<KC>(p, t0, ntok, psum_s, off, cx, loc, ids, slots_s, sorted, src);
-    fill_unreceived(p, psum_s, tot, psum_s[E], static_cast<int>(me), static_cast<int>(ncta));
-  } else {
-    // rank prefix, this CTA's rank scan and (CTA 0, few experts) the expert
-    // prefix on three warps behind one barrier
-    const int warp = threadIdx.x >> 5;
-    const bool warp_psum = E <= kWarpScanMax;
-    if (warp == 0) warp_scan64(tot + E, W, prank);
-    else if (warp == 1) warp_scan64(colcnt + E, W, rcx);
-    else if (warp == 2 && me == 0 && warp_psum) warp_exclusive_scan(tot, E, p.alignment, psum_s);
-    __syncthreads();
-    if (me == 0 && !warp_psum) block_exclusive_scan(tot, E, p.alignment, psum_s, warp_tot);
-    for (int r = threadIdx.x; r < W; r += kClusterThreads) rbase[r] = prank[r] + off[E + r];
-    if (me == 0) write_outputs_nonexpand(p, tot, psum_s, prank, tot + E);
-    // rbase is read after slots_nonexpand_tokens' first barrier
-    slots_nonexpand_tokens<KC>(p, t0, ntok, tpb, rbase, rcx, ids, woff, dslot, src_ne, sorted_ne);
-    fill_unreceived(p, nullptr, nullptr, prank[W], static_cast<int>(me), static_cast<int>(ncta));
-  }
+  finish_range<KC, NE>(p, r, static_cast<int>(me), static_cast<int>(ncta), t0, ntok, tpb);
   // keep this CTA's shared memory until every CTA has finished reading it
   cluster_wait();
+}
+
+// ---------------------------------------------------------------- fused (one launch, mid-size batches)
+
+// Global-memory exchange of the single-launch layout for batches beyond one
+// cluster: a cooperative grid (every CTA resident at once), one token range
+// per CTA.  Each CTA counts its range exactly as the cluster kernel does, then
+// publishes its column totals twice: as a row of 16-bit counts in the range
+// table [C][EW8], and, by atomic adds, into the row of its superchunk (the
+// kFusedSuper consecutive ranges it belongs to) of the superchunk table
+// [S][EW8].  After one grid barrier a CTA has everything in L2: the totals
+// (sum of the S superchunk rows), and its offset in each column (the
+// superchunk rows before its own plus the range rows of its superchunk before
+// it): at most S + kFusedSuper - 1 values per column instead of one per
+// range.  Its ranks are still in registers and its ids in shared memory, so
+// it goes straight on to slots and metadata.
+//
+// The superchunk table is double-buffered by launch parity: a launch adds
+// into buffer (launches so far & 1) and zeroes the other one for the next
+// launch.
+// Integer adds commute, so the sums do not depend on the order of the atomics.
+
+constexpr int kFusedSuper = 16;
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ unsigned ld_relaxed_gpu(const unsigned* a) {
+  unsigned v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(a) : "memory");
+  return v;
+}
+__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* a) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(a) : "memory");
+  return v;
+}
+__device__ __forceinline__ int4 ld_cg_v4(const int4* a) {
+  int4 v;
+  asm volatile("ld.global.cg.v4.s32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(a));
+  return v;
+}
+
+// Words of the fused kernel's staging area (after the range's shared memory):
+// S superchunk rows of EW8 int32 and up to kFusedSuper - 1 range rows of EW8
+// 16-bit counts.
+__host__ __device__ constexpr int FusedStageWords(int S, int EW8) {
+  return S * EW8 + (kFusedSuper / 2) * EW8;
+}
+
+// Barrier over the nctas CTAs of a cooperative grid; every thread of every CTA
+// calls it.  bar[0] counts arrivals and only grows (modulo 2^32); bar[1] is
+// its value when this launch began and bar[2] the number of launches so far,
+// both read by each CTA before it arrives (they change only after every CTA
+// has arrived: the last arrival sets them for the next launch).  A CTA
+// arrives with one atomic add and waits (acquire) until the counter reaches
+// bar[1] + nctas.  The state stays consistent for the next launch whatever the
+// grid size, also when a wait gives up: every CTA arrives exactly once.  A
+// wait is bounded by wait_ns (the deadline is checked before each test, so
+// wait_ns = 0 gives up at once); the function returns false, for every thread
+// of the CTA, when this CTA's wait gave up.
+__device__ bool fused_grid_barrier(unsigned* bar, unsigned base, unsigned gen, unsigned nctas,
+                                   uint64_t wait_ns, int32_t* ok_s) {
+  __syncthreads();  // this CTA's writes are done
+  if (threadIdx.x == 0) {
+    int ok = 1;
+    __threadfence();  // ... and visible at gpu scope before the arrival
+    const unsigned target = base + nctas;
+    const unsigned arrival = atomicAdd(bar, 1u);
+    if (arrival == target - 1u) {
+      bar[1] = target;  // the next launch's base and count (read after this kernel)
+      bar[2] = gen + 1u;
+    } else {
+      const uint64_t t0 = global_ns();
+      for (;;) {
+        if (global_ns() - t0 >= wait_ns) {
+          ok = 0;
+          break;
+        }
+        if (static_cast<int>(ld_acquire_gpu(bar) - target) >= 0) break;
+      }
+    }
+    *ok_s = ok;
+  }
+  __syncthreads();
+  return *ok_s != 0;
+}
+
+template <int KC, bool NE>
+__global__ void __launch_bounds__(kCountThreads, 2) ep_layout_fused_kernel(LayoutParams p) {
+  const int K = KC ? KC : p.topk;
+  const int E = p.num_experts, W = p.world_size, EW = E + W;
+  const int EW8 = (EW + 7) & ~7;
+  const int tpb = p.fused_tpb;
+  extern __shared__ __align__(16) int32_t sm[];
+  const RangeSmem r = carve_range_smem<NE>(sm, E, W, K, tpb);
+  const int c = blockIdx.x, C = gridDim.x;
+  const int tid = threadIdx.x, nthr = blockDim.x;
+  const int t0 = c * tpb;
+  const int ntok = max(0, min(p.num_tokens, t0 + tpb) - t0);
+  if (tid == 0) {
+    r.misc[0] = static_cast<int32_t>(ld_relaxed_gpu(p.fused_bar + 1));   // barrier base
+    r.misc[2] = static_cast<int32_t>(ld_relaxed_gpu(p.fused_bar + 2));   // launches so far
+  }
+  allow_dependent_grids();   // the dispatch that follows may be scheduled now
+  CountRegs<KC> regs;
+  count_tokens<KC>(p, t0, ntok, r.whist, r.tmask, r.colcnt, r.ids, regs);
+  __syncthreads();
+  if constexpr (!NE) write_range_ranks<KC>(ntok, K, r.whist, EW, regs, r.loc);
+
+  // publish this range's column totals
+  const unsigned base = static_cast<unsigned>(r.misc[0]);
+  const unsigned gen = static_cast<unsigned>(r.misc[2]);
+  const int64_t sup_words = static_cast<int64_t>(p.fused_super_rows) * EW8;
+  int32_t* sup = p.fused_super + (gen & 1u) * sup_words;
+  int32_t* sup_next = p.fused_super + ((gen & 1u) ^ 1u) * sup_words;
+  // (CTAs past the last range of tokens only fill padding: nothing to publish,
+  // and no range reads their rows)
+  const int CR = (p.num_tokens + tpb - 1) / tpb;
+  const int s = c / kFusedSuper;
+  if (c < CR) {
+    uint32_t* row = reinterpret_cast<uint32_t*>(p.fused_rows + static_cast<int64_t>(c) * EW8);
+    for (int j2 = tid; j2 < EW8 / 2; j2 += nthr) {
+      const int j = 2 * j2;
+      const uint32_t lo = j < EW ? static_cast<uint32_t>(r.colcnt[j]) : 0u;
+      const uint32_t hi = j + 1 < EW ? static_cast<uint32_t>(r.colcnt[j + 1]) : 0u;
+      row[j2] = lo | (hi << 16);
+    }
+    for (int j = tid; j < EW; j += nthr) {
+      const int v = r.colcnt[j];
+      if (v) atomicAdd(sup + static_cast<int64_t>(s) * EW8 + j, v);
+    }
+  }
+  for (int64_t f = static_cast<int64_t>(c) * nthr + tid; f < sup_words; f += static_cast<int64_t>(C) * nthr)
+    sup_next[f] = 0;  // the next launch's buffer
+
+  if (!fused_grid_barrier(p.fused_bar, base, gen, static_cast<unsigned>(C), p.wait_ns, r.misc + 1)) {
+    if (tid == 0) atomicOr(p.err, kErrTimeout);
+    return;  // uniform per CTA
+  }
+
+  // totals and this range's offsets.  The superchunk rows and the range rows
+  // of this superchunk before this range were written by other CTAs in this
+  // launch: they are staged in shared memory with 16-byte .cg loads (L2, never
+  // the non-coherent path), all in flight at once, then summed per column.
+  const int S = (CR + kFusedSuper - 1) / kFusedSuper;
+  const int c_lo = s * kFusedSuper;
+  const int nrow = max(0, (c < CR ? c : CR) - c_lo);
+  int32_t* st_sup = sm + ((ClusterSmemWords(E, W, K, tpb, NE) + 3) & ~3);     // [S][EW8], 16-byte aligned
+  const uint16_t* st_rows = reinterpret_cast<const uint16_t*>(st_sup + S * EW8);   // [nrow][EW8]
+  {
+    const int n_sup4 = S * EW8 / 4, n4 = n_sup4 + nrow * EW8 / 8;
+    const int4* gs = reinterpret_cast<const int4*>(sup);
+    const int4* gr = reinterpret_cast<const int4*>(p.fused_rows + static_cast<int64_t>(c_lo) * EW8);
+    int4* st4 = reinterpret_cast<int4*>(st_sup);
+    for (int f0 = tid; f0 < n4; f0 += 4 * nthr) {
+      int4 a[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int f = f0 + u * nthr;
+        if (f < n4) a[u] = ld_cg_v4(f < n_sup4 ? gs + f : gr + (f - n_sup4));
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int f = f0 + u * nthr;
+        if (f < n4) st4[f] = a[u];   // the range rows follow the superchunk rows
+      }
+    }
+  }
+  __syncthreads();
+  for (int j = tid; j < EW; j += nthr) {
+    int pre = 0, all = 0;
+    for (int s2 = 0; s2 < S; ++s2) {
+      const int v = st_sup[s2 * EW8 + j];
+      all += v;
+      pre += s2 < s ? v : 0;
+    }
+    for (int q = 0; q < nrow; ++q) pre += st_rows[q * EW8 + j];
+    r.tot[j] = all;
+    r.off[j] = pre;
+  }
+  __syncthreads();
+  finish_range<KC, NE>(p, r, c, C, t0, ntok, tpb);
 }
 
 // ---------------------------------------------------------------- launch
@@ -982,10 +1260,76 @@ cudaError_t launch_cluster(const LayoutParams& p, int tpb, cudaStream_t s) {
   return cudaLaunchKernelEx(&cfg, ep_layout_cluster_kernel<KC, NE>, p, tpb);
 }
 
+// Rows of -1 one CTA of the fused kernel fills at most; batches with more
+// padding than their ranges cover get extra CTAs with no tokens.
+constexpr int64_t kFusedFillPerCta = 8192;
+
+// Geometry of the fused kernel for this launch (tpb = 0: it does not serve
+// it -- no fused state (the allocation-free entry point), switched off, more
+// ranges than the state holds, more CTAs than a cooperative grid keeps
+// resident, or more
+// shared memory than the cluster kernel's limit).  The grid has one CTA per
+// range of tpb tokens, and at least one per kFusedFillPerCta rows to fill.
+struct FusedGeom {
+  int tpb = 0;
+  int ctas = 0;
+  size_t smem = 0;
+};
+
+// Dynamic shared memory of a fused launch: the range's share plus the staging
+// area for S superchunk rows.
+size_t fused_smem(int E, int W, int K, int tpb, bool ne, int S) {
+  const int EW8 = (E + W + 7) & ~7;
+  return sizeof(int32_t) * (((static_cast<size_t>(ClusterSmemWords(E, W, K, tpb, ne)) + 3) & ~static_cast<size_t>(3)) +
+                            static_cast<size_t>(FusedStageWords(S, EW8)));
+}
+
+FusedGeom fused_geom(const LayoutParams& p, const LaunchGeom& g) {
+  FusedGeom f;
+  if (p.fused_bar == nullptr || g.fused_blocks_per_sm <= 0 || p.num_tokens <= 0) return f;
+  // kLayoutTPC tokens per CTA while that gives at most one CTA per SM, else
+  // twice as many (measured at 32768 tokens: 256 ranges on 152 SMs took
+  // 16.5 us back to back, 128 ranges 14.5 us), unless pinned
+  int tpb = g.fused_tpb;
+  if (tpb == 0) tpb = (p.num_tokens + kLayoutTPC - 1) / kLayoutTPC > g.num_sms ? 2 * kLayoutTPC : kLayoutTPC;
+  const int64_t ranges = (p.num_tokens + tpb - 1) / tpb;
+  const int64_t fill = p.rcap - static_cast<int64_t>(p.num_tokens) * p.topk;
+  const int64_t fill_ctas = (fill + kFusedFillPerCta - 1) / kFusedFillPerCta;
+  const int64_t ctas = ranges > fill_ctas ? ranges : fill_ctas;
+  if (ranges > p.fused_max_ranges || ctas > static_cast<int64_t>(g.fused_blocks_per_sm) * g.num_sms)
+    return f;
+  const int S = static_cast<int>((ranges + kFusedSuper - 1) / kFusedSuper);
+  if (S > g.fused_max_super) return f;   // beyond the staging the occupancy was computed for
+  const size_t smem = fused_smem(p.num_experts, p.world_size, p.topk, tpb, p.no_expand != 0, S);
+  if (smem > kClusterMaxSmem) return f;
+  f.tpb = tpb;
+  f.ctas = static_cast<int>(ctas);
+  f.smem = smem;
+  return f;
+}
+
+template <int KC, bool NE>
+cudaError_t launch_fused(LayoutParams p, const FusedGeom& f, cudaStream_t s) {
+  p.fused_tpb = f.tpb;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(f.ctas));
+  cfg.blockDim = dim3(kCountThreads);
+  cfg.dynamicSmemBytes = f.smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;   // every CTA resident at once: the grid barrier's premise
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, ep_layout_fused_kernel<KC, NE>, p);
+}
+
 template <int KC, bool NE>
 cudaError_t launch_layout(const LayoutParams& p, const LaunchGeom& g, cudaStream_t s) {
   const int tpb = cluster_tpb(p, g);
   if (tpb > 0) return launch_cluster<KC, NE>(p, tpb, s);
+  const FusedGeom f = fused_geom(p, g);
+  if (f.tpb > 0) return launch_fused<KC, NE>(p, f, s);
   const int EW = p.num_experts + p.world_size;
   if (p.num_chunks > 0)
     ep_layout_count_kernel<KC><<<p.num_chunks, kCountThreads, count_smem(p.topk, EW), s>>>(p);
@@ -1025,10 +1369,32 @@ cudaError_t prepare_layout(int, int, int, LaunchGeom* g) {
   if (e != cudaSuccess) return e;
   g->blocks_per_sm = 1;
   g->cluster_ok = 0;
+  g->fused_blocks_per_sm = 0;
   e = cudaFuncSetAttribute(ep_layout_cluster_kernel<KC, NE>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(kClusterMaxSmem));
   if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(ep_layout_fused_kernel<KC, NE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(kClusterMaxSmem));
+  if (e != cudaSuccess) return e;
+  // tokens per CTA of the fused kernel pinned by EP_GB300_LAYOUT_FUSED_TPB (64,
+  // 128 or 256); 0: chosen per launch from the batch size
+  const char* tenv = std::getenv("EP_GB300_LAYOUT_FUSED_TPB");
+  const int t = tenv ? std::atoi(tenv) : 0;
+  g->fused_tpb = (t == 64 || t == 128 || t == 256) ? t : 0;
+  const char* fenv = std::getenv("EP_GB300_LAYOUT_FUSED");
+  // superchunk rows staged at most: enough for two resident CTAs per SM
+  g->fused_max_super = (2 * g->num_sms + kFusedSuper - 1) / kFusedSuper;
+  if (g->layout_experts > 0 && !(fenv != nullptr && fenv[0] == '0')) {
+    // resident CTAs per SM at the largest range and staging the fused kernel takes
+    const size_t smem = fused_smem(g->layout_experts, g->layout_world, kmax, 256, NE, g->fused_max_super);
+    int n = 0;
+    if (smem <= kClusterMaxSmem &&
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, ep_layout_fused_kernel<KC, NE>, kCountThreads,
+                                                      smem) == cudaSuccess)
+      g->fused_blocks_per_sm = n;
+    cudaGetLastError();
+  }
   const char* env = std::getenv("EP_GB300_LAYOUT_CLUSTER");
   if (env != nullptr && env[0] == '0') return cudaSuccess;
   cudaLaunchConfig_t cfg = {};
@@ -1054,7 +1420,11 @@ cudaError_t prepare_layout(int, int, int, LaunchGeom* g) {
 
 }  // namespace
 
-bool LayoutUsesCluster(const LayoutParams& p, const LaunchGeom& g) { return cluster_tpb(p, g) > 0; }
+LayoutPath LayoutPathOf(const LayoutParams& p, const LaunchGeom& g) {
+  if (cluster_tpb(p, g) > 0) return LayoutPath::kCluster;
+  if (fused_geom(p, g).tpb > 0) return LayoutPath::kFused;
+  return LayoutPath::kLaunches;
+}
 
 int64_t LayoutScratchInts(int max_chunks, int columns) {
   return 3LL * columns * (max_chunks > 0 ? max_chunks : 1) + columns;
@@ -1066,6 +1436,33 @@ void BindLayoutScratch(LayoutParams* p, int32_t* base, int max_chunks, int colum
   p->chunk_hist_cols = base + static_cast<int64_t>(columns) * cap;
   p->chunk_off = p->chunk_hist_cols + static_cast<int64_t>(columns) * cap;
   p->col_total = p->chunk_off + static_cast<int64_t>(columns) * cap;
+}
+
+namespace {
+constexpr int kFusedMaxRanges = 1024;   // above any cooperative grid of 512-thread CTAs on one GPU
+int fused_ranges(int max_chunks) {
+  const int r = 2 * (max_chunks > 0 ? max_chunks : 1);   // ranges of 64 tokens at the smallest
+  return r < kFusedMaxRanges ? r : kFusedMaxRanges;
+}
+}  // namespace
+
+int64_t LayoutFusedStateInts(int max_chunks, int columns) {
+  const int64_t R = fused_ranges(max_chunks);
+  const int64_t S = (R + kFusedSuper - 1) / kFusedSuper;
+  const int64_t EW8 = (columns + 7) & ~7;
+  const int64_t rows_words = ((R * EW8 + 1) / 2 + 63) & ~int64_t{63};
+  return 64 + 2 * S * EW8 + rows_words;
+}
+
+void BindLayoutFusedState(LayoutParams* p, int32_t* base, int max_chunks, int columns) {
+  const int R = fused_ranges(max_chunks);
+  const int S = (R + kFusedSuper - 1) / kFusedSuper;
+  const int64_t EW8 = (columns + 7) & ~7;
+  p->fused_bar = reinterpret_cast<uint32_t*>(base);
+  p->fused_super = base + 64;
+  p->fused_rows = reinterpret_cast<uint16_t*>(base + 64 + 2 * S * EW8);
+  p->fused_super_rows = S;
+  p->fused_max_ranges = R;
 }
 
 uint32_t RankMagic(int num_expert_per_rank) {

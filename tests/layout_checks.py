@@ -114,3 +114,27 @@ def check_layout_nonexpand(topk_idx, W, T, Epr, A, rcap, cnt, tok_per_rank, psum
             exp_meta[s, 0], exp_meta[s, 1] = t // T, t % T
             exp_meta[s, 2:] = dst_slot[t]
     assert np.array_equal(meta, exp_meta), "recv_src_metadata is not the inverse of send_slot"
+
+
+# Layout kernels a handle may run (read from the environment when the handle is
+# built): the single-launch cluster kernel (small batches), the single-launch
+# fused kernel (a cooperative grid) and the three launches count / spine /
+# slots.  Each path's tag in the handle's layout variant name.
+LAYOUT_PATHS = ("cluster", "fused", "launches")
+PATH_TAG = {"cluster": "_cluster_", "fused": "_fused_", "launches": None}
+
+
+def set_layout_path(monkeypatch, path):
+    """Make handles built after this call run `path` where it applies (the
+    cluster and fused kernels fall back to the three launches beyond their
+    limits)."""
+    monkeypatch.setenv("EP_GB300_LAYOUT_CLUSTER", "1" if path == "cluster" else "0")
+    monkeypatch.setenv("EP_GB300_LAYOUT_FUSED", "1" if path == "fused" else "0")
+
+
+def ran_path(variant):
+    """The layout path a handle's last layout ran, from its variant name."""
+    for p, tag in PATH_TAG.items():
+        if tag and tag in variant:
+            return p
+    return "launches"

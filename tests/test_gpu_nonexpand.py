@@ -8,7 +8,7 @@ import torch
 import combine_ep_layout_gb300 as ep
 import oracle
 import synth
-from layout_checks import check_layout_nonexpand
+from layout_checks import check_layout_nonexpand, LAYOUT_PATHS, set_layout_path, ran_path
 
 pytestmark = pytest.mark.gpu
 
@@ -206,16 +206,16 @@ def test_identity_round_trip_prefill():
     assert torch.equal(out.view(torch.int16), want.view(torch.int16))
 
 
-@pytest.mark.parametrize("path", ["cluster", "launches"])
+@pytest.mark.parametrize("path", LAYOUT_PATHS)
 @pytest.mark.parametrize("case", ["tiny", "masked", "ragged", "one_token", "k_above_w", "w1",
                                   "generic_k5", "epr7", "full_2048"])
 def test_small_batch_layout_both_paths(case, path, monkeypatch):
-    monkeypatch.setenv("EP_GB300_LAYOUT_CLUSTER", "1" if path == "cluster" else "0")
+    set_layout_path(monkeypatch, path)
     spec = EDGE.get(case, dict(base="decode", max_tok_per_rank=256, num_tokens=2048))
     wl, mask = edge_wl(spec)
     topk = synth.gen_topk(wl, mask_frac=mask)
     h = ep.EpHandle(cfg_of(wl))
     h.layout(topk.cuda())
     assert_equal(gpu_fields(h), ref_layout(wl, topk.numpy()))
-    assert ("_cluster_" in h.variant(0)) == (path == "cluster"), h.variant(0)
+    assert ran_path(h.variant(0)) == path, h.variant(0)
     assert h.status() == 0

@@ -17,7 +17,7 @@ import torch
 import combine_ep_layout_gb300 as ep
 import oracle
 import synth
-from layout_checks import check_layout
+from layout_checks import check_layout, LAYOUT_PATHS, set_layout_path, ran_path
 
 pytestmark = pytest.mark.gpu
 
@@ -397,7 +397,7 @@ def test_identity_round_trip_prefill():
     assert torch.equal(out.view(torch.int16), want.view(torch.int16))
 
 
-@pytest.mark.parametrize("path", ["cluster", "launches"])
+@pytest.mark.parametrize("path", LAYOUT_PATHS)
 def test_graph_capture_replay(path, monkeypatch):
     """layout -> dispatch -> identity expert -> combine (and an FP8 dispatch on
     the same layout) captured once in a CUDA graph and replayed with new
@@ -406,7 +406,7 @@ def test_graph_capture_replay(path, monkeypatch):
     first are launched with programmatic stream serialisation, so each replay
     also checks that no kernel reads a predecessor's output before it is
     complete, nor a stale copy of the previous replay's."""
-    monkeypatch.setenv("EP_GB300_LAYOUT_CLUSTER", "1" if path == "cluster" else "0")
+    set_layout_path(monkeypatch, path)
     wl = synth.WORKLOADS["decode"]
     h = ep.EpHandle(cfg_of(wl))
     h8 = ep.EpHandle(cfg_of(wl, "fp8"), layout_of=h)
@@ -428,7 +428,7 @@ def test_graph_capture_replay(path, monkeypatch):
         h.dispatch(x_buf, recv, stream=s)
         h.combine(recv, w_buf, out, stream=s)
         h8.dispatch(x_buf, rq, rs, stream=s)
-    assert ("_cluster_" in h.variant(0)) == (path == "cluster"), h.variant(0)
+    assert ran_path(h.variant(0)) == path, h.variant(0)
     for seed in range(4):
         c = synth.make_case(wl.with_(seed=0x1000 + seed), device="cuda")
         topk_buf.copy_(c["topk_idx"])
@@ -570,16 +570,16 @@ SMALL = {
 }
 
 
-@pytest.mark.parametrize("path", ["cluster", "launches"])
+@pytest.mark.parametrize("path", LAYOUT_PATHS)
 @pytest.mark.parametrize("case", list(SMALL))
 def test_small_batch_layout_both_paths(case, path, monkeypatch):
-    monkeypatch.setenv("EP_GB300_LAYOUT_CLUSTER", "1" if path == "cluster" else "0")
+    set_layout_path(monkeypatch, path)
     wl, mask = edge_wl(SMALL[case])
     topk = synth.gen_topk(wl, mask_frac=mask)
     h, got, ref = layout_case(wl, topk)
     assert_layout_equal(got, ref)
     assert h.status() == 0
-    assert ("_cluster_" in h.variant(0)) == (path == "cluster"), h.variant(0)
+    assert ran_path(h.variant(0)) == path, h.variant(0)
     # a second, different routing on the same handle
     topk2 = synth.gen_topk(wl.with_(seed=wl.seed + 1), mask_frac=0.1)
     h.layout(topk2.cuda())
