@@ -555,7 +555,8 @@ __device__ void write_outputs_expand(const LayoutParams& p, const int32_t* cnt_s
 // counts, loc[i] the entry's rank among the range's entries of its expert
 // (may alias p.dst_slot of the range, which is overwritten with the slots),
 // ids[i] the staged expert ids or nullptr (then read from topk_idx).
-// Scratch: slots_s and sorted [ntok*K], src [2*ntok].
+// Scratch: slots_s and sorted [ntok*K], src [2*ntok]; slots_s and src 8-byte
+// aligned (the metadata rows are read from them as word pairs).
 template <int KC>
 __device__ void slots_expand_tokens(const LayoutParams& p, int t0, int ntok, const int32_t* psum_s,
                                     const int32_t* co, const int32_t* cx, const int32_t* loc,
@@ -595,8 +596,8 @@ __device__ void slots_expand_tokens(const LayoutParams& p, int t0, int ntok, con
       const int q = f / hw, c2 = f - q * hw;
       const int entry = sorted[q];
       const int tl = entry / K;
-      const int2 v = c2 == 0 ? make_int2(src[2 * tl], src[2 * tl + 1])
-                             : make_int2(slots_s[tl * K + 2 * c2 - 2], slots_s[tl * K + 2 * c2 - 1]);
+      // one 8-byte load per word pair (src and slots_s are 8-byte aligned, K even)
+      const int2 v = *reinterpret_cast<const int2*>(c2 == 0 ? src + 2 * tl : slots_s + tl * K + 2 * c2 - 2);
       reinterpret_cast<int2*>(p.meta + static_cast<int64_t>(slots_s[entry]) * KW)[c2] = v;
     }
   } else {
@@ -644,7 +645,7 @@ __global__ void __launch_bounds__(kSlotThreads, 1) ep_layout_slots_kernel(Layout
   int32_t* co = cl + E;                   // [E]   chunk_off of this chunk per expert
   int32_t* cx = co + E;                   // [E+1] exclusive scan of cl over experts
   int32_t* warp_tot = cx + E + 1;         // [33]
-  int32_t* slots_s = warp_tot + 33;       // [TPC*K]
+  int32_t* slots_s = warp_tot + 33 + ((5 * E + 35) & 1);   // [TPC*K], 8-byte aligned
   int32_t* sorted = slots_s + kLayoutTPC * K;  // [TPC*K] entries ordered by (expert, rank)
   int32_t* src = sorted + kLayoutTPC * K;      // [2*TPC] {t / T, t mod T} per token
 
@@ -865,7 +866,7 @@ __host__ __device__ constexpr int ClusterSmemWords(int E, int W, int K, int tpb,
   const int EW = E + W;
   return (ne ? NonExpandScratchWords(tpb, K, W) : 0)      // non-expand scratch (first: int2)
          + 2 * tpb                                        // tmask (64-bit words)
-         + kLayoutCountWarps * EW + 3 * EW                // whist, colcnt, tot, off
+         + kLayoutCountWarps * EW + 3 * EW + (EW & 1)     // whist, colcnt, tot, off (+ pad to even)
          + tpb * K                                        // ids
          + (ne ? 0 : 3 * tpb * K + 2 * tpb)               // loc, slots_s, sorted, src (expand)
          + 2 * (E + 1) + 33                               // psum_s, cx, warp_tot
@@ -918,7 +919,7 @@ __device__ __forceinline__ RangeSmem carve_range_smem(int32_t* sm, int E, int W,
   r.colcnt = r.whist + kLayoutCountWarps * EW;
   r.tot = r.colcnt + EW;
   r.off = r.tot + EW;
-  r.ids = r.off + EW;
+  r.ids = r.off + EW + (EW & 1);   // even offset: slots_s and src below are 8-byte aligned
   r.loc = r.ids + tpb * K;
   r.slots_s = r.loc + (NE ? 0 : tpb * K);
   r.sorted = r.slots_s + (NE ? 0 : tpb * K);
@@ -1217,7 +1218,7 @@ size_t count_smem(int, int cols) {
 }
 
 size_t slots_smem(int E, int topk) {
-  return sizeof(int32_t) * (5 * static_cast<size_t>(E) + 2 + 33 + 2 * kLayoutTPC * topk +
+  return sizeof(int32_t) * (5 * static_cast<size_t>(E) + 2 + 34 + 2 * kLayoutTPC * topk +
                             2 * kLayoutTPC);
 }
 
