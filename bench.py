@@ -434,6 +434,16 @@ def run_ours(args, rank, local_rank, world):
 
     e2e = run_e2e(args, ep, torch, dev, wl, topk_cpu, w_cpu, x, (h16, h8), (recv, recv8, scales),
                   step_bytes, world) if not args.no_e2e else None
+    # the decode workload (1024 tokens, the pages' small-batch shape), measured
+    # after the timed region as --all-configs measures it: context, not `value`
+    decode = None
+    if not args.no_decode:
+        d = measure_workload("decode", synth.WORKLOADS["decode"], False, 50, 5, ColdRegions(dev))
+        decode = {k: d[k] for k in ("workload", "tokens", "hidden", "experts", "topk", "l2", "timing",
+                                    "steps")}
+        for k in ("layout", "dispatch", "combine", "step"):
+            keep = ("us_median", "gbs", "frac_of_8tbs", "frac_of_peak", "tokens_per_s")
+            decode[k] = {kk: d[k][kk] for kk in keep + (("variant",) if k != "step" else ())}
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(wl, topk_cpu, w_cpu, x, budget_s=args.cpu_seconds)
@@ -458,6 +468,7 @@ def run_ours(args, rank, local_rank, world):
         "ms_per_step_x_sm_mhz": round(ms * clocks["sm_mhz"], 1) if clocks.get("sm_mhz") else None,
         "e2e": e2e,
         "cpu_baseline": cpu,
+        "decode_workload": decode,
     }
     return line
 
@@ -568,6 +579,106 @@ def host_link(torch, x_h, x_d, out_d, out_h, s_in, s_out, reps=5):
 
 # ------------------------------------------------------------- all configs
 
+class ColdRegions:
+    """The L2 flush (256 MB written, then 256 MB read) and the ~100 us GPU sleep
+    that precede every region timed by measure_workload, on one stream."""
+
+    def __init__(self, dev):
+        import torch
+        self.dev = dev
+        self.flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+        self.flush_read = torch.ones(256 << 20, dtype=torch.uint8, device=dev)
+        self.stream = torch.cuda.Stream(device=dev)
+
+    def __call__(self, i):
+        import torch
+        with torch.cuda.stream(self.stream):
+            self.flush.fill_(i & 0xFF)
+            self.flush_read.sum(dtype=torch.int32)
+            torch.cuda._sleep(SLEEP_CYCLES)
+
+
+def measure_workload(name, wl, ne, steps, warmup, cold):
+    """One workload's layout, dispatch, combine and step, each timed in its own
+    region after cold(i) (see run_all_configs); returns the JSON line's dict."""
+    import torch
+
+    import combine_ep_layout_gb300 as ep
+    import synth
+
+    dev, s = cold.dev, cold.stream
+    peak, peak_kind = measured_peaks()
+    N, H, K = wl.num_tokens, wl.hidden, wl.topk
+    cfg = ep.make_cfg(wl.world_size, H, wl.max_tok_per_rank, wl.num_expert_per_rank, K,
+                      wl.alignment, wl.dispatch_dtype, wl.use_weights and not ne, no_expand=ne)
+    R = ep.ep_recv_capacity(cfg)
+    h = ep.EpHandle(cfg)
+    topk = synth.gen_topk(wl).to(dev)
+    w = synth.gen_weights(wl).to(dev)
+    x = synth.gen_x(wl, device=dev)
+    fp8 = wl.dispatch_dtype == "fp8"
+    recv = torch.empty((R, H), dtype=torch.uint8 if fp8 else torch.bfloat16, device=dev)
+    scales = torch.empty((R, H // 128), dtype=torch.float32, device=dev) if fp8 else None
+    # combine reads bf16 expert outputs: the dispatched rows (identity experts), or
+    # for the FP8 workload an independent bf16 N(0,1) [Rcap, H]
+    y = synth.gen_y(wl, device=dev) if fp8 else recv
+    out = torch.empty((N, H), dtype=torch.bfloat16, device=dev)
+    wc = None if ne else w
+    regions = {
+        "layout": lambda: h.layout(topk, stream=s),
+        "dispatch": lambda: h.dispatch(x, recv, scales, stream=s),
+        "combine": lambda: h.combine(y, wc, out, stream=s),
+        "step": lambda: (h.layout(topk, stream=s), h.dispatch(x, recv, scales, stream=s),
+                         h.combine(y, wc, out, stream=s)),
+    }
+    times = {k: [] for k in regions}
+    for i in range(warmup + steps):
+        ev = []
+        for k, fn in regions.items():
+            cold(i)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(s)
+            fn()
+            b.record(s)
+            ev.append((k, a, b))
+        s.synchronize()
+        if i >= warmup:
+            for k, a, b in ev:
+                times[k].append(a.elapsed_time(b) * 1e3)
+    assert h.status() == 0
+    if ne:
+        rows = int(h.field(ep.FIELD_NUM_RECV).cpu()[0])
+        nb = algorithmic_bytes_nonexpand(N, H, K, rows, R, fp8)
+        dkey = "dispatch"
+    else:
+        nb = algorithmic_bytes(N, H, K, R)
+        dkey = "dispatch_fp8" if fp8 else "dispatch_bf16"
+    line = {"workload": name, "layout_kind": "non-expand" if ne else "expand",
+            "tokens": N, "hidden": H, "experts": wl.num_experts, "topk": K,
+            "alignment": wl.alignment, "dispatch_dtype": wl.dispatch_dtype,
+            "routing": wl.routing,
+            "l2": "flushed before every timed region (256 MB write, then 256 MB read)",
+            "timing": "device: each region enqueued behind a 100 us GPU sleep",
+            "steps": steps, "peak_gbs": peak, "peak_kind": peak_kind}
+    step_bytes = nb["layout"] + nb[dkey] + nb["combine"]
+    for k, b in (("layout", nb["layout"]), ("dispatch", nb[dkey]), ("combine", nb["combine"]),
+                 ("step", step_bytes)):
+        us = statistics.median(times[k])
+        line[k] = {"us_median": round(us, 2), "us_mean": round(statistics.mean(times[k]), 2),
+                   "us_min": round(min(times[k]), 2),
+                   "us_max": round(max(times[k]), 2), "algorithmic_bytes": b,
+                   "gbs": round(b / (us * 1e-6) / 1e9, 1),
+                   "frac_of_peak": round(b / (us * 1e-6) / 1e9 / peak, 4),
+                   "frac_of_8tbs": round(b / (us * 1e-6) / 1e9 / 8000.0, 4),
+                   "tokens_per_s": round(N / (us * 1e-6), 1)}
+        if k != "step":
+            line[k]["variant"] = h.variant({"layout": 0, "dispatch": 1, "combine": 2}[k])
+    h.free()
+    del recv, scales, y, out, x
+    torch.cuda.empty_cache()
+    return line
+
+
 def run_all_configs(args):
     """Per workload (tiny, decode, prefill bf16, prefill FP8, skewed) and layout
     (expand, then non-expand: one row per (token, rank), unweighted combine),
@@ -591,94 +702,15 @@ def run_all_configs(args):
     launch latency, which is longer than a small workload's kernels."""
     import torch
 
-    import combine_ep_layout_gb300 as ep
     import synth
 
     torch.cuda.set_device(0)
     dev = torch.device("cuda", 0)
-    peak, peak_kind = measured_peaks()
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
-    flush_read = torch.ones(256 << 20, dtype=torch.uint8, device=dev)
-    s = torch.cuda.Stream(device=dev)
     only = set(args.workload.split(",")) if args.workload else None
-
-    def cold(i):
-        with torch.cuda.stream(s):
-            flush.fill_(i & 0xFF)
-            flush_read.sum(dtype=torch.int32)
-            torch.cuda._sleep(SLEEP_CYCLES)
-
+    cold = ColdRegions(dev)
     for name, wl, ne in [(n, w, ne) for ne in (False, True) for n, w in synth.WORKLOADS.items()
                          if only is None or n in only]:
-        N, H, K = wl.num_tokens, wl.hidden, wl.topk
-        cfg = ep.make_cfg(wl.world_size, H, wl.max_tok_per_rank, wl.num_expert_per_rank, K,
-                          wl.alignment, wl.dispatch_dtype, wl.use_weights and not ne, no_expand=ne)
-        R = ep.ep_recv_capacity(cfg)
-        h = ep.EpHandle(cfg)
-        topk = synth.gen_topk(wl).to(dev)
-        w = synth.gen_weights(wl).to(dev)
-        x = synth.gen_x(wl, device=dev)
-        fp8 = wl.dispatch_dtype == "fp8"
-        recv = torch.empty((R, H), dtype=torch.uint8 if fp8 else torch.bfloat16, device=dev)
-        scales = torch.empty((R, H // 128), dtype=torch.float32, device=dev) if fp8 else None
-        # combine reads bf16 expert outputs: the dispatched rows (identity experts), or
-        # for the FP8 workload an independent bf16 N(0,1) [Rcap, H]
-        y = synth.gen_y(wl, device=dev) if fp8 else recv
-        out = torch.empty((N, H), dtype=torch.bfloat16, device=dev)
-        wc = None if ne else w
-        regions = {
-            "layout": lambda: h.layout(topk, stream=s),
-            "dispatch": lambda: h.dispatch(x, recv, scales, stream=s),
-            "combine": lambda: h.combine(y, wc, out, stream=s),
-            "step": lambda: (h.layout(topk, stream=s), h.dispatch(x, recv, scales, stream=s),
-                             h.combine(y, wc, out, stream=s)),
-        }
-        times = {k: [] for k in regions}
-        for i in range(args.warmup + args.steps):
-            ev = []
-            for k, fn in regions.items():
-                cold(i)
-                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                a.record(s)
-                fn()
-                b.record(s)
-                ev.append((k, a, b))
-            s.synchronize()
-            if i >= args.warmup:
-                for k, a, b in ev:
-                    times[k].append(a.elapsed_time(b) * 1e3)
-        assert h.status() == 0
-        if ne:
-            rows = int(h.field(ep.FIELD_NUM_RECV).cpu()[0])
-            nb = algorithmic_bytes_nonexpand(N, H, K, rows, R, fp8)
-            dkey = "dispatch"
-        else:
-            nb = algorithmic_bytes(N, H, K, R)
-            dkey = "dispatch_fp8" if fp8 else "dispatch_bf16"
-        line = {"workload": name, "layout_kind": "non-expand" if ne else "expand",
-                "tokens": N, "hidden": H, "experts": wl.num_experts, "topk": K,
-                "alignment": wl.alignment, "dispatch_dtype": wl.dispatch_dtype,
-                "routing": wl.routing,
-                "l2": "flushed before every timed region (256 MB write, then 256 MB read)",
-                "timing": "device: each region enqueued behind a 100 us GPU sleep",
-                "steps": args.steps, "peak_gbs": peak, "peak_kind": peak_kind}
-        step_bytes = nb["layout"] + nb[dkey] + nb["combine"]
-        for k, b in (("layout", nb["layout"]), ("dispatch", nb[dkey]), ("combine", nb["combine"]),
-                     ("step", step_bytes)):
-            us = statistics.median(times[k])
-            line[k] = {"us_median": round(us, 2), "us_mean": round(statistics.mean(times[k]), 2),
-                       "us_min": round(min(times[k]), 2),
-                       "us_max": round(max(times[k]), 2), "algorithmic_bytes": b,
-                       "gbs": round(b / (us * 1e-6) / 1e9, 1),
-                       "frac_of_peak": round(b / (us * 1e-6) / 1e9 / peak, 4),
-                       "frac_of_8tbs": round(b / (us * 1e-6) / 1e9 / 8000.0, 4),
-                       "tokens_per_s": round(N / (us * 1e-6), 1)}
-            if k != "step":
-                line[k]["variant"] = h.variant({"layout": 0, "dispatch": 1, "combine": 2}[k])
-        print(json.dumps(line), flush=True)
-        h.free()
-        del recv, scales, y, out, x
-        torch.cuda.empty_cache()
+        print(json.dumps(measure_workload(name, wl, ne, args.steps, args.warmup, cold)), flush=True)
     return 0
 
 
@@ -791,6 +823,8 @@ def main(argv=None):
                     help="device input/output buffers the end-to-end loop rotates through")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-decode", action="store_true",
+                    help="skip the decode-workload measurement added to the step line")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-block", type=int, default=256)
     ap.add_argument("--tokens", type=int, default=None,

@@ -68,3 +68,9 @@ def test_library_arm_line():
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] == 1 and cb["value"] > 0 and cb["sample"]
     assert d["config"]["tokens"] == 2048
+    # the decode workload measured beside the step (context for the small-batch shape)
+    dw = d["decode_workload"]
+    assert dw["workload"] == "decode" and dw["tokens"] == 1024
+    for k in ("layout", "dispatch", "combine", "step"):
+        assert dw[k]["us_median"] > 0 and dw[k]["gbs"] > 0
+    assert "_cluster_" in dw["layout"]["variant"]
