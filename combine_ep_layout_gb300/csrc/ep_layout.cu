@@ -1288,11 +1288,18 @@ size_t fused_smem(int E, int W, int K, int tpb, bool ne, int S) {
 FusedGeom fused_geom(const LayoutParams& p, const LaunchGeom& g) {
   FusedGeom f;
   if (p.fused_bar == nullptr || g.fused_blocks_per_sm <= 0 || p.num_tokens <= 0) return f;
-  // kLayoutTPC tokens per CTA while that gives at most one CTA per SM, else
-  // twice as many (measured at 32768 tokens: 256 ranges on 152 SMs took
-  // 16.5 us back to back, 128 ranges 14.5 us), unless pinned
+  // Unless pinned: the fewest tokens per CTA (a multiple of 32, from kLayoutTPC
+  // to kClusterMaxTPB) that give at most one range per SM, so that the
+  // metadata stores of the tail phase are spread over as many SMs as possible
+  // without two ranges sharing one.  Measured at 32768 tokens on 152 SMs (cold):
+  // 256 ranges of 128 tokens 18.4 us, 128 of 256 18.4 us, 147 of 224 17.2 us,
+  // 171 of 192 20.5 us.
   int tpb = g.fused_tpb;
-  if (tpb == 0) tpb = (p.num_tokens + kLayoutTPC - 1) / kLayoutTPC > g.num_sms ? 2 * kLayoutTPC : kLayoutTPC;
+  if (tpb == 0) {
+    const int per_sm = (p.num_tokens + g.num_sms - 1) / g.num_sms;
+    tpb = (per_sm + 31) / 32 * 32;
+    tpb = tpb < kLayoutTPC ? kLayoutTPC : (tpb > kClusterMaxTPB ? kClusterMaxTPB : tpb);
+  }
   const int64_t ranges = (p.num_tokens + tpb - 1) / tpb;
   const int64_t fill = p.rcap - static_cast<int64_t>(p.num_tokens) * p.topk;
   const int64_t fill_ctas = (fill + kFusedFillPerCta - 1) / kFusedFillPerCta;
@@ -1378,11 +1385,11 @@ cudaError_t prepare_layout(int, int, int, LaunchGeom* g) {
   e = cudaFuncSetAttribute(ep_layout_fused_kernel<KC, NE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(kClusterMaxSmem));
   if (e != cudaSuccess) return e;
-  // tokens per CTA of the fused kernel pinned by EP_GB300_LAYOUT_FUSED_TPB (64,
-  // 128 or 256); 0: chosen per launch from the batch size
+  // tokens per CTA of the fused kernel pinned by EP_GB300_LAYOUT_FUSED_TPB (a
+  // multiple of 32 from 64 to 256); 0: chosen per launch from the batch size
   const char* tenv = std::getenv("EP_GB300_LAYOUT_FUSED_TPB");
   const int t = tenv ? std::atoi(tenv) : 0;
-  g->fused_tpb = (t == 64 || t == 128 || t == 256) ? t : 0;
+  g->fused_tpb = (t >= 64 && t <= kClusterMaxTPB && t % 32 == 0) ? t : 0;
   const char* fenv = std::getenv("EP_GB300_LAYOUT_FUSED");
   // superchunk rows staged at most: enough for two resident CTAs per SM
   g->fused_max_super = (2 * g->num_sms + kFusedSuper - 1) / kFusedSuper;

@@ -81,10 +81,11 @@ def run(wl, topk, no_expand=False, expect="fused"):
     return h, got
 
 
-# every workload; prefill at 128 and 256 tokens per CTA (256 and 128 ranges),
-# the smaller ones also at 64 (many ranges: several superchunks)
-CASES = [(n, t) for n in ("tiny", "decode", "skewed") for t in (64, 128, 256)] + \
-        [(n, t) for n in ("prefill_bf16", "prefill_fp8") for t in (128, 256)]
+# every workload; prefill at 128, 224 and 256 tokens per CTA (256, 147 and 128
+# ranges), the smaller ones also at 64 (many ranges: several superchunks) and at
+# range sizes that are not powers of two
+CASES = [(n, t) for n in ("tiny", "decode", "skewed") for t in (64, 96, 128, 160, 256)] + \
+        [(n, t) for n in ("prefill_bf16", "prefill_fp8") for t in (128, 224, 256)]
 
 
 @pytest.mark.parametrize("name,tpb", CASES)
