@@ -548,6 +548,10 @@ __device__ void write_outputs_expand(const LayoutParams& p, const int32_t* cnt_s
   if (threadIdx.x == 0) *p.num_recv = psum_s[E];
 }
 
+template <int KC>
+__device__ void write_metadata_rows(const LayoutParams& p, int nvalid, const int32_t* sorted,
+                                    const int32_t* slots_s, const int32_t* src);
+
 // Slots and metadata of the tokens [t0, t0 + ntok) of this CTA (expand
 // layout; all threads call, entry i = (t - t0)*K + k spread over all of them).
 // psum_s [E+1] is the aligned expert prefix, co[E] the range's offset inside
@@ -563,7 +567,6 @@ __device__ void slots_expand_tokens(const LayoutParams& p, int t0, int ntok, con
                                     const int32_t* ids, int32_t* slots_s, int32_t* sorted,
                                     int32_t* src) {
   const int K = KC ? KC : p.topk;
-  const int KW = K + 2;  // metadata row width
   const int E = p.num_experts, T = p.max_tok_per_rank;
   const int nthr = blockDim.x;
   const int nent = ntok * K;
@@ -583,12 +586,22 @@ __device__ void slots_expand_tokens(const LayoutParams& p, int t0, int ntok, con
     src[2 * tl + 1] = t - r * T;
   }
   __syncthreads();
+  write_metadata_rows<KC>(p, cx[E], sorted, slots_s, src);
+}
 
-  // metadata rows of this range, in (expert, rank) order: flat words f of the
-  // concatenated rows; rows of one expert are contiguous in memory, so
-  // consecutive threads write consecutive words.  (One row per thread instead
-  // measured 29% slower at prefill: the stores lose their coalescing.)
-  const int nvalid = cx[E];
+// The metadata rows of a range, in (expert, rank) order: sorted[q] is the entry
+// of the range's q-th row (nvalid rows), slots_s[i] entry i's slot and src the
+// tokens' {t / T, t mod T} (both 8-byte aligned).  Flat words f of the
+// concatenated rows: rows of one expert are contiguous in memory, so
+// consecutive threads write consecutive words.  (One row per thread instead
+// measured 29% slower at prefill: the stores lose their coalescing.)  All
+// threads call, after a barrier that makes the inputs visible.
+template <int KC>
+__device__ void write_metadata_rows(const LayoutParams& p, int nvalid, const int32_t* sorted,
+                                    const int32_t* slots_s, const int32_t* src) {
+  const int K = KC ? KC : p.topk;
+  const int KW = K + 2;  // metadata row width
+  const int nthr = blockDim.x;
   if ((KW & 1) == 0) {
     // even row width: word pairs (8-byte stores; rows start 8-byte aligned)
     const int hw = KW / 2;
@@ -934,6 +947,60 @@ __device__ __forceinline__ RangeSmem carve_range_smem(int32_t* sm, int E, int W,
   return r;
 }
 
+// Local half of an expand range's slot pass (E <= kWarpScanMax), which needs nothing from the
+// other ranges: cx = exclusive scan over experts of the range's counts, the
+// entries ordered by (expert, rank) (sorted[cx[e] + loc[i]] = i) and each
+// token's {t / T, t mod T}.  The fused kernel runs it between arriving at its
+// grid barrier and waiting on it, while the other ranges are still counting.
+// All threads call, after a barrier that makes colcnt and loc visible.
+template <int KC>
+__device__ void presort_expand_range(const LayoutParams& p, const RangeSmem& r, int t0, int ntok) {
+  const int K = KC ? KC : p.topk;
+  const int E = p.num_experts, T = p.max_tok_per_rank;
+  // every warp but the last (whose lane 0 is arriving at the grid barrier, an
+  // atomic round trip through L2) takes part; they meet at named barrier 1
+  const int nthr = blockDim.x - 32, nent = ntok * K;
+  if (threadIdx.x >= nthr) return;
+  if ((threadIdx.x >> 5) == 0) warp_exclusive_scan(r.colcnt, E, 1, r.cx);   // E <= kWarpScanMax
+  asm volatile("bar.sync 1, %0;" ::"r"(nthr) : "memory");
+  for (int i = threadIdx.x; i < nent; i += nthr) {
+    const int e = r.ids[i];
+    if (e >= 0) r.sorted[r.cx[e] + r.loc[i]] = i;
+  }
+  for (int tl = threadIdx.x; tl < ntok; tl += nthr) {
+    const int t = t0 + tl, q = t / T;
+    r.src[2 * tl] = q;
+    r.src[2 * tl + 1] = t - q * T;
+  }
+}
+
+// The rest of an expand range (E <= kWarpScanMax) once presort_expand_range has run and r.tot
+// (totals over all ranges) and r.off (the sum over the ranges before this
+// one) are known: the aligned prefix over experts, CTA 0's outputs, the slots,
+// the metadata rows and this range's share of the rows that receive nothing.
+// All threads call, after a barrier that makes tot, off and the presort
+// visible.
+template <int KC>
+__device__ void finish_expand_presorted(const LayoutParams& p, const RangeSmem& r, int me, int nranges,
+                                        int t0, int ntok) {
+  const int K = KC ? KC : p.topk;
+  const int E = p.num_experts;
+  const int nthr = blockDim.x, nent = ntok * K;
+  if (threadIdx.x < 32) warp_exclusive_scan(r.tot, E, p.alignment, r.psum_s);   // E <= kWarpScanMax
+  __syncthreads();
+  if (me == 0) write_outputs_expand(p, r.tot, r.psum_s, r.tot + E);
+  int32_t* ds = p.dst_slot + static_cast<int64_t>(t0) * K;
+  for (int i = threadIdx.x; i < nent; i += nthr) {
+    const int e = r.ids[i];
+    const int slot = e >= 0 ? r.psum_s[e] + r.off[e] + r.loc[i] : -1;
+    ds[i] = slot;
+    r.slots_s[i] = slot;
+  }
+  __syncthreads();
+  write_metadata_rows<KC>(p, r.cx[E], r.sorted, r.slots_s, r.src);
+  fill_unreceived(p, r.psum_s, r.tot, r.psum_s[E], me, nranges);
+}
+
 // The rest of a range once r.tot (totals over all ranges) and r.off (the sum
 // over the ranges before this one) are known, for range `me` of `nranges`:
 // prefix sums, CTA 0's outputs, slots, metadata and this range's share of the
@@ -982,7 +1049,9 @@ __global__ void __launch_bounds__(kClusterThreads, 1) ep_layout_cluster_kernel(L
   count_tokens<KC>(p, t0, ntok, r.whist, r.tmask, r.colcnt, r.ids, regs);
 
   // every CTA's column totals are complete: gather the cluster's totals and
-  // this CTA's offsets from the other CTAs' shared memory
+  // this CTA's offsets from the other CTAs' shared memory.  (The CTAs of a
+  // cluster finish counting together, so there is no wait here to hide the
+  // range's local work behind, as the fused kernel does: measured slower.)
   cluster_arrive();
   cluster_wait();
   if constexpr (!NE) write_range_ranks<KC>(ntok, K, r.whist, EW, regs, r.loc);
@@ -1060,36 +1129,56 @@ __host__ __device__ constexpr int FusedStageWords(int S, int EW8) {
   return S * EW8 + (kFusedSuper / 2) * EW8;
 }
 
-// Barrier over the nctas CTAs of a cooperative grid; every thread of every CTA
-// calls it.  bar[0] counts arrivals and only grows (modulo 2^32); bar[1] is
-// its value when this launch began and bar[2] the number of launches so far,
-// both read by each CTA before it arrives (they change only after every CTA
-// has arrived: the last arrival sets them for the next launch).  A CTA
+// Barrier over the nctas CTAs of a cooperative grid, in two halves so that a
+// CTA can do local work between arriving and waiting; every thread of every
+// CTA calls both.  bar[0] counts arrivals and only grows (modulo 2^32); bar[1]
+// is its value when this launch began and bar[2] the number of launches so
+// far, both read by each CTA before it arrives (they change only after every
+// CTA has arrived: the last arrival sets them for the next launch).  A CTA
 // arrives with one atomic add and waits (acquire) until the counter reaches
-// bar[1] + nctas.  The state stays consistent for the next launch whatever the
-// grid size, also when a wait gives up: every CTA arrives exactly once.  A
-// wait is bounded by wait_ns (the deadline is checked before each test, so
-// wait_ns = 0 gives up at once); the function returns false, for every thread
-// of the CTA, when this CTA's wait gave up.
-__device__ bool fused_grid_barrier(unsigned* bar, unsigned base, unsigned gen, unsigned nctas,
-                                   uint64_t wait_ns, int32_t* ok_s) {
+// bar[1] + nctas.  The state stays consistent for the next launch whatever
+// the grid size, also when a wait gives up: every CTA arrives exactly once.
+struct GridArrival {
+  unsigned target;  // counter value once every CTA has arrived
+  bool last;        // this CTA arrived last (thread 0's value)
+};
+
+// The arriving (and later waiting) thread: lane 0 of the CTA's last warp, so
+// that the fence and the atomic round trip of the arrival stall no warp that
+// the local work between the halves uses.
+__device__ __forceinline__ bool is_arriving_thread() { return threadIdx.x == blockDim.x - 32; }
+
+__device__ GridArrival fused_grid_arrive(unsigned* bar, unsigned base, unsigned gen, unsigned nctas) {
   __syncthreads();  // this CTA's writes are done
-  if (threadIdx.x == 0) {
-    int ok = 1;
+  GridArrival a{base + nctas, false};
+  if (is_arriving_thread()) {
     __threadfence();  // ... and visible at gpu scope before the arrival
-    const unsigned target = base + nctas;
     const unsigned arrival = atomicAdd(bar, 1u);
-    if (arrival == target - 1u) {
-      bar[1] = target;  // the next launch's base and count (read after this kernel)
+    if (arrival == a.target - 1u) {
+      bar[1] = a.target;  // the next launch's base and count (read after this kernel)
       bar[2] = gen + 1u;
-    } else {
+      a.last = true;
+      __threadfence();  // order this CTA's later reads after every arrival it observed
+    }
+  }
+  return a;
+}
+
+// The waiting half, bounded by wait_ns (the deadline is checked before each
+// test, so wait_ns = 0 gives up at once unless this CTA arrived last); returns
+// false, for every thread of the CTA, when this CTA's wait gave up.
+__device__ bool fused_grid_wait(const unsigned* bar, const GridArrival& a, uint64_t wait_ns,
+                                int32_t* ok_s) {
+  if (is_arriving_thread()) {
+    int ok = 1;
+    if (!a.last) {
       const uint64_t t0 = global_ns();
       for (;;) {
         if (global_ns() - t0 >= wait_ns) {
           ok = 0;
           break;
         }
-        if (static_cast<int>(ld_acquire_gpu(bar) - target) >= 0) break;
+        if (static_cast<int>(ld_acquire_gpu(bar) - a.target) >= 0) break;
       }
     }
     *ok_s = ok;
@@ -1146,7 +1235,11 @@ __global__ void __launch_bounds__(kCountThreads, 2) ep_layout_fused_kernel(Layou
   for (int64_t f = static_cast<int64_t>(c) * nthr + tid; f < sup_words; f += static_cast<int64_t>(C) * nthr)
     sup_next[f] = 0;  // the next launch's buffer
 
-  if (!fused_grid_barrier(p.fused_bar, base, gen, static_cast<unsigned>(C), p.wait_ns, r.misc + 1)) {
+  // the range's local work runs between arriving and waiting (up to 512 experts)
+  const bool presort = !NE && E <= kWarpScanMax;
+  const GridArrival arrival = fused_grid_arrive(p.fused_bar, base, gen, static_cast<unsigned>(C));
+  if (presort) presort_expand_range<KC>(p, r, t0, ntok);
+  if (!fused_grid_wait(p.fused_bar, arrival, p.wait_ns, r.misc + 1)) {
     if (tid == 0) atomicOr(p.err, kErrTimeout);
     return;  // uniform per CTA
   }
@@ -1192,7 +1285,8 @@ __global__ void __launch_bounds__(kCountThreads, 2) ep_layout_fused_kernel(Layou
     r.off[j] = pre;
   }
   __syncthreads();
-  finish_range<KC, NE>(p, r, c, C, t0, ntok, tpb);
+  if (presort) finish_expand_presorted<KC>(p, r, c, C, t0, ntok);
+  else finish_range<KC, NE>(p, r, c, C, t0, ntok, tpb);
 }
 
 // ---------------------------------------------------------------- launch
