@@ -160,7 +160,12 @@ int ep_handle_create_shared(const ep_cfg_t *cfg, ep_handle_t layout_src, ep_hand
  *   send_slot [num_tokens, K]                  t's distinct rows, ascending, then -1
  *   recv_src_metadata [Rcap, K+2]              {t / T, t mod T, dst_slot[t][0..K-1]} per row
  * 0 <= num_tokens <= W*T, else EP_EINVAL.  The number of tokens is kept in the
- * handle for the following ep_dispatch / ep_combine calls. */
+ * handle for the following ep_dispatch / ep_combine calls.
+ * Mid-size batches run as one cooperative launch whose CTAs meet at a grid
+ * barrier; each wait there is bounded (EP_GB300_WAIT_NS when the handle was
+ * created, default 1 s) and a CTA that gives up records the value 2 (bit 1)
+ * in the device error word and leaves its part of the outputs unwritten.  A
+ * cooperative launch that cannot be resident at once fails with EP_ECUDA. */
 int ep_layout(ep_handle_t h, const int64_t *topk_idx, int32_t num_tokens, ep_stream_t stream) EP_NOEXCEPT;
 
 /* Dispatch ("Dispatch data flow": token data + scale factors to the receive
@@ -286,7 +291,8 @@ int ep_handle_get(ep_handle_t h, int32_t field, void **dev_ptr, int64_t *numel) 
 /* Read and clear the sticky device error word, in order on the stream of
  * the handle's last layout / dispatch / combine call, and wait for that
  * stream only.  Values: 1 (bit 0) = a topk id outside [-1, E) was skipped;
- * 2 (bit 1) is reserved for a kernel that gives up a bounded wait.  Returns EP_ECUDA if the
+ * 2 (bit 1) = a kernel gave up a bounded wait (the layout's grid barrier, the
+ * TMA dispatch's copies).  Returns EP_ECUDA if the
  * copy or the synchronisation fails. */
 int ep_handle_status(ep_handle_t h, int32_t *device_error) EP_NOEXCEPT;
 
@@ -297,7 +303,10 @@ int ep_handle_status(ep_handle_t h, int32_t *device_error) EP_NOEXCEPT;
  * layout it names what the last ep_layout ran: "ep_layout_cluster_k8" for
  * the single-launch thread-block-cluster kernel that serves batches of up to
  * 2048 tokens (unless EP_GB300_LAYOUT_CLUSTER=0 when the handle was created),
- * "ep_layout_k8" for the three launches (count, spine, slots). */
+ * "ep_layout_fused_k8" for the single-launch cooperative kernel that serves
+ * batches of up to a few hundred ranges of 128-256 tokens (unless
+ * EP_GB300_LAYOUT_FUSED=0), "ep_layout_k8" for the three launches (count,
+ * spine, slots). */
 int ep_handle_variant(ep_handle_t h, int32_t step, char *buf, int32_t len) EP_NOEXCEPT;
 
 /* Run-time specialisation ("MORI JIT v2" §1-§3.4, §6 precompile; the JIT
