@@ -236,3 +236,25 @@ def test_fused_barrier_wait_limit_gives_up_cleanly(monkeypatch):
     h2.layout(topk.cuda())
     assert_layout_equal(gpu_fields(h2), ref_layout(wl, topk.numpy()))
     assert h2.status() == 0
+
+
+def test_fused_layouts_on_two_streams_at_once(fused):
+    """Two handles, each on its own stream, launch their cooperative layouts
+    back to back without synchronising, so the two grids run at the same time
+    where the GPU has room: each keeps its barrier and sums in its own handle,
+    and both give the oracle's layout."""
+    a = synth.WORKLOADS["prefill_bf16"]
+    b = synth.WORKLOADS["skewed"]
+    ha, hb = ep.EpHandle(cfg_of(a)), ep.EpHandle(cfg_of(b))
+    ta, tb = synth.gen_topk(a), synth.gen_topk(b, mask_frac=0.05)
+    da, db = ta.cuda(), tb.cuda()
+    sa, sb = torch.cuda.Stream(), torch.cuda.Stream()
+    torch.cuda.synchronize()
+    for _ in range(20):
+        ha.layout(da, stream=sa)
+        hb.layout(db, stream=sb)
+    torch.cuda.synchronize()
+    assert ran_path(ha.variant(0)) == "fused" and ran_path(hb.variant(0)) == "fused"
+    assert_layout_equal(gpu_fields(ha), ref_layout(a, ta.numpy()), "a")
+    assert_layout_equal(gpu_fields(hb), ref_layout(b, tb.numpy()), "b")
+    assert ha.status() == 0 and hb.status() == 0
