@@ -632,8 +632,11 @@ __device__ void fill_unreceived(const LayoutParams& p, const int32_t* psum_s, co
   const int KW = p.topk + 2;
   const int nthr = blockDim.x;
   if (cnt_s != nullptr && p.alignment > 1) {
+    // a warp per expert, experts dealt round-robin over the CTAs first (CTA
+    // `part` takes experts part, part + parts, ...), so that the padding is
+    // spread over the grid instead of loading its first CTAs
     const int lane = threadIdx.x & 31, nwarp = nthr >> 5;
-    for (int e = part * nwarp + (threadIdx.x >> 5); e < p.num_experts; e += parts * nwarp) {
+    for (int e = part + (threadIdx.x >> 5) * parts; e < p.num_experts; e += parts * nwarp) {
       const int64_t beg = static_cast<int64_t>(psum_s[e] + cnt_s[e]) * KW;
       const int64_t end = static_cast<int64_t>(psum_s[e + 1]) * KW;
       for (int64_t f = beg + lane; f < end; f += 32) p.meta[f] = -1;
