@@ -977,20 +977,18 @@ __device__ void presort_expand_range(const LayoutParams& p, const RangeSmem& r, 
   }
 }
 
-// The rest of an expand range (E <= kWarpScanMax) once presort_expand_range has run and r.tot
-// (totals over all ranges) and r.off (the sum over the ranges before this
-// one) are known: the aligned prefix over experts, CTA 0's outputs, the slots,
-// the metadata rows and this range's share of the rows that receive nothing.
-// All threads call, after a barrier that makes tot, off and the presort
-// visible.
+// The rest of an expand range (E <= kWarpScanMax) once presort_expand_range has
+// run and r.tot (totals over all ranges), r.off (the sum over the ranges
+// before this one) and r.psum_s (the aligned prefix over experts) are known:
+// CTA 0's outputs, the slots, the metadata rows and this range's share of the
+// rows that receive nothing.  All threads call, after a barrier that makes
+// them visible.
 template <int KC>
 __device__ void finish_expand_presorted(const LayoutParams& p, const RangeSmem& r, int me, int nranges,
                                         int t0, int ntok) {
   const int K = KC ? KC : p.topk;
   const int E = p.num_experts;
   const int nthr = blockDim.x, nent = ntok * K;
-  if (threadIdx.x < 32) warp_exclusive_scan(r.tot, E, p.alignment, r.psum_s);   // E <= kWarpScanMax
-  __syncthreads();
   if (me == 0) write_outputs_expand(p, r.tot, r.psum_s, r.tot + E);
   int32_t* ds = p.dst_slot + static_cast<int64_t>(t0) * K;
   for (int i = threadIdx.x; i < nent; i += nthr) {
@@ -1276,6 +1274,7 @@ __global__ void __launch_bounds__(kCountThreads, 2) ep_layout_fused_kernel(Layou
     }
   }
   __syncthreads();
+  int own_total = 0;   // thread e's expert column total (e < E)
   for (int j = tid; j < EW; j += nthr) {
     int pre = 0, all = 0;
     for (int s2 = 0; s2 < S; ++s2) {
@@ -1286,10 +1285,34 @@ __global__ void __launch_bounds__(kCountThreads, 2) ep_layout_fused_kernel(Layou
     for (int q = 0; q < nrow; ++q) pre += st_rows[q * EW8 + j];
     r.tot[j] = all;
     r.off[j] = pre;
+    if (j == tid) own_total = all;
   }
-  __syncthreads();
-  if (presort) finish_expand_presorted<KC>(p, r, c, C, t0, ntok);
-  else finish_range<KC, NE>(p, r, c, C, t0, ntok, tpb);
+  if (presort) {
+    // the aligned exclusive prefix over experts straight from the threads'
+    // own totals (thread e holds expert e; E <= kWarpScanMax = blockDim.x), a
+    // block scan instead of a single warp's pass over E values in shared memory
+    const int A = p.alignment;
+    const bool p2 = (A & (A - 1)) == 0;
+    const int v = tid < E ? (p2 ? align_to<true>(own_total, A) : align_to<false>(own_total, A)) : 0;
+    const int lane = tid & 31, warp = tid >> 5;
+    int incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (lane == 31) r.warp_tot[warp] = incl;
+    __syncthreads();   // also makes tot and off visible
+    int base = 0;
+    for (int w = 0; w < warp; ++w) base += r.warp_tot[w];
+    if (tid < E) r.psum_s[tid] = base + incl - v;
+    if (tid == E - 1) r.psum_s[E] = base + incl;
+    __syncthreads();
+    finish_expand_presorted<KC>(p, r, c, C, t0, ntok);
+  } else {
+    __syncthreads();
+    finish_range<KC, NE>(p, r, c, C, t0, ntok, tpb);
+  }
 }
 
 // ---------------------------------------------------------------- launch
