@@ -245,6 +245,48 @@ __device__ __forceinline__ void warp_exclusive_scan(const int32_t* v, int n, int
   else warp_exclusive_scan_a<false>(v, n, A, out);
 }
 
+// Two exclusive scans over the E <= blockDim.x experts at once, from values
+// the threads hold in registers (thread e: a = expert e's total, rounded up
+// to A into out_a; b = its count, into out_b; E+1 outputs each).  All threads
+// call; one block barrier inside, a second before returning so that both
+// outputs are visible.  warp_tot needs 2 * (blockDim.x / 32) words.
+__device__ void dual_block_scan(int a, int b, int A, int E, int32_t* out_a, int32_t* out_b,
+                                int32_t* warp_tot) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarp = blockDim.x >> 5;
+  const bool p2 = (A & (A - 1)) == 0;
+  const int va = tid < E ? (p2 ? align_to<true>(a, A) : align_to<false>(a, A)) : 0;
+  const int vb = tid < E ? b : 0;
+  int ia = va, ib = vb;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int ya = __shfl_up_sync(0xffffffffu, ia, o);
+    const int yb = __shfl_up_sync(0xffffffffu, ib, o);
+    if (lane >= o) {
+      ia += ya;
+      ib += yb;
+    }
+  }
+  if (lane == 31) {
+    warp_tot[warp] = ia;
+    warp_tot[nwarp + warp] = ib;
+  }
+  __syncthreads();
+  int ba = 0, bb = 0;
+  for (int w = 0; w < warp; ++w) {
+    ba += warp_tot[w];
+    bb += warp_tot[nwarp + w];
+  }
+  if (tid < E) {
+    out_a[tid] = ba + ia - va;
+    out_b[tid] = bb + ib - vb;
+  }
+  if (tid == E - 1) {
+    out_a[E] = ba + ia;
+    out_b[E] = bb + ib;
+  }
+  __syncthreads();
+}
+
 // Expert counts up to this many are scanned by single warps (no block barriers
 // inside the scan; at most 16 values per lane); larger ones by the whole block.
 constexpr int kWarpScanMax = 512;
@@ -1056,6 +1098,7 @@ __global__ void __launch_bounds__(kClusterThreads, 1) ep_layout_cluster_kernel(L
   cluster_arrive();
   cluster_wait();
   if constexpr (!NE) write_range_ranks<KC>(ntok, K, r.whist, EW, regs, r.loc);
+  int own_total = 0, own_count = 0;   // thread e's expert column: cluster total, own count
   for (int j = threadIdx.x; j < EW; j += kClusterThreads) {
     int v[kClusterCtas];
 #pragma unroll
@@ -1071,10 +1114,23 @@ __global__ void __launch_bounds__(kClusterThreads, 1) ep_layout_cluster_kernel(L
     }
     r.tot[j] = t;
     r.off[j] = o;
+    if (j == static_cast<int>(threadIdx.x)) {
+      own_total = t;
+      own_count = r.colcnt[j];
+    }
   }
   cluster_arrive_relaxed();  // this CTA is done reading remote shared memory
-  __syncthreads();
-  finish_range<KC, NE>(p, r, static_cast<int>(me), static_cast<int>(ncta), t0, ntok, tpb);
+  if (!NE && E <= kWarpScanMax) {
+    // both scans over experts from the threads' own values in registers:
+    // psum_s (aligned cluster totals) and cx (this range's counts)
+    dual_block_scan(own_total, own_count, p.alignment, E, r.psum_s, r.cx, r.warp_tot);
+    if (me == 0) write_outputs_expand(p, r.tot, r.psum_s, r.tot + E);
+    slots_expand_tokens<KC>(p, t0, ntok, r.psum_s, r.off, r.cx, r.loc, r.ids, r.slots_s, r.sorted, r.src);
+    fill_unreceived(p, r.psum_s, r.tot, r.psum_s[E], static_cast<int>(me), static_cast<int>(ncta));
+  } else {
+    __syncthreads();
+    finish_range<KC, NE>(p, r, static_cast<int>(me), static_cast<int>(ncta), t0, ntok, tpb);
+  }
   // keep this CTA's shared memory until every CTA has finished reading it
   cluster_wait();
 }
