@@ -8,22 +8,24 @@
 // entry is psum_expert[e] + (number of earlier entries routed to e): a stable
 // counting sort.  The tokens are cut into ranges, one per CTA; each range is
 // counted (count_tokens), the ranges' counts are scanned, and each range
-// writes its slots and metadata (slots_*_tokens).  Two ways to run that:
+// writes its slots and metadata.  Three ways to run that, by batch size:
+//
+// Counting (the same device code everywhere): a range's entries, flat index
+// (t - t0)*K + k, are cut into one run of whole 32-entry batches per warp;
+// each lane loads its ids straight into registers.  Per batch the lanes that
+// carry the same expert find each other with __match_any_sync, so one pass
+// gives each warp's histogram (a row private to the warp) and every entry's
+// rank among its warp's earlier entries of that expert.  A thread per column
+// then scans the 16 warps' counts (each warp's start, the range's total);
+// tokens per rank come from per-token rank masks counted with ballots.
 //
 // Large batches, three launches (the last two with programmatic dependent
 // launch so that each is scheduled while its predecessor drains; the last
-// one, like the cluster kernel, lets the dispatch that follows be scheduled
-// early too):
-//   count  one CTA per chunk of kLayoutTPC tokens.  The chunk's ids are staged
-//          in shared memory with one coalesced load and every pass runs from
-//          there.  Per-warp histograms over contiguous runs of entries use
-//          shared-memory atomics; an exclusive scan across the warps gives each
-//          warp its start per expert, and a pass over 32-entry batches that
-//          combines lanes carrying the same expert with __match_any_sync gives
-//          each entry its stable rank in the chunk.  Tokens per rank: each
-//          entry ORs its rank bit into its token's mask, then warp ballots
-//          count the set bits.  The chunk's column totals (E experts + W ranks)
-//          go to one contiguous row of a row-major [C][E+W] table.
+// one, like the single-launch kernels, lets the dispatch that follows be
+// scheduled early too):
+//   count  one CTA per chunk of kLayoutTPC tokens: the ranks go to dst_slot,
+//          the chunk's column totals (E experts + W ranks) to a row-major
+//          [C][E+W] table and a column-major copy.
 //   spine  a warp per column scans the C chunk totals (chunk offsets and
 //          column totals).
 //   slots  every CTA rebuilds the aligned exclusive prefix over the experts
@@ -47,8 +49,9 @@
 // Mid-size batches (as many ranges as a cooperative grid keeps resident), one
 // launch: the fused kernel counts each range like the cluster kernel, but
 // exchanges the column totals through L2 -- a row per range and atomic sums
-// per superchunk of 16 ranges -- around one grid barrier, then finishes its
-// range with the same device code.  This is the single-pass form of the
+// per superchunk of 16 ranges -- around one grid barrier (split into arrive
+// and wait, with the range's local sort in between), then finishes its range
+// with the same device code.  This is the single-pass form of the
 // counting the pages give the "notify warps" of the Dispatch data flow
 // figure: no count / scan / slots kernel boundaries, ranks kept on chip.
 //
