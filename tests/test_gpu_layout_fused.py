@@ -117,6 +117,9 @@ EDGE = {
     "zipf_hot": dict(base="skewed", num_tokens=4096),
     # 262080 padding rows: 32 CTAs for 8 ranges of tokens (the others only fill)
     "big_alignment": dict(base="decode", alignment=4096),
+    # more experts than one warp scans (600): the block-wide scans, no presort
+    "experts_600": dict(base="prefill_bf16", num_expert_per_rank=75, max_tok_per_rank=512,
+                        num_tokens=4096, alignment=4),
     # 17 superchunks of 16 ranges and a ragged last range
     "superchunks": dict(base="prefill_bf16", max_tok_per_rank=4352, num_tokens=34800),
 }

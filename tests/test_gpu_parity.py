@@ -567,6 +567,9 @@ SMALL = {
                 num_tokens=1024, topk=8),
     "epr7": dict(base="tiny", world_size=3, num_expert_per_rank=7, max_tok_per_rank=64,
                  num_tokens=150, alignment=5),
+    # more experts than one warp scans (600): the block-wide scans
+    "experts_600": dict(base="decode", num_expert_per_rank=75, max_tok_per_rank=256,
+                        num_tokens=2000, alignment=4),
 }
 
 
