@@ -720,6 +720,63 @@ def run_all_configs(args):
     return 0
 
 
+def run_mix_ceilings(args):
+    """Context for the roofline fractions: torch's own elementwise kernels timed
+    on the byte mixes of the prefill data kernels (32768 tokens, hidden 7168,
+    top-8, bf16), each in its own region after the same L2 flush and GPU sleep
+    as --all-configs:
+      write_only   fill a [N*K, H] buffer              (dispatch's write volume)
+      read_only    sum the [N*K, H] buffer              (combine's read volume)
+      copy_1to1    copy [N, H] -> [N, H]                (the measured-peak copy)
+      bcast_1to8   x[N, H] broadcast into [N, K, H]     (dispatch's mix, no index)
+      reduce_8to1  sum over K of [N, K, H] into [N, H]  (combine's mix, no index)
+    GB/s = bytes read + written / device time; best and median over args.steps."""
+    import torch
+
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    cold = ColdRegions(dev)
+    s = cold.stream
+    N, H, K = 32768, 7168, 8
+    big = torch.empty((N, K, H), dtype=torch.bfloat16, device=dev)
+    with torch.cuda.stream(s):
+        big.normal_()
+    x = big[:, 0].contiguous()
+    xo = torch.empty_like(x)
+    acc = torch.empty((), dtype=torch.float32, device=dev)
+    eb = 2
+    cases = {
+        "write_only": (lambda: big.fill_(1.0), N * K * H * eb),
+        "read_only": (lambda: torch.sum(big, dtype=torch.float32, out=acc), N * K * H * eb),
+        "copy_1to1": (lambda: xo.copy_(x), 2 * N * H * eb),
+        "bcast_1to8": (lambda: big.copy_(x[:, None, :].expand(N, K, H)), (K + 1) * N * H * eb),
+        "reduce_8to1": (lambda: torch.sum(big, dim=1, out=xo), (K + 1) * N * H * eb),
+    }
+    peak, peak_kind = measured_peaks()
+    line = {"mix_ceilings": "torch kernels on the prefill data kernels' byte mixes",
+            "tokens": N, "hidden": H, "topk": K, "dtype": "bf16",
+            "l2": "flushed before every timed region (256 MB write, then 256 MB read)",
+            "steps": args.steps, "peak_gbs": peak, "peak_kind": peak_kind, "cases": {}}
+    for name, (fn, nbytes) in cases.items():
+        ts = []
+        for i in range(args.warmup + args.steps):
+            cold(i)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(s):
+                a.record(s)
+                fn()
+                b.record(s)
+            s.synchronize()
+            if i >= args.warmup:
+                ts.append(a.elapsed_time(b) * 1e3)
+        best, med = min(ts), statistics.median(ts)
+        line["cases"][name] = {"bytes": nbytes, "us_best": round(best, 1), "us_median": round(med, 1),
+                               "gbs_best": round(nbytes / best / 1e3, 1),
+                               "gbs_median": round(nbytes / med / 1e3, 1)}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 # ------------------------------------------------------------- CPU oracle
 
 def oracle_bufs(wl, block):
@@ -839,6 +896,8 @@ def main(argv=None):
                     help="time layout / dispatch / combine on every workload (one line each)")
     ap.add_argument("--workload", default=None,
                     help="with --all-configs: comma-separated workload names (default: all)")
+    ap.add_argument("--mix-ceilings", action="store_true",
+                    help="time torch's copy kernels on the data kernels' read/write mixes")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -848,6 +907,8 @@ def main(argv=None):
         if line is not None:
             print(json.dumps(line), flush=True)
         return 0
+    if args.mix_ceilings:
+        return run_mix_ceilings(args)
     if args.all_configs:
         import __graft_entry__
         __graft_entry__.build()
