@@ -743,11 +743,10 @@ def run_mix_ceilings(args):
         big.normal_()
     x = big[:, 0].contiguous()
     xo = torch.empty_like(x)
-    acc = torch.empty((), dtype=torch.float32, device=dev)
     eb = 2
     cases = {
         "write_only": (lambda: big.fill_(1.0), N * K * H * eb),
-        "read_only": (lambda: torch.sum(big, dtype=torch.float32, out=acc), N * K * H * eb),
+        "read_only": (lambda: big.sum(dtype=torch.float32), N * K * H * eb),
         "copy_1to1": (lambda: xo.copy_(x), 2 * N * H * eb),
         "bcast_1to8": (lambda: big.copy_(x[:, None, :].expand(N, K, H)), (K + 1) * N * H * eb),
         "reduce_8to1": (lambda: torch.sum(big, dim=1, out=xo), (K + 1) * N * H * eb),
