@@ -720,58 +720,192 @@ def run_all_configs(args):
     return 0
 
 
+# Probe kernels for --mix-ceilings: the memory traffic of the data kernels
+# with no routing (no index loads, contiguous destinations, xor instead of the
+# fold), so that their times are what the memory system gives these byte mixes.
+MIX_PROBE_CU = r"""
+#include <cstdint>
+#include <cuda_runtime.h>
+struct V8 { uint32_t w[8]; };
+__device__ __forceinline__ void ld8(const uint8_t* p, V8& v) {
+  asm volatile("ld.global.cg.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3]), "=r"(v.w[4]),
+                 "=r"(v.w[5]), "=r"(v.w[6]), "=r"(v.w[7]) : "l"(p));
+}
+__device__ __forceinline__ void st8(uint8_t* p, const V8& v) {
+  asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" :: "l"(p), "r"(v.w[0]),
+               "r"(v.w[1]), "r"(v.w[2]), "r"(v.w[3]), "r"(v.w[4]), "r"(v.w[5]), "r"(v.w[6]),
+               "r"(v.w[7]) : "memory");
+}
+// grid-stride over n32 32-byte vectors
+__global__ void write_only(uint8_t* dst, int64_t n32) {
+  V8 v;
+  for (int j = 0; j < 8; ++j) v.w[j] = 0x3f803f80u + j;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n32; i += stride)
+    st8(dst + i * 32, v);
+}
+__global__ void read_only(const uint8_t* src, int64_t n32, uint32_t* sink) {
+  uint32_t acc = 0;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  for (; i + 3 * stride < n32; i += 4 * stride) {
+    V8 a, b, c, d;
+    ld8(src + i * 32, a); ld8(src + (i + stride) * 32, b);
+    ld8(src + (i + 2 * stride) * 32, c); ld8(src + (i + 3 * stride) * 32, d);
+    for (int j = 0; j < 8; ++j) acc ^= a.w[j] ^ b.w[j] ^ c.w[j] ^ d.w[j];
+  }
+  for (; i < n32; i += stride) {
+    V8 a;
+    ld8(src + i * 32, a);
+    for (int j = 0; j < 8; ++j) acc ^= a.w[j];
+  }
+  if (acc == 0x9e3779b9u) sink[0] = acc;  // keeps the loads
+}
+__global__ void copy_1to1(const uint8_t* src, uint8_t* dst, int64_t n32) {
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n32; i += stride) {
+    V8 a;
+    ld8(src + i * 32, a);
+    st8(dst + i * 32, a);
+  }
+}
+// a CTA per row of `vecs` 32-byte vectors, 2 per thread (blockDim = vecs / 2):
+// row t read once and written to rows t*K .. t*K+K-1 (dispatch's mix), or rows
+// t*K .. t*K+K-1 read and their xor written to row t (combine's mix)
+template <int K>
+__global__ void bcast(const uint8_t* x, uint8_t* big, int row) {
+  const int64_t t = blockIdx.x;
+  const int T = blockDim.x;
+  V8 a, b;
+  ld8(x + t * row + threadIdx.x * 32, a);
+  ld8(x + t * row + (threadIdx.x + T) * 32, b);
+  for (int k = 0; k < K; ++k) {
+    uint8_t* d = big + (t * K + k) * row;
+    st8(d + threadIdx.x * 32, a);
+    st8(d + (threadIdx.x + T) * 32, b);
+  }
+}
+template <int K>
+__global__ void reduce(const uint8_t* big, uint8_t* out, int row) {
+  const int64_t t = blockIdx.x;
+  const int T = blockDim.x;
+  V8 a[K], b[K];
+#pragma unroll
+  for (int k = 0; k < K; ++k) {
+    const uint8_t* s = big + (t * K + k) * row;
+    ld8(s + threadIdx.x * 32, a[k]);
+    ld8(s + (threadIdx.x + T) * 32, b[k]);
+  }
+#pragma unroll
+  for (int k = 1; k < K; ++k)
+    for (int j = 0; j < 8; ++j) { a[0].w[j] ^= a[k].w[j]; b[0].w[j] ^= b[k].w[j]; }
+  st8(out + t * row + threadIdx.x * 32, a[0]);
+  st8(out + t * row + (threadIdx.x + T) * 32, b[0]);
+}
+extern "C" int mix_write(void* d, long long n32, int g, int b, void* s) {
+  write_only<<<g, b, 0, (cudaStream_t)s>>>((uint8_t*)d, n32); return (int)cudaGetLastError();
+}
+extern "C" int mix_read(const void* x, long long n32, void* sink, int g, int b, void* s) {
+  read_only<<<g, b, 0, (cudaStream_t)s>>>((const uint8_t*)x, n32, (uint32_t*)sink);
+  return (int)cudaGetLastError();
+}
+extern "C" int mix_copy(const void* x, void* d, long long n32, int g, int b, void* s) {
+  copy_1to1<<<g, b, 0, (cudaStream_t)s>>>((const uint8_t*)x, (uint8_t*)d, n32);
+  return (int)cudaGetLastError();
+}
+extern "C" int mix_bcast8(const void* x, void* big, int n, int row, void* s) {
+  bcast<8><<<n, row / 64, 0, (cudaStream_t)s>>>((const uint8_t*)x, (uint8_t*)big, row);
+  return (int)cudaGetLastError();
+}
+extern "C" int mix_reduce8(const void* big, void* out, int n, int row, void* s) {
+  reduce<8><<<n, row / 64, 0, (cudaStream_t)s>>>((const uint8_t*)big, (uint8_t*)out, row);
+  return (int)cudaGetLastError();
+}
+"""
+
+
 def run_mix_ceilings(args):
-    """Context for the roofline fractions: torch's own elementwise kernels timed
-    on the byte mixes of the prefill data kernels (32768 tokens, hidden 7168,
-    top-8, bf16), each in its own region after the same L2 flush and GPU sleep
-    as --all-configs:
-      write_only   fill a [N*K, H] buffer              (dispatch's write volume)
-      read_only    sum the [N*K, H] buffer              (combine's read volume)
-      copy_1to1    copy [N, H] -> [N, H]                (the measured-peak copy)
-      bcast_1to8   x[N, H] broadcast into [N, K, H]     (dispatch's mix, no index)
-      reduce_8to1  sum over K of [N, K, H] into [N, H]  (combine's mix, no index)
-    GB/s = bytes read + written / device time; best and median over args.steps."""
+    """What the memory system gives the data kernels' byte mixes on the prefill
+    shape (32768 tokens, rows of 7168 bf16 = 14336 bytes, top-8): probe kernels
+    (MIX_PROBE_CU, compiled here with nvcc) that move the same bytes as the data
+    kernels with no routing, each timed in its own region after the same L2
+    flush and GPU sleep as --all-configs:
+      write_only   fill the [N*K] rows                   (dispatch's write volume)
+      read_only    read the [N*K] rows                   (combine's read volume)
+      copy_1to1    copy [N] rows                         (the measured-peak copy)
+      bcast_1to8   row t -> rows t*K..t*K+K-1, a CTA per row      (dispatch's mix)
+      reduce_8to1  rows t*K..t*K+K-1 -> row t, a CTA per row      (combine's mix)
+    The grid-stride cases run several grids (SMs x 2..16 CTAs of 256 or 512
+    threads); the best is reported with its geometry.  GB/s = bytes read +
+    written / device time; best and median over args.steps."""
+    import ctypes
+
     import torch
 
+    from combine_ep_layout_gb300 import build as native_build
+
+    out_dir = os.path.join(ROOT, "_build")
+    os.makedirs(out_dir, exist_ok=True)
+    src, so = os.path.join(out_dir, "mix_probe.cu"), os.path.join(out_dir, "mix_probe.so")
+    with open(src, "w") as f:
+        f.write(MIX_PROBE_CU)
+    subprocess.check_call([native_build.nvcc(), "-gencode", "arch=compute_103a,code=sm_103a", "-O3",
+                           "-shared", "-Xcompiler", "-fPIC", "-o", so, src])
+    lib = ctypes.CDLL(so)
     torch.cuda.set_device(0)
     dev = torch.device("cuda", 0)
     cold = ColdRegions(dev)
     s = cold.stream
-    N, H, K = 32768, 7168, 8
-    big = torch.empty((N, K, H), dtype=torch.bfloat16, device=dev)
-    with torch.cuda.stream(s):
-        big.normal_()
-    x = big[:, 0].contiguous()
-    xo = torch.empty_like(x)
-    eb = 2
-    cases = {
-        "write_only": (lambda: big.fill_(1.0), N * K * H * eb),
-        "read_only": (lambda: big.sum(dtype=torch.float32), N * K * H * eb),
-        "copy_1to1": (lambda: xo.copy_(x), 2 * N * H * eb),
-        "bcast_1to8": (lambda: big.copy_(x[:, None, :].expand(N, K, H)), (K + 1) * N * H * eb),
-        "reduce_8to1": (lambda: torch.sum(big, dim=1, out=xo), (K + 1) * N * H * eb),
-    }
+    sp = ctypes.c_void_p(s.cuda_stream)
+    N, K, H = 32768, 8, 7168
+    row = H * 2
+    big = torch.empty(N * K * row, dtype=torch.uint8, device=dev)
+    x = torch.randint(0, 255, (N * row,), dtype=torch.uint8, device=dev)
+    out = torch.empty(N * row, dtype=torch.uint8, device=dev)
+    sink = torch.zeros(4, dtype=torch.int32, device=dev)
+    P = ctypes.c_void_p
+    nbig, nx = big.numel() // 32, x.numel() // 32
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    grids = [(sms * c, b) for c in (2, 4, 8, 16) for b in (256, 512)]
+    cases = []
+    for g, b in grids:
+        cases.append(("write_only", "%d x %d" % (g, b), big.numel(),
+                      lambda g=g, b=b: lib.mix_write(P(big.data_ptr()), ctypes.c_longlong(nbig), g, b, sp)))
+        cases.append(("read_only", "%d x %d" % (g, b), big.numel(),
+                      lambda g=g, b=b: lib.mix_read(P(big.data_ptr()), ctypes.c_longlong(nbig),
+                                                    P(sink.data_ptr()), g, b, sp)))
+        cases.append(("copy_1to1", "%d x %d" % (g, b), 2 * x.numel(),
+                      lambda g=g, b=b: lib.mix_copy(P(x.data_ptr()), P(out.data_ptr()),
+                                                    ctypes.c_longlong(nx), g, b, sp)))
+    cases.append(("bcast_1to8", "%d x %d" % (N, row // 64), (K + 1) * N * row,
+                  lambda: lib.mix_bcast8(P(x.data_ptr()), P(big.data_ptr()), N, row, sp)))
+    cases.append(("reduce_8to1", "%d x %d" % (N, row // 64), (K + 1) * N * row,
+                  lambda: lib.mix_reduce8(P(big.data_ptr()), P(out.data_ptr()), N, row, sp)))
     peak, peak_kind = measured_peaks()
-    line = {"mix_ceilings": "torch kernels on the prefill data kernels' byte mixes",
-            "tokens": N, "hidden": H, "topk": K, "dtype": "bf16",
+    line = {"mix_ceilings": "probe kernels moving the prefill data kernels' bytes with no routing",
+            "tokens": N, "row_bytes": row, "topk": K,
             "l2": "flushed before every timed region (256 MB write, then 256 MB read)",
             "steps": args.steps, "peak_gbs": peak, "peak_kind": peak_kind, "cases": {}}
-    for name, (fn, nbytes) in cases.items():
+    for name, geom, nbytes, fn in cases:
         ts = []
         for i in range(args.warmup + args.steps):
             cold(i)
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            with torch.cuda.stream(s):
-                a.record(s)
-                fn()
-                b.record(s)
+            a.record(s)
+            rc = fn()
+            b.record(s)
             s.synchronize()
+            if rc != 0:
+                raise RuntimeError("mix probe %s launch failed: %d" % (name, rc))
             if i >= args.warmup:
                 ts.append(a.elapsed_time(b) * 1e3)
         best, med = min(ts), statistics.median(ts)
-        line["cases"][name] = {"bytes": nbytes, "us_best": round(best, 1), "us_median": round(med, 1),
-                               "gbs_best": round(nbytes / best / 1e3, 1),
-                               "gbs_median": round(nbytes / med / 1e3, 1)}
+        r = {"grid": geom, "bytes": nbytes, "us_best": round(best, 1), "us_median": round(med, 1),
+             "gbs_best": round(nbytes / best / 1e3, 1), "gbs_median": round(nbytes / med / 1e3, 1)}
+        prev = line["cases"].get(name)
+        if prev is None or r["gbs_median"] > prev["gbs_median"]:
+            line["cases"][name] = r
     print(json.dumps(line), flush=True)
     return 0
 
@@ -896,7 +1030,7 @@ def main(argv=None):
     ap.add_argument("--workload", default=None,
                     help="with --all-configs: comma-separated workload names (default: all)")
     ap.add_argument("--mix-ceilings", action="store_true",
-                    help="time torch's copy kernels on the data kernels' read/write mixes")
+                    help="time probe kernels that move the data kernels' bytes with no routing")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

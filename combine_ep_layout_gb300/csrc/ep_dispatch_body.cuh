@@ -92,6 +92,31 @@ __device__ __forceinline__ void forward_routing(const DispatchParams& p, int t, 
   }
 }
 
+// The K slots of a token (sl) as the compiled row kernels read them.  With row
+// slices (S > 1: small batches, one short-lived wave) lane k of each warp loads
+// slot k up front, in flight with the row's loads, and the store loop takes it
+// from that lane: one round trip instead of K dependent ones between the stores
+// (decode, 1024 tokens: FP8 dispatch 16.9 -> 14.3 us, bf16 20.9 -> 20.5 us).
+// With one CTA per row (large batches) slot k is loaded right before its
+// stores: that pacing of each CTA's stores measured 1.2% faster at 32768 tokens
+// (627 vs 635 us, bf16) than issuing all of them at once.  All lanes of the
+// warp call both (the row kernels' CTAs are whole warps); K <= kMaxTopk (16).
+static_assert(kMaxTopk <= 32, "a warp holds one slot per lane");
+template <int S>
+struct RowSlots {
+  int32_t lane_slot = -1;
+  __device__ __forceinline__ RowSlots(const int32_t* sl, int K) {
+    if constexpr (S > 1) {
+      const int lane = threadIdx.x & 31;
+      if (lane < K) lane_slot = ld_coherent(sl + lane);
+    }
+  }
+  __device__ __forceinline__ int32_t at(const int32_t* sl, int k) const {
+    if constexpr (S > 1) return __shfl_sync(0xffffffffu, lane_slot, k);
+    else return ld_coherent(sl + k);
+  }
+};
+
 // ---- copy (bf16, fp32 and packed-fp4 transports) ------------------------------
 
 // S > 1 (compiled row geometries only): each row is split into S contiguous
@@ -118,6 +143,7 @@ __device__ __forceinline__ void dispatch_copy_body(const DispatchParams& p) {
   grid_dependency_wait();
   if constexpr (T != 0) {
     constexpr int PER = CH / T;
+    const RowSlots<S> slots(sl, K);
     Vec<V> v[PER];
 #pragma unroll
     for (int u = 0; u < PER; ++u)
@@ -125,7 +151,7 @@ __device__ __forceinline__ void dispatch_copy_body(const DispatchParams& p) {
 #pragma unroll
     for (int k = 0; k < KM; ++k) {
       if (k >= K) break;
-      const int32_t d = ld_coherent(sl + k);
+      const int32_t d = slots.at(sl, k);
       if (d < 0) continue;
       uint8_t* dr = rx + static_cast<int64_t>(d) * row + base;
 #pragma unroll
@@ -242,6 +268,7 @@ __device__ __forceinline__ void dispatch_fp8_body(const DispatchParams& p) {
   grid_dependency_wait();
   if constexpr (T != 0) {
     constexpr int PER = CH / T;
+    const RowSlots<S> slots(sl, K);
     Vec<V> v[PER];
 #pragma unroll
     for (int u = 0; u < PER; ++u)
@@ -253,7 +280,7 @@ __device__ __forceinline__ void dispatch_fp8_body(const DispatchParams& p) {
 #pragma unroll
     for (int k = 0; k < KM; ++k) {
       if (k >= K) break;
-      const int32_t d = ld_coherent(sl + k);
+      const int32_t d = slots.at(sl, k);
       if (d < 0) continue;
 #pragma unroll
       for (int u = 0; u < PER; ++u) {

@@ -77,3 +77,34 @@ def test_library_arm_line():
     for k in ("layout", "dispatch", "combine", "step"):
         assert dw[k]["us_median"] > 0 and dw[k]["gbs"] > 0
     assert dw["layout"]["variant"].startswith("ep_layout_")
+
+
+def test_mix_probe_kernels_compile(tmp_path):
+    """The --mix-ceilings probe kernels build for sm_103a (nvcc cross-compiles
+    without a GPU) and export the launchers bench.py calls."""
+    import shutil
+    nvcc = shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc"
+    if not os.path.exists(nvcc):
+        pytest.skip("no nvcc")
+    sys.path.insert(0, ROOT)
+    import bench
+    src, so = tmp_path / "mix_probe.cu", tmp_path / "mix_probe.so"
+    src.write_text(bench.MIX_PROBE_CU)
+    subprocess.check_call([nvcc, "-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-shared",
+                           "-Xcompiler", "-fPIC", "-o", str(so), str(src)], timeout=300)
+    import ctypes
+    lib = ctypes.CDLL(str(so))
+    for name in ("mix_write", "mix_read", "mix_copy", "mix_bcast8", "mix_reduce8"):
+        assert hasattr(lib, name)
+
+
+@pytest.mark.gpu
+def test_mix_ceilings_line():
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--mix-ceilings",
+                        "--steps", "2", "--warmup", "3"], cwd=ROOT, capture_output=True, text=True,
+                       timeout=900)
+    assert r.returncode == 0, r.stdout[-2000:] + r.stderr[-2000:]
+    d = json.loads([l for l in r.stdout.splitlines() if l.startswith("{")][-1])
+    assert set(d["cases"]) == {"write_only", "read_only", "copy_1to1", "bcast_1to8", "reduce_8to1"}
+    for c in d["cases"].values():
+        assert c["us_best"] > 0 and c["gbs_best"] >= c["gbs_median"] > 0
