@@ -634,6 +634,7 @@ def measure_workload(name, wl, ne, steps, warmup, cold):
         "layout": lambda: h.layout(topk, stream=s),
         "dispatch": lambda: h.dispatch(x, recv, scales, stream=s),
         "combine": lambda: h.combine(y, wc, out, stream=s),
+        "layout_dispatch": lambda: (h.layout(topk, stream=s), h.dispatch(x, recv, scales, stream=s)),
         "step": lambda: (h.layout(topk, stream=s), h.dispatch(x, recv, scales, stream=s),
                          h.combine(y, wc, out, stream=s)),
     }
@@ -668,7 +669,7 @@ def measure_workload(name, wl, ne, steps, warmup, cold):
             "steps": steps, "peak_gbs": peak, "peak_kind": peak_kind}
     step_bytes = nb["layout"] + nb[dkey] + nb["combine"]
     for k, b in (("layout", nb["layout"]), ("dispatch", nb[dkey]), ("combine", nb["combine"]),
-                 ("step", step_bytes)):
+                 ("layout_dispatch", nb["layout"] + nb[dkey]), ("step", step_bytes)):
         us = statistics.median(times[k])
         line[k] = {"us_median": round(us, 2), "us_mean": round(statistics.mean(times[k]), 2),
                    "us_min": round(min(times[k]), 2),
@@ -677,7 +678,7 @@ def measure_workload(name, wl, ne, steps, warmup, cold):
                    "frac_of_peak": round(b / (us * 1e-6) / 1e9 / peak, 4),
                    "frac_of_8tbs": round(b / (us * 1e-6) / 1e9 / 8000.0, 4),
                    "tokens_per_s": round(N / (us * 1e-6), 1)}
-        if k != "step":
+        if k in ("layout", "dispatch", "combine"):
             line[k]["variant"] = h.variant({"layout": 0, "dispatch": 1, "combine": 2}[k])
     h.free()
     del recv, scales, y, out, x
@@ -693,6 +694,7 @@ def run_all_configs(args):
       layout    the layout alone;
       dispatch  the dispatch alone (on the layout just computed);
       combine   the combine alone (on the rows just dispatched, or y);
+      layout_dispatch  layout -> dispatch back to back (dispatch with its layout);
       step      layout -> dispatch -> combine back to back, events only at its
                 two ends, so that the kernels' programmatic dependent launch
                 (each scheduled while its predecessor drains) is counted.

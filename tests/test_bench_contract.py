@@ -74,7 +74,7 @@ def test_library_arm_line():
     # the decode workload measured beside the step (context for the small-batch shape)
     dw = d["decode_workload"]
     assert dw["workload"] == "decode" and dw["tokens"] == 1024
-    for k in ("layout", "dispatch", "combine", "step"):
+    for k in ("layout", "dispatch", "combine", "layout_dispatch", "step"):
         assert dw[k]["us_median"] > 0 and dw[k]["gbs"] > 0
     assert dw["layout"]["variant"].startswith("ep_layout_")
 
