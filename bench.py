@@ -829,7 +829,7 @@ extern "C" int mix_reduce8(const void* big, void* out, int n, int row, void* s) 
 
 def run_mix_ceilings(args):
     """What the memory system gives the data kernels' byte mixes on the prefill
-    shape (32768 tokens, rows of 7168 bf16 = 14336 bytes, top-8): probe kernels
+    shape (32768 tokens, or --tokens; rows of 7168 bf16 = 14336 bytes, top-8): probe kernels
     (MIX_PROBE_CU, compiled here with nvcc) that move the same bytes as the data
     kernels with no routing, each timed in its own region after the same L2
     flush and GPU sleep as --all-configs:
@@ -860,7 +860,7 @@ def run_mix_ceilings(args):
     cold = ColdRegions(dev)
     s = cold.stream
     sp = ctypes.c_void_p(s.cuda_stream)
-    N, K, H = 32768, 8, 7168
+    N, K, H = args.tokens or 32768, 8, 7168
     row = H * 2
     big = torch.empty(N * K * row, dtype=torch.uint8, device=dev)
     x = torch.randint(0, 255, (N * row,), dtype=torch.uint8, device=dev)
@@ -1026,7 +1026,7 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-block", type=int, default=256)
     ap.add_argument("--tokens", type=int, default=None,
-                    help="tokens of a smaller case of the prefill shape (profiling only)")
+                    help="tokens of a smaller case of the prefill shape (profiling, --mix-ceilings)")
     ap.add_argument("--all-configs", action="store_true",
                     help="time layout / dispatch / combine on every workload (one line each)")
     ap.add_argument("--workload", default=None,
