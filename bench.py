@@ -441,9 +441,9 @@ def run_ours(args, rank, local_rank, world):
         d = measure_workload("decode", synth.WORKLOADS["decode"], False, 50, 5, ColdRegions(dev))
         decode = {k: d[k] for k in ("workload", "tokens", "hidden", "experts", "topk", "l2", "timing",
                                     "steps")}
-        for k in ("layout", "dispatch", "combine", "step"):
+        for k in ("layout", "dispatch", "combine", "layout_dispatch", "step"):
             keep = ("us_median", "gbs", "frac_of_8tbs", "frac_of_peak", "tokens_per_s")
-            decode[k] = {kk: d[k][kk] for kk in keep + (("variant",) if k != "step" else ())}
+            decode[k] = {kk: d[k][kk] for kk in keep + (("variant",) if "variant" in d[k] else ())}
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(wl, topk_cpu, w_cpu, x, budget_s=args.cpu_seconds)
