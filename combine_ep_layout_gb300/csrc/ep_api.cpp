@@ -120,7 +120,8 @@ struct ep_handle {
   std::string layout_ran;  // kernel name of the last ep_layout (cluster, fused or three launches)
   Variant<DispatchLaunch> dispatch{};
   Variant<CombineLaunch> combine{};
-  LaunchGeom g_layout{}, g_dispatch{}, g_combine{};
+  Variant<CombineLaunch> combine_tma{};   // EP_GB300_COMBINE_TMA=1: rows staged by TMA (bf16 out, no bias)
+  LaunchGeom g_layout{}, g_dispatch{}, g_combine{}, g_combine_tma{};
   uint64_t wait_ns = kDefaultWaitNs;  // bound of a device-side wait (EP_GB300_WAIT_NS)
   // run-time specialisations for shapes outside the compiled table (function
   // null when not used); they serve 32-byte-aligned buffers, the compiled
@@ -233,6 +234,13 @@ int create_handle(const ep_cfg_t* cfg, ep_handle* src, ep_handle_t* out) {
       return bail(fail(EP_EUNSUPPORTED, "dispatch kernel does not fit on an SM for this hidden_dim"));
     if ((e = h->combine.prepare(h->H, h->K, 0, &h->g_combine)) != cudaSuccess)
       return bail(fail_cuda(e, "combine kernel set-up"));
+    if (CombineTmaRequested()) {  // expert rows staged through shared memory by TMA bulk copies
+      h->combine_tma = FindCombineTma(h->H, h->K, cfg->use_weights != 0);
+      h->g_combine_tma.num_sms = sms;
+      if (h->combine_tma.launch &&
+          (e = h->combine_tma.prepare(h->H, h->K, 0, &h->g_combine_tma)) != cudaSuccess)
+        return bail(fail_cuda(e, "TMA combine kernel set-up"));
+    }
     // shapes outside the compiled table: specialise at run time when possible;
     // when not (no NVRTC, switched off), the compiled generic variants serve
     if (jit::Enabled()) {
@@ -472,11 +480,16 @@ int ep_combine_ex(ep_handle_t h, const void* y, const float* topk_weights, const
     p.hidden = h->H;
     p.topk = h->K;
     p.out_f32 = out_dtype == EP_FP32 ? 1 : 0;
+    p.err = o->err;
+    p.wait_ns = h->wait_ns;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    // the TMA combine (EP_GB300_COMBINE_TMA=1) serves the plain bf16 combine
+    const bool tma_ok = h->combine_tma.launch && !bias && p.out_f32 == 0;
     const bool jit_ok = h->jit_combine.function && !bias && p.out_f32 == 0 && aligned32(y) &&
                         aligned32(out);
-    cudaError_t e = jit_ok ? jit::Launch(h->jit_combine, p.num_tokens, &p, s)
-                           : h->combine.launch(p, h->g_combine, s);
+    cudaError_t e = tma_ok   ? h->combine_tma.launch(p, h->g_combine_tma, s)
+                    : jit_ok ? jit::Launch(h->jit_combine, p.num_tokens, &p, s)
+                             : h->combine.launch(p, h->g_combine, s);
     if (e != cudaSuccess) return fail_cuda(e, "combine launch");
     h->last_stream = s;
     h->launched = true;
@@ -563,8 +576,9 @@ int ep_handle_variant(ep_handle_t h, int32_t step, char* buf, int32_t len) noexc
     const char* name = step == 0 ? (o->layout_ran.empty() ? o->layout.name : o->layout_ran.c_str())
                      : step == 1 ? (h->jit_dispatch.function ? h->jit_dispatch.name.c_str()
                                                              : h->dispatch.name)
-                     : step == 2 ? (h->jit_combine.function ? h->jit_combine.name.c_str()
-                                                            : h->combine.name)
+                     : step == 2 ? (h->combine_tma.launch ? h->combine_tma.name
+                                    : h->jit_combine.function ? h->jit_combine.name.c_str()
+                                                              : h->combine.name)
                                  : nullptr;
     if (!name) return fail(EP_EINVAL, "step must be 0, 1 or 2");
     std::snprintf(buf, static_cast<size_t>(len), "%s", name);

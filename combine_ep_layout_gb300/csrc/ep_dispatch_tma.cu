@@ -25,78 +25,15 @@
 #include "ep_cfg.hpp"
 #include "ep_dispatch_body.cuh"
 #include "ep_kernels.hpp"
+#include "ep_tma.cuh"
 
 namespace epg {
 namespace {
 
 constexpr int kTmaMaxStages = 4;
 constexpr size_t kTmaSmemLimit = 227 * 1024;      // dynamic shared memory a CTA may opt into
-constexpr uint64_t kTmaDrainNs = 2000000000ull;  // bound of the clean-up waits after a timeout
 
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ uint64_t global_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-}
-
-// Non-blocking test of the phase with the given parity.
-__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-// Wait for the phase with the given parity for at most limit_ns; false on
-// timeout.  A limit of 0 gives up at the first test that finds the phase open.
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
-  if (mbar_test(bar, parity)) return true;
-  if (limit_ns == 0) return false;
-  const uint64_t t0 = global_ns();
-  while (global_ns() - t0 <= limit_ns) {
-    if (mbar_test(bar, parity)) return true;
-    __nanosleep(64);
-  }
-  return false;
-}
-
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-      "l"(src), "r"(bytes), "r"(bar)
-      : "memory");
-}
-
-__device__ __forceinline__ void bulk_store(void* dst, uint32_t src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src), "r"(bytes)
-               : "memory");
-}
-
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-
-// All but the newest `n` bulk groups have finished reading shared memory.
-template <int N>
-__device__ __forceinline__ void bulk_wait_read() {
-  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
-}
-
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+using namespace tma;
 
 constexpr uint32_t AlignRow(uint32_t row) { return (row + 127u) & ~127u; }
 
@@ -126,7 +63,7 @@ __global__ void __launch_bounds__(32, 1) ep_dispatch_tma_kernel(DispatchParams p
   if (n <= 0) return;
   if (lane == 0) {
     for (int s = 0; s < S; ++s) mbar_init(bars + 8 * s, 1);
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    mbar_init_fence();
   }
   __syncwarp();
   allow_dependent_grids();
@@ -179,7 +116,7 @@ __global__ void __launch_bounds__(32, 1) ep_dispatch_tma_kernel(DispatchParams p
       atomicOr(p.err, kErrTimeout);
       // no load may still be writing into this CTA's shared memory when it exits
       for (int jj = j; jj < issued; ++jj)
-        mbar_wait_bounded(bars + 8 * (jj % S), static_cast<uint32_t>(jj / S) & 1u, kTmaDrainNs);
+        mbar_wait_bounded(bars + 8 * (jj % S), static_cast<uint32_t>(jj / S) & 1u, kDrainNs);
     }
     __syncwarp();
   }

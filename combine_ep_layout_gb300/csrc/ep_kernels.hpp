@@ -129,6 +129,11 @@ bool DispatchTmaRequested();
 // Bound of a device-side wait in ns: EP_GB300_WAIT_NS, else kDefaultWaitNs.
 uint64_t WaitLimitNs();
 Variant<CombineLaunch> FindCombine(int hidden, int topk, bool use_weights);
+// The combine that stages the K expert rows of a token through shared memory
+// with TMA bulk copies (bf16 output, no bias; null launch when the row cannot
+// be cut into 16-byte pieces), requested by EP_GB300_COMBINE_TMA=1.
+Variant<CombineLaunch> FindCombineTma(int hidden, int topk, bool use_weights);
+bool CombineTmaRequested();
 
 // int32 words of layout scratch for up to max_chunks chunks and `columns` = E+W
 // columns: [chunk_hist] [chunk_hist_cols] [chunk_off], each columns x max_chunks,

@@ -101,6 +101,8 @@ struct CombineParams {
   int hidden;
   int topk;
   int out_f32;               // 1: fp32 output, 0: bf16
+  int32_t* err;              // device error word (the TMA combine's timeouts)
+  uint64_t wait_ns;          // bound of one wait on the TMA combine's mbarrier
 };
 
 }  // namespace epg
