@@ -208,7 +208,10 @@ int ep_dispatch_fwd(ep_handle_t h, const void *x, void *recv_x, float *recv_scal
  *   out[t][c] = bf16 round-to-nearest-even(acc).
  * Non-expand layout: acc = +0.0f; acc = acc + y[send_slot[t][j]][c] for the
  * token's rows in ascending order (ascending rank); no weights.
- * Padding rows of y are never read.  Buffers must be 16-byte aligned. */
+ * Padding rows of y are never read.  Buffers must be 16-byte aligned.  With
+ * EP_GB300_COMBINE_TMA=1 set when the handle was created, the rows are staged
+ * in shared memory by TMA bulk copies (same result; a wait on those copies is
+ * bounded and reports device error value 2 when it gives up). */
 int ep_combine(ep_handle_t h, const void *y, const float *topk_weights, void *out,
                ep_stream_t stream) EP_NOEXCEPT;
 
@@ -292,7 +295,7 @@ int ep_handle_get(ep_handle_t h, int32_t field, void **dev_ptr, int64_t *numel) 
  * the handle's last layout / dispatch / combine call, and wait for that
  * stream only.  Values: 1 (bit 0) = a topk id outside [-1, E) was skipped;
  * 2 (bit 1) = a kernel gave up a bounded wait (the layout's grid barrier, the
- * TMA dispatch's copies).  Returns EP_ECUDA if the
+ * TMA dispatch's or TMA combine's copies).  Returns EP_ECUDA if the
  * copy or the synchronisation fails. */
 int ep_handle_status(ep_handle_t h, int32_t *device_error) EP_NOEXCEPT;
 
