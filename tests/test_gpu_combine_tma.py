@@ -1,10 +1,10 @@
 """The TMA combine (EP_GB300_COMBINE_TMA=1: each token's K expert rows staged in
 shared memory by bulk copies, piece by piece) against the CPU oracle, bit for
 bit: the same fixed fma order as the register combine.  Cases: every workload
-shape with and without weights, masked entries, the top-k edge cases (1, 5,
-16) and the whole 32768-token prefill batch.  A wait limit of 0 makes the
-copies' wait give up: the kernel reports device error value 2 (bit 1), stores
-nothing and leaves the context usable."""
+shape with and without weights, masked entries, the non-expand layout, the
+top-k edge cases (1, 5, 16) and the whole 32768-token prefill batch.  A wait
+limit of 0 makes the copies' wait give up: the kernel reports device error
+value 2 (bit 1), stores nothing and leaves the context usable."""
 import numpy as np
 import pytest
 import torch
@@ -106,3 +106,29 @@ def test_tma_combine_wait_limit_gives_up_cleanly(monkeypatch):
     want = oracle.combine(synth.bits16(y2), ref2["dst_slot"], w2.numpy())
     assert_combine_close(synth.bits16(out2), want)
     assert h2.status() == 0
+
+
+@pytest.mark.parametrize("name", ["tiny", "decode", "skewed"])
+def test_tma_combine_nonexpand(name):
+    """The non-expand layout (one row per (token, destination rank), unweighted):
+    the token's rows in ascending rank order, 5% of the entries masked."""
+    wl = synth.WORKLOADS[name]
+    topk = synth.gen_topk(wl, mask_frac=0.05)
+    ref = oracle.layout_nonexpand(topk.numpy(), wl.world_size, wl.max_tok_per_rank,
+                                  wl.num_expert_per_rank, wl.alignment)
+    R = ref["rcap"]
+    valid = np.zeros(R, bool)
+    valid[:ref["num_recv"]] = True
+    y = synth.gen_bf16_normal(R, wl.hidden, seed=wl.seed * 16 + 3, device="cuda")
+    y[torch.from_numpy(~valid).cuda()] = float("nan")      # rows nobody sends must not be read
+    h = ep.EpHandle(ep.make_cfg(wl.world_size, wl.hidden, wl.max_tok_per_rank,
+                                wl.num_expert_per_rank, wl.topk, wl.alignment, "bf16", False,
+                                no_expand=True))
+    h.layout(topk.cuda())
+    out = torch.full((wl.num_tokens, wl.hidden), -1, dtype=torch.bfloat16, device="cuda")
+    h.combine(y, None, out)
+    torch.cuda.synchronize()
+    check_served_by_tma(h)
+    want = oracle.combine_ex(synth.bits16(y), ref["send_slot"], None, None, "bf16")
+    assert np.array_equal(synth.bits16(out), want)
+    assert h.status() == 0
