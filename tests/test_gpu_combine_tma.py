@@ -132,3 +132,33 @@ def test_tma_combine_nonexpand(name):
     want = oracle.combine_ex(synth.bits16(y), ref["send_slot"], None, None, "bf16")
     assert np.array_equal(synth.bits16(out), want)
     assert h.status() == 0
+
+
+@pytest.mark.parametrize("kernel", ["register", "tma"])
+def test_combine_tokens_with_every_entry_masked(monkeypatch, kernel):
+    """Tokens whose K entries are all -1 fold nothing: their output is bf16 +0
+    (the fold starts at +0.0f), on both combine kernels; a partly masked token
+    folds only its routed rows."""
+    monkeypatch.setenv("EP_GB300_COMBINE_TMA", "1" if kernel == "tma" else "0")
+    wl = synth.WORKLOADS["decode"]
+    topk = synth.gen_topk(wl)
+    for t in (0, 5, 17, wl.num_tokens - 1):
+        topk[t] = -1
+    topk[3, ::2] = -1
+    ref = oracle.layout(topk.numpy(), wl.world_size, wl.max_tok_per_rank, wl.num_expert_per_rank,
+                        wl.alignment)
+    y = synth.gen_y(wl, valid_rows=ref["meta"][:, 0] >= 0, device="cuda")
+    w = synth.gen_weights(wl)
+    h = ep.EpHandle(ep.make_cfg(wl.world_size, wl.hidden, wl.max_tok_per_rank,
+                                wl.num_expert_per_rank, wl.topk, wl.alignment, "bf16", True))
+    h.layout(topk.cuda())
+    out = torch.full((wl.num_tokens, wl.hidden), -1, dtype=torch.bfloat16, device="cuda")
+    h.combine(y, w.cuda(), out)
+    torch.cuda.synchronize()
+    assert h.variant(2).startswith("ep_combine_tma") == (kernel == "tma"), h.variant(2)
+    got = synth.bits16(out)
+    want = oracle.combine(synth.bits16(y), ref["dst_slot"], w.numpy())
+    assert np.array_equal(got, want)
+    for t in (0, 5, 17, wl.num_tokens - 1):
+        assert not got[t].any()
+    assert h.status() == 0
