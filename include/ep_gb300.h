@@ -30,6 +30,11 @@
  *     stream is being captured into a CUDA graph.
  *   - Return value 0 on success, else one of the negative EP_E* codes, with
  *     a message available from ep_last_error() on the calling thread.
+ *   - One handle holds one routing (its fields, and the barrier state of the
+ *     single-launch layout): the caller orders the work it enqueues on one
+ *     handle (one stream, or events between streams), as it would for any
+ *     buffer two kernels write.  Different handles are independent and may
+ *     run at the same time on different streams.
  */
 #ifndef EP_GB300_H
 #define EP_GB300_H
