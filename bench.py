@@ -434,16 +434,23 @@ def run_ours(args, rank, local_rank, world):
 
     e2e = run_e2e(args, ep, torch, dev, wl, topk_cpu, w_cpu, x, (h16, h8), (recv, recv8, scales),
                   step_bytes, world) if not args.no_e2e else None
-    # the decode workload (1024 tokens, the pages' small-batch shape), measured
-    # after the timed region as --all-configs measures it: context, not `value`
-    decode = None
-    if not args.no_decode:
-        d = measure_workload("decode", synth.WORKLOADS["decode"], False, 50, 5, ColdRegions(dev))
-        decode = {k: d[k] for k in ("workload", "tokens", "hidden", "experts", "topk", "l2", "timing",
-                                    "steps")}
+    # the other workloads (decode: 1024 tokens, the pages' small-batch shape;
+    # tiny; skewed Zipf routing), each measured after the timed region as
+    # --all-configs measures it: context, not `value`
+    def summary(name):
+        d = measure_workload(name, synth.WORKLOADS[name], False, 50, 5, cold)
+        out = {k: d[k] for k in ("workload", "tokens", "hidden", "experts", "topk", "l2", "timing",
+                                 "steps")}
         for k in ("layout", "dispatch", "combine", "layout_dispatch", "step"):
             keep = ("us_median", "gbs", "frac_of_8tbs", "frac_of_peak", "tokens_per_s")
-            decode[k] = {kk: d[k][kk] for kk in keep + (("variant",) if "variant" in d[k] else ())}
+            out[k] = {kk: d[k][kk] for kk in keep + (("variant",) if "variant" in d[k] else ())}
+        return out
+    decode, others = None, None
+    if not args.no_decode:
+        cold = ColdRegions(dev)
+        decode = summary("decode")
+        others = {name: summary(name) for name in ("tiny", "skewed")}
+        del cold
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(wl, topk_cpu, w_cpu, x, budget_s=args.cpu_seconds)
@@ -469,6 +476,7 @@ def run_ours(args, rank, local_rank, world):
         "e2e": e2e,
         "cpu_baseline": cpu,
         "decode_workload": decode,
+        "other_workloads": others,
     }
     return line
 
@@ -1022,7 +1030,7 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true",
-                    help="skip the decode-workload measurement added to the step line")
+                    help="skip the decode, tiny and skewed measurements added to the step line")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-block", type=int, default=256)
     ap.add_argument("--tokens", type=int, default=None,

@@ -77,6 +77,10 @@ def test_library_arm_line():
     for k in ("layout", "dispatch", "combine", "layout_dispatch", "step"):
         assert dw[k]["us_median"] > 0 and dw[k]["gbs"] > 0
     assert dw["layout"]["variant"].startswith("ep_layout_")
+    ow = d["other_workloads"]
+    assert set(ow) == {"tiny", "skewed"}
+    for name, w in ow.items():
+        assert w["workload"] == name and w["step"]["us_median"] > 0 and w["combine"]["gbs"] > 0
 
 
 def test_mix_probe_kernels_compile(tmp_path):
