@@ -111,9 +111,14 @@ def kernel_source_digest(kernel):
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(kernel):
-    """DRAM bytes per launch of `kernel` from the committed ncu summary, or None
-    when the summary is missing or was taken on other kernel sources."""
+# The record's DRAM bytes are per launch of the 32768-token prefill batch.
+TRAFFIC_TOKENS = 32768
+
+
+def ncu_traffic(kernel, tokens=TRAFFIC_TOKENS):
+    """DRAM bytes of one launch of `kernel` on `tokens` tokens of the prefill
+    shape, from the committed ncu summary (scaled by the tokens processed), or
+    None when the summary is missing or was taken on other kernel sources."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     try:
         with open(path) as f:
@@ -122,7 +127,7 @@ def ncu_traffic(kernel):
         return None
     if k is None or k.get("source_digest") != kernel_source_digest(kernel):
         return None
-    return k.get("dram_bytes_per_launch")
+    return int(round(k["dram_bytes_per_launch"] * tokens / TRAFFIC_TOKENS))
 
 
 # NVML clock-event reason bits (nvml.h, nvmlClocksEventReason*) reported by name
@@ -427,9 +432,16 @@ def run_ours(args, rank, local_rank, world):
     dom = max(["dispatch_bf16", "combine", "dispatch_fp8"], key=lambda n: avg[n])
     kname = {"dispatch_bf16": "ep_dispatch_copy_kernel", "combine": "ep_combine_kernel",
              "dispatch_fp8": "ep_dispatch_fp8_kernel"}[dom]
-    roof = {"bound": "hbm", "kernel": dom, "achieved": kernels[dom]["gbs"], "peak": peak,
-            "peak_kind": peak_kind + " hbm_gbs (burst copy)", "unit": "GB/s",
-            "frac": kernels[dom]["frac_of_peak"], "traffic": ncu_traffic(kname),
+    variant = {"dispatch_bf16": h16.variant(1), "combine": h16.variant(2),
+               "dispatch_fp8": h8.variant(1)}[dom]
+    # the record holds the compiled register kernels' counters: none for the
+    # TMA-staged or run-time specialised variants
+    compiled = variant.startswith({"dispatch_bf16": "ep_dispatch_bf16_h", "combine": "ep_combine_w_h",
+                                   "dispatch_fp8": "ep_dispatch_fp8_h"}[dom])
+    roof = {"bound": "hbm", "kernel": dom, "variant": variant, "achieved": kernels[dom]["gbs"],
+            "peak": peak, "peak_kind": peak_kind + " hbm_gbs (burst copy)", "unit": "GB/s",
+            "frac": kernels[dom]["frac_of_peak"],
+            "traffic": ncu_traffic(kname, N) if compiled else None,
             "algorithmic_bytes": nbytes[dom]}
 
     e2e = run_e2e(args, ep, torch, dev, wl, topk_cpu, w_cpu, x, (h16, h8), (recv, recv8, scales),
