@@ -10,13 +10,13 @@
 // P the smallest power of two for which the K pieces of one token take at most
 // kCombineTmaStageBytes of shared memory, so that many CTAs per SM keep their
 // copies in flight while others fold.  Thread 0 issues one bulk copy per
-// routed entry (its piece of that expert row), all completing on one mbarrier;
-// every thread waits on it, bounded by %globaltimer (CombineParams::wait_ns),
-// then folds the K pieces from shared memory in k order with the register
-// combine's arithmetic (fp32 fmaf from +0, masked entries skipped, bf16 round
-// to nearest even) and stores its 16-byte output vectors.  A CTA whose wait
-// gives up records kErrTimeout (value 2) in the device error word, lets its
-// copies land (again bounded) and stores nothing.
+// routed entry (its piece of that expert row), all completing on one
+// mbarrier, and waits on it, bounded by %globaltimer (CombineParams::wait_ns);
+// after a block barrier every thread folds the K pieces from shared memory in
+// k order with the register combine's arithmetic (fp32 fmaf from +0, masked
+// entries skipped, bf16 round to nearest even) and stores its 16-byte output
+// vectors.  A CTA whose wait gives up records kErrTimeout (value 2) in the
+// device error word, lets its copies land (again bounded) and stores nothing.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -82,7 +82,9 @@ __global__ void __launch_bounds__(kCombineTmaThreads) ep_combine_tma_kernel(Comb
         bulk_load(smem_u32(stage + k * piece), y + static_cast<int64_t>(slot_s[k]) * row,
                   static_cast<uint32_t>(piece), bar);
   }
-  const bool ok = mbar_wait_bounded(bar, 0, p.wait_ns);
+  // thread 0 waits for the copies; the block barrier then orders every
+  // thread's reads of the staged pieces after the copies' completion
+  const bool ok = threadIdx.x != 0 || mbar_wait_bounded(bar, 0, p.wait_ns);
   if (__syncthreads_or(!ok)) {
     if (threadIdx.x == 0) {
       atomicOr(p.err, kErrTimeout);

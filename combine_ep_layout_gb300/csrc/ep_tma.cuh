@@ -46,6 +46,20 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Potentially blocking test of the phase with the given parity: the thread
+// may be suspended in the instruction until the phase completes or a
+// hardware time limit passes (then false).
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Wait for the phase with the given parity for at most limit_ns; false on
 // timeout.  A limit of 0 gives up at the first test that finds the phase open.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
@@ -53,8 +67,7 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
   if (limit_ns == 0) return false;
   const uint64_t t0 = global_ns();
   while (global_ns() - t0 <= limit_ns) {
-    if (mbar_test(bar, parity)) return true;
-    __nanosleep(64);
+    if (mbar_try_wait(bar, parity)) return true;
   }
   return false;
 }
