@@ -33,9 +33,9 @@ namespace {
 using namespace tma;
 
 // 128 threads and at most 16 KB of pieces per CTA (the prefill row of 14336
-// bytes in 8 pieces of 1792): measured best of 64 / 128 threads and 4-120 KB
-// per CTA (prefill combine 618 us at 16 KB, 660 at 32 KB, 754 at 64 KB and
-// at whole rows, 897 at 8 KB; 64 threads: 635 at 16 KB, 647 at 8 KB).
+// bytes in 8 pieces of 1792): measured best of 64 / 128 / 256 threads and
+// 4-120 KB per CTA (prefill combine 606 us at 16 KB, 647 at 32 KB, 762 at
+// 8 KB; 256 threads: 761 at 16 KB, 614 at 32 KB).
 constexpr int kCombineTmaThreads = 128;
 constexpr int kCombineTmaStageBytes = 16 * 1024;
 
