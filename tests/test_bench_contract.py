@@ -112,3 +112,25 @@ def test_mix_ceilings_line():
     assert set(d["cases"]) == {"write_only", "read_only", "copy_1to1", "bcast_1to8", "reduce_8to1"}
     for c in d["cases"].values():
         assert c["us_best"] > 0 and c["gbs_best"] >= c["gbs_median"] > 0
+
+
+def test_traffic_record_is_scaled_and_tied_to_the_sources(tmp_path, monkeypatch):
+    """The roofline's DRAM traffic comes from the committed ncu record only while
+    the kernel's sources are the captured ones, and is scaled to the batch that
+    ran (traffic grows with the tokens processed)."""
+    sys.path.insert(0, ROOT)
+    import bench
+    rec = json.load(open(os.path.join(ROOT, "profiles", "ncu_traffic.json")))
+    for name, k in rec["kernels"].items():
+        full = bench.ncu_traffic(name)
+        if full is None:      # sources changed since the capture: nothing to check
+            continue
+        assert full == k["dram_bytes_per_launch"]
+        assert bench.ncu_traffic(name, bench.TRAFFIC_TOKENS // 2) == round(full / 2)
+    # a record taken on other sources gives no traffic
+    fake = dict(rec, kernels={n: dict(k, source_digest="0" * 16) for n, k in rec["kernels"].items()})
+    (tmp_path / "profiles").mkdir()
+    (tmp_path / "profiles" / "ncu_traffic.json").write_text(json.dumps(fake))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setattr(bench, "kernel_source_digest", lambda kernel: "f" * 16)
+    assert all(bench.ncu_traffic(n) is None for n in rec["kernels"])
