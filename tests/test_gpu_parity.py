@@ -397,16 +397,21 @@ def test_identity_round_trip_prefill():
     assert torch.equal(out.view(torch.int16), want.view(torch.int16))
 
 
-@pytest.mark.parametrize("path", LAYOUT_PATHS)
-def test_graph_capture_replay(path, monkeypatch):
+@pytest.mark.parametrize("path,tma", [(p, False) for p in LAYOUT_PATHS] + [("cluster", True)])
+def test_graph_capture_replay(path, tma, monkeypatch):
     """layout -> dispatch -> identity expert -> combine (and an FP8 dispatch on
     the same layout) captured once in a CUDA graph and replayed with new
     routings written into the same input buffers ("MORI JIT v2" §4: the step
     must replay correctly, no host-side state frozen).  The kernels after the
     first are launched with programmatic stream serialisation, so each replay
     also checks that no kernel reads a predecessor's output before it is
-    complete, nor a stale copy of the previous replay's."""
+    complete, nor a stale copy of the previous replay's.  tma: the bf16
+    dispatch and the combine are the TMA-staged variants (mbarriers in the
+    captured kernels)."""
     set_layout_path(monkeypatch, path)
+    if tma:
+        monkeypatch.setenv("EP_GB300_DISPATCH_TMA", "1")
+        monkeypatch.setenv("EP_GB300_COMBINE_TMA", "1")
     wl = synth.WORKLOADS["decode"]
     h = ep.EpHandle(cfg_of(wl))
     h8 = ep.EpHandle(cfg_of(wl, "fp8"), layout_of=h)
@@ -429,6 +434,7 @@ def test_graph_capture_replay(path, monkeypatch):
         h.combine(recv, w_buf, out, stream=s)
         h8.dispatch(x_buf, rq, rs, stream=s)
     assert ran_path(h.variant(0)) == path, h.variant(0)
+    assert ("tma" in h.variant(1) and "tma" in h.variant(2)) == tma, (h.variant(1), h.variant(2))
     for seed in range(4):
         c = synth.make_case(wl.with_(seed=0x1000 + seed), device="cuda")
         topk_buf.copy_(c["topk_idx"])
